@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Decode-step attention benchmark for GraniKV's HOT/COLD KV cache on GB300.
+
+Metric: decode-attention query-tokens/s (one decode query token per request per layer) on
+the Llama-3.1-8B attention shape with one shared prefix of L_p = 16384 tokens, B = 64
+requests and log-normal suffixes (median 300), plus the achieved fraction of the HBM
+roofline of the decode-attention launches.
+
+A step is one pass of the whole path over one batch: COLD slot allocation for one new token
+per request, the scatter of each layer's new K/V into the COLD pool, the per-step dispatch,
+and decode attention (prefix partial, suffix partial, log-sum-exp merge) for every layer.
+Each layer has its own K/V pools, so one step touches far more memory than the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--layers L] [--impl granikv|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica (request-level data
+parallelism, no collective on the data path); rank 0 prints one JSON line with the whole-job
+throughput over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn query-tokens/s at L_p=16K on 1 GB300; % HBM / tensor roofline"
+UNIT = "q-tok/s"
+WORKLOAD = "llama8b_single_prefix_16k"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--impl", choices=["granikv", "reference"], default="granikv")
+    ap.add_argument("--backend", choices=["auto", "dense", "cascade"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="rough bound on the CPU-baseline sample's run time")
+    return ap.parse_args(argv)
+
+
+# ---- distributed plumbing (host-side timing reduction only) --------------------------------
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a host scalar over all ranks (no-op for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- accounting -----------------------------------------------------------------------------
+
+def algorithmic_bytes(spec, slab_ids, seq_lens, esize: int) -> int:
+    """Bytes one decode-attention call must move at minimum: each HOT prefix's K and V once,
+    every COLD token's K and V plus its 4-byte table entry, q and o once, lse once."""
+    row = spec.n_kv * spec.d * esize
+    prefixes = {s for s in slab_ids if s >= 0}
+    lp_of = {}
+    for b, s in enumerate(slab_ids):
+        if s >= 0:
+            lp_of[s] = spec.prefix_lens[spec.req_prefix[b]]
+    prefix = sum(2 * lp_of[s] * row for s in prefixes)
+    cold = sum(2 * L * row + 4 * L for L in seq_lens)
+    B = len(seq_lens)
+    qo = 2 * B * spec.n_q * spec.d * esize + 4 * B * spec.n_q
+    return prefix + cold + qo
+
+
+def algorithmic_flops(spec, slab_ids, seq_lens) -> int:
+    tot = 0
+    for b, s in enumerate(slab_ids):
+        lp = spec.prefix_lens[spec.req_prefix[b]] if s >= 0 else 0
+        tot += 4 * spec.d * spec.n_q * (lp + seq_lens[b])
+    return tot
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shared_prefix_kv_decode_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload, if it
+    was taken on the current sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    digest = None
+    traffic = None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("source_digest:"):
+                digest = line.split(":", 1)[1].strip()
+            if line.startswith("dram_bytes_per_launch:"):
+                try:
+                    traffic = float(line.split(":", 1)[1].strip())
+                except ValueError:
+                    traffic = None
+    if digest != source_digest():
+        return None
+    return traffic
+
+
+# ---- clocks ------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join("/tmp", f"granikv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        all_rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    all_rows.append(parts)
+        rows = [r for r in all_rows if self.uuid and self.uuid in r[0]]
+        if not rows and len({r[0] for r in all_rows}) == 1:
+            rows = all_rows
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        busy = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---- CPU baseline (the oracle, as it stands) -------------------------------------------------
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl, requests):
+    import oracle.attention as OA
+    t = time.perf_counter()
+    for b in requests:
+        OA.request_attention(wl, b)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(wl, seconds: float):
+    """Time the fp64 oracle on a bounded sample of the workload's requests (one layer)."""
+    B = wl.spec.B
+    t1 = oracle_sample(wl, [0])
+    n = max(1, min(B, int(seconds / max(t1, 1e-6))))
+    reqs = list(range(n))
+    t = oracle_sample(wl, reqs)
+    return {"value": n / t, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{n} of {B} requests of {wl.spec.name}, one layer, fp64 numpy oracle "
+                      f"({t:.1f} s; host cores: os.cpu_count()={os.cpu_count()})"}
+
+
+# ---- the reference arm: the oracle on the host cores ----------------------------------------
+
+def run_reference(args):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return 0
+    import workloads as W
+    wl = W.llama8b_single_prefix_16k(seed=0)
+    per_step = 2
+    B = wl.spec.B
+    for i in range(args.warmup):
+        oracle_sample(wl, [(i * per_step + k) % B for k in range(per_step)])
+    times = []
+    for i in range(args.steps):
+        times.append(oracle_sample(wl, [((args.warmup + i) * per_step + k) % B for k in range(per_step)]))
+    t = sum(times)
+    value = per_step * args.steps / t
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD, "n_q": 32, "n_kv": 8, "head_dim": 128, "L_p": 16384,
+                       "B": B, "sample_per_step": f"{per_step} requests, one layer"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"{per_step} requests per step of {wl.spec.name}, one layer"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the GraniKV arm -------------------------------------------------------------------------
+
+def run_granikv(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import workloads as W
+    from shared_prefix_kv_decode_gb300 import _binding as gb
+    from shared_prefix_kv_decode_gb300.workload_io import load_workload
+
+    L = args.layers
+    steps_total = args.warmup + args.steps
+    e2e_steps = max(3, min(args.steps, 10))
+    wl = W.llama8b_single_prefix_16k(seed=rank)
+    spec = wl.spec
+    B = spec.B
+    extra = steps_total + e2e_steps + 8
+    cap = max(wl.cold_len(b) for b in range(B)) + extra + 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+
+    def layer_fill(layer, shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    lw = load_workload(wl, n_layers=L, device=dev.index, cap=cap, layer_fill=layer_fill)
+    cache = lw.cache
+    ctx = cache.ctx
+    ctx.force_backend({"auto": gb.BACKEND_AUTO, "dense": gb.BACKEND_DENSE,
+                       "cascade": gb.BACKEND_CASCADE}[args.backend])
+    ctx.set_checks(True)
+    stream = torch.cuda.current_stream(dev)
+    qs = [lw.q] + [(torch.randn((B, spec.n_q, spec.d), generator=gen, device=dev) / math.sqrt(spec.d)
+                    ).to(torch.bfloat16) for _ in range(L - 1)]
+    knew = [torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    vnew = [torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    outs = [torch.empty((B, spec.n_q, spec.d), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    lses = [torch.empty((B, spec.n_q), dtype=torch.float32, device=dev) for _ in range(L)]
+    slots = torch.empty((B,), dtype=torch.int32, device=dev)
+    plan = ctx.plan()
+    slab_ids = lw.slab_ids
+    seq = list(cache.seq_len_host[:B])
+    # workspace sized for the largest plan of the run (suffixes grow by one token per step)
+    probe = gb.Batch(slab_ids, [x + extra for x in seq], cache.req_to_slot, cache.cap)
+    ws_bytes = ctx.workspace_size(ctx.dispatch(probe, plan))
+    ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+    ones = [1] * B
+    ev_pairs = []
+    timed_bytes = []
+
+    def step(record):
+        ctx.cold_alloc(ones, cache.req_to_slot, cache.suffix_len, cache.cap, slots, stream)
+        for i in range(B):
+            seq[i] += 1
+        for layer in range(L):
+            ctx.cold_append(layer, knew[layer], vnew[layer], slots, B, stream)
+        batch = gb.Batch(slab_ids, seq, cache.req_to_slot, cache.cap)
+        ctx.dispatch(batch, plan)
+        nbytes = algorithmic_bytes(spec, slab_ids, seq, 2)
+        for layer in range(L):
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            ctx.decode_attention(layer, qs[layer], batch, plan, outs[layer], lses[layer], ws, ws_bytes, stream)
+            if record:
+                e1.record(stream)
+                ev_pairs.append((e0, e1))
+                timed_bytes.append(nbytes)
+        return batch
+
+    for _ in range(args.warmup):
+        step(False)
+    ctx.sync_status(stream)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(uuid)
+    k0, c0 = ctx.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    k1, c1 = ctx.launch_count()
+    ctx.sync_status(stream)
+    t_local = t_start.elapsed_time(t_end) / 1000.0
+    t_max = max_over_ranks(t_local, world, dev)
+    value = world * B * L * args.steps / t_max
+    call_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    avg_call_s = statistics.mean(call_ms) / 1000.0
+    avg_bytes = statistics.mean(timed_bytes)
+
+    # end to end through the C ABI with host buffers: pinned host inputs copied in and the
+    # step's outputs read back inside the timed region, every step
+    q_h = [x.cpu().pin_memory() for x in qs]
+    k_h = [x.cpu().pin_memory() for x in knew]
+    v_h = [x.cpu().pin_memory() for x in vnew]
+    o_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    l_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in lses]
+    h2d = sum(x.numel() * x.element_size() for x in q_h + k_h + v_h)
+    d2h = sum(x.numel() * x.element_size() for x in o_h + l_h)
+
+    def e2e_step():
+        for layer in range(L):
+            qs[layer].copy_(q_h[layer], non_blocking=True)
+            knew[layer].copy_(k_h[layer], non_blocking=True)
+            vnew[layer].copy_(v_h[layer], non_blocking=True)
+        step(False)
+        for layer in range(L):
+            o_h[layer].copy_(outs[layer], non_blocking=True)
+            l_h[layer].copy_(lses[layer], non_blocking=True)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1000.0, world, dev)
+    ctx.sync_status(stream)
+    e2e_value = world * B * L * e2e_steps / t_e2e
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    hbm, tflops, peak_src = read_peaks()
+    achieved = avg_bytes / avg_call_s / 1e9
+    groups = plan.groups()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": profiled_traffic("decode_attention_" + WORKLOAD),
+                "kernel": "granikv_decode_attention launches (prefix + suffix + merge)",
+                "peak_source": f"{peak_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": avg_bytes,
+                "avg_launch_us": avg_call_s * 1e6,
+                "prefix_tflops": algorithmic_flops(spec, slab_ids, seq) / avg_call_s / 1e12}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_q": spec.n_q, "n_kv": spec.n_kv, "head_dim": spec.d,
+                   "L_p": spec.prefix_lens[0], "B": B,
+                   "suffix": "log-normal median 300, sigma 1, clipped [32, 2048]",
+                   "layers_per_step": L, "backend": args.backend,
+                   "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
+                               "n_splits": g["n_splits"]} for g in groups],
+                   "l2": (f"inputs larger than L2: each step reads {L} distinct layers' pools, "
+                          f"{L * avg_bytes / 1e6:.0f} MB > 129 MB L2"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": k1 - k0,
+        "host_copies": c1 - c0,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_granikv(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

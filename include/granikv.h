@@ -1,0 +1,215 @@
+/*
+ * granikv.h -- C ABI of libgranikv: decode-step attention over an asymmetric HOT/COLD KV cache.
+ *
+ * Source of every operation: "GraniKV: Asymmetric Granularity KV-Cache Paging for Multi-Agent
+ * Systems with Long Shared Prefix" (arXiv:2608.15584).  Section names below refer to that
+ * paper's summary page and card page.
+ *
+ * Conventions
+ * -----------
+ *  - Every call returns a granikv_status.  No C++ exception or abort crosses this boundary.
+ *  - The caller owns every device buffer that holds data: the per-layer K/V pools, q, o, lse,
+ *    the per-request token tables, the per-request lengths and the workspace.  Pointers marked
+ *    "device" must be device (or managed) memory of the context's device; "host" pointers
+ *    must be host memory.
+ *  - The library owns the pool metadata: the HOT extent list and slab table (host), the COLD
+ *    free ring (device, allocated by granikv_create), and a device error word.
+ *  - Calls that take a cudaStream_t are stream-ordered and asynchronous.  Errors that only
+ *    the device can see (bounds checks, see granikv_set_checks) are latched in the error word
+ *    and reported by granikv_sync_status.
+ *  - A context is not thread-safe; use one per host thread or serialise calls.
+ *
+ * KV layout
+ * ---------
+ *  Each layer has one K pool and one V pool, each [n_slots, n_kv, head_dim] of the context's
+ *  dtype, row-major (slot stride n_kv*head_dim elements).  Slots [0, n_hot) form the HOT pool
+ *  and [n_hot, n_slots) the COLD pool, n_hot = floor(hot_fraction * n_slots)
+ *  ("Limitations", static HOT/COLD pool fraction f_p, default 0.2).  A slot id means the same
+ *  token position in every layer's pools.
+ */
+#ifndef GRANIKV_H
+#define GRANIKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* granikv_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef int32_t granikv_status;
+enum {
+  GRANIKV_OK = 0,
+  GRANIKV_ERR_INVALID = 1,        /* bad argument or descriptor; nothing was changed        */
+  GRANIKV_ERR_NO_HOT_SPACE = 2,   /* no free HOT extent can hold the prefix (or slab table full) */
+  GRANIKV_ERR_NO_COLD_SPACE = 3,  /* fewer free COLD slots than asked; nothing was popped    */
+  GRANIKV_ERR_CUDA = 4,           /* a CUDA runtime call failed                              */
+  GRANIKV_ERR_DEVICE_CHECK = 5,   /* a kernel's bounds check failed (see granikv_set_checks) */
+  GRANIKV_ERR_UNSUPPORTED = 6,    /* shape or dtype this build has no kernel for             */
+  GRANIKV_ERR_NO_DEVICE = 7       /* the call needs device resources the context lacks       */
+};
+
+enum { GRANIKV_DTYPE_F32 = 0, GRANIKV_DTYPE_BF16 = 1 };
+
+enum {
+  GRANIKV_BACKEND_AUTO = 0,     /* per-group dispatch on M_eff >= M_sat                    */
+  GRANIKV_BACKEND_DENSE = 1,    /* batched-GEMM prefix backend (tensor cores)              */
+  GRANIKV_BACKEND_CASCADE = 2   /* prefix read once per step, bandwidth-bound backend      */
+};
+
+typedef struct granikv_ctx granikv_ctx;
+typedef struct granikv_plan granikv_plan;
+
+typedef struct granikv_config {
+  int32_t n_layers;
+  int32_t n_q;        /* query heads                                   */
+  int32_t n_kv;       /* KV heads; n_q % n_kv == 0                      */
+  int32_t head_dim;   /* d                                             */
+  int32_t dtype;      /* GRANIKV_DTYPE_*: pools, q and o                */
+  int32_t device;     /* CUDA device ordinal                           */
+  int64_t n_slots;    /* slots per pool                                */
+  double hot_fraction;/* f_p in (0, 1); 0 selects the default 0.2       */
+  void* const* k_pool;/* host array [n_layers] of device pointers      */
+  void* const* v_pool;/* host array [n_layers] of device pointers      */
+  const int32_t* cold_init_order; /* host [n_slots - n_hot]: initial COLD free-ring content, a
+                                     permutation of [n_hot, n_slots); NULL = ascending order   */
+  int32_t m_sat;      /* dense iff M_eff >= m_sat; 0 selects the built-in GB300 fit       */
+  int32_t max_slabs;  /* slab table size; 0 selects 1024                                  */
+  int32_t max_batch;  /* largest B of any call; 0 selects 4096                            */
+  int32_t host_only;  /* 1: create no device resources (HOT pool and dispatch only)       */
+} granikv_config;
+
+/* One decode step's batch.  Request b attends over its HOT prefix slab (if slab_id[b] >= 0)
+ * followed by the seq_len[b] tokens listed in req_to_slot[b, 0:seq_len[b]].  A prefix that is
+ * not in HOT is simply the head of that list (the paged fallback). */
+typedef struct granikv_batch {
+  int32_t B;
+  const int32_t* slab_id;     /* host [B]: HOT slab of request b, or -1                   */
+  const int32_t* seq_len;     /* host [B]: tokens of request b in its COLD token table     */
+  const int32_t* req_to_slot; /* device [B, cap] int32: COLD slot of each token, row-major */
+  int32_t cap;                /* row stride of req_to_slot                                 */
+} granikv_batch;
+
+typedef struct granikv_group_info {
+  int32_t slab_id;
+  int32_t n_requests;
+  int32_t m_eff;      /* n_requests * n_q / n_kv                        */
+  int32_t backend;    /* GRANIKV_BACKEND_DENSE or GRANIKV_BACKEND_CASCADE */
+  int32_t L_p;
+  int32_t n_splits;   /* pieces the prefix is split into along L_p      */
+  int64_t slot_offset;
+} granikv_group_info;
+
+/* Text for a status code (static storage). */
+const char* granikv_status_string(granikv_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t granikv_version(void);
+
+/* Create a context.  Allocates the COLD free ring and a few small device buffers with
+ * cudaMalloc on cfg->device (none when host_only).  The pools stay caller-owned.
+ * "3 GraniKV", asymmetric KV-cache paging; "Limitations", static pool fraction. */
+granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out);
+granikv_status granikv_destroy(granikv_ctx* ctx);
+
+/* ---- HOT pool ("B.10 Cross-pool admission and promotion policy"; "B.8 Multi-prefix
+ * sensitivity": first-fit packing of mixed slab sizes; card page: one slab per prefix node).
+ * Host only, no device access. ------------------------------------------------------------- */
+
+/* Reserve a contiguous slab of L_p slots: the lowest-offset free extent that can hold it,
+ * carved from its start.  Returns the lowest unused slab id and the slab's first slot.
+ * GRANIKV_ERR_NO_HOT_SPACE if no extent is large enough or the slab table is full; the caller
+ * then stores the prefix in COLD (admission fallback).  Existing slabs never move. */
+granikv_status granikv_hot_alloc(granikv_ctx* ctx, int32_t L_p, int32_t* slab_id,
+                                 int64_t* slot_offset);
+/* Release a slab; its extent merges with free neighbours. */
+granikv_status granikv_hot_free(granikv_ctx* ctx, int32_t slab_id);
+/* Offset and length of a live slab. */
+granikv_status granikv_hot_info(granikv_ctx* ctx, int32_t slab_id, int64_t* slot_offset,
+                                int32_t* L_p);
+/* Number of HOT slots, and the largest free extent. */
+granikv_status granikv_hot_stats(granikv_ctx* ctx, int64_t* n_hot, int64_t* largest_free);
+/* Copy a prefix's K/V ([L_p, n_kv, head_dim], device, contiguous) into a slab of one layer.
+ * Stream-ordered device-to-device copies; the prefill that produces K/V is outside the path. */
+granikv_status granikv_hot_fill(granikv_ctx* ctx, int32_t layer, int32_t slab_id,
+                                const void* k, const void* v, granikv_stream_t stream);
+
+/* ---- COLD pool ("1 Introduction" and "3 GraniKV": a token-level pool, page size 1, for
+ * suffix and decoded tokens; card page: a token-level free list). ------------------------- */
+
+/* Pop n_new[b] slots for each request b from the free ring, in request order: request b gets
+ * ring entries head + sum(n_new[0:b]) ..., appended to req_to_slot[b, suffix_len[b]:] and
+ * suffix_len[b] += n_new[b].  The popped slots, in the same order, are also written to
+ * slots_out (device [sum n_new], may be NULL) for granikv_cold_append.
+ *   n_new:       host [B], each >= 0
+ *   req_to_slot: device [B, cap] int32;  suffix_len: device [B] int32
+ * All-or-nothing: GRANIKV_ERR_NO_COLD_SPACE (checked on the host, nothing popped) when fewer
+ * slots are free than asked.  A row that would pass cap is a device check failure. */
+granikv_status granikv_cold_alloc(granikv_ctx* ctx, const int32_t* n_new, int32_t B,
+                                  int32_t* req_to_slot, int32_t* suffix_len, int32_t cap,
+                                  int32_t* slots_out, granikv_stream_t stream);
+/* Return n slots (device [n]) to the tail of the free ring, in the given order.
+ * GRANIKV_ERR_INVALID if that would hold more than the pool's size. */
+granikv_status granikv_cold_free(granikv_ctx* ctx, const int32_t* slots, int32_t n,
+                                 granikv_stream_t stream);
+/* Free COLD slots (host mirror of the ring's fill). */
+granikv_status granikv_cold_free_count(granikv_ctx* ctx, int64_t* n_free);
+/* Scatter N new tokens' K/V ([N, n_kv, head_dim] each, device) into one layer's pools at
+ * slots[i] (device [N]).  A slot outside [n_hot, n_slots) is a device check failure. */
+granikv_status granikv_cold_append(granikv_ctx* ctx, int32_t layer, const void* k_new,
+                                   const void* v_new, const int32_t* slots, int32_t N,
+                                   granikv_stream_t stream);
+
+/* ---- per-step dispatch ("3 GraniKV", per-step dispatch; "B.4 Per-Step Dispatch Trace";
+ * "B.8": class-local dense batching).  Host only, no device access. ------------------------ */
+
+granikv_status granikv_plan_create(granikv_ctx* ctx, granikv_plan** out);
+granikv_status granikv_plan_destroy(granikv_plan* plan);
+/* Group the batch's requests by HOT slab, compute M_eff = B_g * n_q / n_kv per group, choose
+ * DENSE iff M_eff >= M_sat (unless a backend is forced), and lay out the step's work: prefix
+ * splits, suffix chunks and partial-state records.  GRANIKV_ERR_INVALID for an unknown slab,
+ * a request with neither prefix nor tokens, seq_len > cap, or B > max_batch. */
+granikv_status granikv_dispatch(granikv_ctx* ctx, const granikv_batch* batch, granikv_plan* plan);
+granikv_status granikv_plan_num_groups(const granikv_plan* plan, int32_t* n_groups);
+granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_group_info* out);
+/* Workspace bytes granikv_decode_attention needs for this plan (256-byte aligned pointer). */
+granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan, size_t* bytes);
+
+granikv_status granikv_set_msat(granikv_ctx* ctx, int32_t m_sat);
+granikv_status granikv_get_msat(granikv_ctx* ctx, int32_t* m_sat);
+granikv_status granikv_force_backend(granikv_ctx* ctx, int32_t backend);
+
+/* ---- decode-step attention ("2 Related Work", prefix-suffix attention: prefix and suffix
+ * partial attentions merged by log-sum-exp; "3 GraniKV", dual attention backends). -------- */
+
+/* o[b, h, :] and lse[b, h] of softmax attention (scale 1/sqrt(head_dim), natural-log lse) of
+ * query q[b, h, :] over request b's HOT prefix slab followed by its COLD tokens, using KV
+ * head h / (n_q / n_kv) of layer `layer`.
+ *   q: device [B, n_q, head_dim] (dtype);  o: device [B, n_q, head_dim] (dtype);
+ *   lse: device [B, n_q] float32;  workspace: device, >= granikv_workspace_size bytes,
+ *   256-byte aligned, not touched by the caller between calls that share a plan.
+ * plan: from granikv_dispatch on this batch; NULL runs the dispatcher into the context's own
+ * plan.  Its work list is copied into the workspace on first use with that workspace. */
+granikv_status granikv_decode_attention(granikv_ctx* ctx, int32_t layer, const void* q,
+                                        const granikv_batch* batch, granikv_plan* plan,
+                                        void* o, float* lse, void* workspace, size_t ws_bytes,
+                                        granikv_stream_t stream);
+
+/* ---- checks -------------------------------------------------------------------------- */
+
+/* 1: kernels bounds-check slot ids, slab ranges and table rows, skip bad accesses and latch
+ * GRANIKV_ERR_DEVICE_CHECK (no trap, no assert).  Default 1 for alloc/append, which are cheap;
+ * the attention kernels check when on. */
+granikv_status granikv_set_checks(granikv_ctx* ctx, int32_t on);
+/* Synchronise the stream and report (and clear) the device error word. */
+granikv_status granikv_sync_status(granikv_ctx* ctx, granikv_stream_t stream);
+/* Kernels (and host-to-device plan or offset copies) this context has enqueued since it was
+ * created: the count a caller uses to attribute device work to the library. */
+granikv_status granikv_launch_count(granikv_ctx* ctx, int64_t* kernels, int64_t* copies);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRANIKV_H */

@@ -1,0 +1,733 @@
+// granikv_host.cpp -- host side of libgranikv: context, HOT first-fit pool, COLD ring
+// bookkeeping, the per-step dispatcher and planner, and the C ABI entry points.
+//
+// GraniKV (arXiv:2608.15584): "3 GraniKV" (asymmetric HOT/COLD paging, dual backends,
+// per-step dispatch), "B.8 Multi-prefix sensitivity" (first-fit packing, class-local dense
+// batching), "B.10 Cross-pool admission and promotion policy" (HOT first, COLD fallback, no
+// demotion).
+#include "../../include/granikv.h"
+#include "internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+using namespace granikv;
+
+namespace {
+
+constexpr int32_t kDefaultMaxSlabs = 1024;
+constexpr int32_t kDefaultMaxBatch = 4096;
+// Dense/cascade crossover on GB300 for the Llama-3.1-8B shape, re-fitted from the L_p x B
+// sweep (the pages' A100 value is 1024 and they state other GPUs need a re-fit).
+constexpr int32_t kDefaultMsat = 1024;
+
+struct Extent {
+  int64_t off, len;
+};
+struct Slab {
+  int64_t off = 0;
+  int32_t len = 0;
+  bool live = false;
+};
+
+}  // namespace
+
+struct granikv_ctx {
+  granikv_config cfg{};
+  std::vector<void*> kpool, vpool;
+  int64_t n_hot = 0, n_cold = 0;
+  int32_t g = 1;
+  // HOT pool: free extents sorted by offset, slab table
+  std::vector<Extent> free_ext;
+  std::vector<Slab> slabs;
+  // COLD ring: entries [head, tail) are free; positions are taken modulo n_cold
+  int64_t head = 0, tail = 0;
+  // device resources
+  int32_t* d_ring = nullptr;
+  int32_t* d_err = nullptr;
+  int32_t* d_stage = nullptr;  // [max_batch + 1] exclusive offsets for cold_alloc
+  int32_t num_sms = 152;
+  int32_t cc_major = 0, cc_minor = 0;
+  // dispatch state
+  int32_t m_sat = kDefaultMsat;
+  int32_t forced = GRANIKV_BACKEND_AUTO;
+  int32_t checks = 1;
+  granikv_plan* own_plan = nullptr;
+  // enqueued work, for attribution
+  int64_t n_kernels = 0, n_copies = 0;
+};
+
+struct granikv_plan {
+  granikv_ctx* ctx = nullptr;
+  std::vector<unsigned char> blob;  // device image of the plan
+  size_t off_groups = 0, off_group_req = 0, off_req = 0, off_pitems = 0, off_sitems = 0;
+  int32_t n_groups = 0, n_pitems = 0, n_sitems = 0, B = 0, n_records = 0;
+  int32_t suffix_impl = kImplGeneric;
+  std::vector<granikv_group_info> info;
+  std::vector<int32_t> group_impl;
+  uint64_t version = 0;
+  const void* uploaded_ws = nullptr;
+  uint64_t uploaded_version = ~0ull;
+  bool valid = false;
+};
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int elem_size(int32_t dtype) { return dtype == GRANIKV_DTYPE_BF16 ? 2 : 4; }
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+granikv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GRANIKV_OK : GRANIKV_ERR_CUDA; }
+
+bool has_device(const granikv_ctx* c) { return c && !c->cfg.host_only && c->d_ring; }
+
+// Which prefix implementation serves a group of this shape and backend.
+int32_t prefix_impl_for(const granikv_ctx* c, int32_t backend) {
+  (void)backend;
+  (void)c;
+  return kImplGeneric;
+}
+
+int32_t rows_per_cta_for(int32_t impl) {
+  switch (impl) {
+    case kImplDenseTc: return 128;
+    case kImplCascadeMma: return 64;
+    default: return 16;
+  }
+}
+
+int32_t tile_tokens_for(int32_t impl) {
+  switch (impl) {
+    case kImplDenseTc: return 128;
+    case kImplCascadeMma: return 64;
+    default: return 32;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* granikv_status_string(granikv_status s) {
+  switch (s) {
+    case GRANIKV_OK: return "ok";
+    case GRANIKV_ERR_INVALID: return "invalid argument or descriptor";
+    case GRANIKV_ERR_NO_HOT_SPACE: return "no HOT extent large enough (or slab table full)";
+    case GRANIKV_ERR_NO_COLD_SPACE: return "not enough free COLD slots";
+    case GRANIKV_ERR_CUDA: return "CUDA runtime error";
+    case GRANIKV_ERR_DEVICE_CHECK: return "device bounds check failed";
+    case GRANIKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case GRANIKV_ERR_NO_DEVICE: return "context has no device resources";
+    default: return "unknown status";
+  }
+}
+
+int32_t granikv_version(void) { return 100; }
+
+granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
+  if (!cfg || !out) return GRANIKV_ERR_INVALID;
+  *out = nullptr;
+  if (cfg->n_layers <= 0 || cfg->n_q <= 0 || cfg->n_kv <= 0 || cfg->n_q % cfg->n_kv)
+    return GRANIKV_ERR_INVALID;
+  if (cfg->head_dim <= 0 || cfg->head_dim % 32 || cfg->head_dim > 256) return GRANIKV_ERR_UNSUPPORTED;
+  if (cfg->dtype != GRANIKV_DTYPE_F32 && cfg->dtype != GRANIKV_DTYPE_BF16) return GRANIKV_ERR_INVALID;
+  if (cfg->n_slots <= 1 || cfg->n_slots > (int64_t)INT32_MAX) return GRANIKV_ERR_INVALID;
+  double fp = cfg->hot_fraction == 0.0 ? 0.2 : cfg->hot_fraction;
+  if (!(fp > 0.0 && fp < 1.0)) return GRANIKV_ERR_INVALID;
+  if (cfg->max_slabs < 0 || cfg->max_batch < 0 || cfg->m_sat < 0) return GRANIKV_ERR_INVALID;
+
+  granikv_ctx* c = new (std::nothrow) granikv_ctx();
+  if (!c) return GRANIKV_ERR_INVALID;
+  c->cfg = *cfg;
+  c->cfg.hot_fraction = fp;
+  if (c->cfg.max_slabs == 0) c->cfg.max_slabs = kDefaultMaxSlabs;
+  if (c->cfg.max_batch == 0) c->cfg.max_batch = kDefaultMaxBatch;
+  c->m_sat = cfg->m_sat ? cfg->m_sat : kDefaultMsat;
+  c->g = cfg->n_q / cfg->n_kv;
+  c->n_hot = (int64_t)std::floor(fp * (double)cfg->n_slots);
+  c->n_cold = cfg->n_slots - c->n_hot;
+  if (c->n_hot < 0 || c->n_cold <= 0) {
+    delete c;
+    return GRANIKV_ERR_INVALID;
+  }
+  if (c->n_hot > 0) c->free_ext.push_back({0, c->n_hot});
+  c->slabs.resize(c->cfg.max_slabs);
+  c->head = 0;
+  c->tail = c->n_cold;
+  c->cfg.k_pool = nullptr;
+  c->cfg.v_pool = nullptr;
+  c->cfg.cold_init_order = nullptr;
+  if (cfg->k_pool && cfg->v_pool) {
+    c->kpool.assign(cfg->k_pool, cfg->k_pool + cfg->n_layers);
+    c->vpool.assign(cfg->v_pool, cfg->v_pool + cfg->n_layers);
+  }
+
+  if (!cfg->host_only) {
+    if (!cfg->k_pool || !cfg->v_pool) {
+      delete c;
+      return GRANIKV_ERR_INVALID;
+    }
+    std::vector<int32_t> init(c->n_cold);
+    if (cfg->cold_init_order) {
+      std::vector<char> seen(c->n_cold, 0);
+      for (int64_t i = 0; i < c->n_cold; ++i) {
+        int64_t v = cfg->cold_init_order[i];
+        if (v < c->n_hot || v >= cfg->n_slots || seen[v - c->n_hot]) {
+          delete c;
+          return GRANIKV_ERR_INVALID;
+        }
+        seen[v - c->n_hot] = 1;
+        init[i] = (int32_t)v;
+      }
+    } else {
+      for (int64_t i = 0; i < c->n_cold; ++i) init[i] = (int32_t)(c->n_hot + i);
+    }
+    DeviceGuard dg(cfg->device);
+    cudaError_t e = dg.ok ? cudaSuccess : cudaErrorInvalidDevice;
+    cudaDeviceProp prop;
+    if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, cfg->device);
+    if (e == cudaSuccess) {
+      c->num_sms = prop.multiProcessorCount;
+      c->cc_major = prop.major;
+      c->cc_minor = prop.minor;
+    }
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_ring, sizeof(int32_t) * c->n_cold);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_err, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_stage, sizeof(int32_t) * (c->cfg.max_batch + 1));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(c->d_ring, init.data(), sizeof(int32_t) * c->n_cold, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int32_t) * 4);
+    if (e != cudaSuccess) {
+      if (c->d_ring) cudaFree(c->d_ring);
+      if (c->d_err) cudaFree(c->d_err);
+      if (c->d_stage) cudaFree(c->d_stage);
+      delete c;
+      return GRANIKV_ERR_CUDA;
+    }
+  }
+  *out = c;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_destroy(granikv_ctx* c) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  if (c->own_plan) delete c->own_plan;
+  if (!c->cfg.host_only) {
+    DeviceGuard dg(c->cfg.device);
+    if (c->d_ring) cudaFree(c->d_ring);
+    if (c->d_err) cudaFree(c->d_err);
+    if (c->d_stage) cudaFree(c->d_stage);
+  }
+  delete c;
+  return GRANIKV_OK;
+}
+
+// ---- HOT pool -------------------------------------------------------------------------------
+
+granikv_status granikv_hot_alloc(granikv_ctx* c, int32_t L_p, int32_t* slab_id, int64_t* off) {
+  if (!c || !slab_id || !off || L_p <= 0) return GRANIKV_ERR_INVALID;
+  int32_t sid = -1;
+  for (int32_t i = 0; i < (int32_t)c->slabs.size(); ++i)
+    if (!c->slabs[i].live) {
+      sid = i;
+      break;
+    }
+  if (sid < 0) return GRANIKV_ERR_NO_HOT_SPACE;
+  for (size_t i = 0; i < c->free_ext.size(); ++i) {
+    Extent& e = c->free_ext[i];
+    if (e.len >= L_p) {
+      int64_t o = e.off;
+      e.off += L_p;
+      e.len -= L_p;
+      if (e.len == 0) c->free_ext.erase(c->free_ext.begin() + i);
+      c->slabs[sid].off = o;
+      c->slabs[sid].len = L_p;
+      c->slabs[sid].live = true;
+      *slab_id = sid;
+      *off = o;
+      return GRANIKV_OK;
+    }
+  }
+  return GRANIKV_ERR_NO_HOT_SPACE;
+}
+
+granikv_status granikv_hot_free(granikv_ctx* c, int32_t sid) {
+  if (!c || sid < 0 || sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live)
+    return GRANIKV_ERR_INVALID;
+  Slab& s = c->slabs[sid];
+  Extent ne{s.off, s.len};
+  s.live = false;
+  auto it = std::lower_bound(c->free_ext.begin(), c->free_ext.end(), ne,
+                             [](const Extent& a, const Extent& b) { return a.off < b.off; });
+  it = c->free_ext.insert(it, ne);
+  size_t i = it - c->free_ext.begin();
+  if (i + 1 < c->free_ext.size() && c->free_ext[i].off + c->free_ext[i].len == c->free_ext[i + 1].off) {
+    c->free_ext[i].len += c->free_ext[i + 1].len;
+    c->free_ext.erase(c->free_ext.begin() + i + 1);
+  }
+  if (i > 0 && c->free_ext[i - 1].off + c->free_ext[i - 1].len == c->free_ext[i].off) {
+    c->free_ext[i - 1].len += c->free_ext[i].len;
+    c->free_ext.erase(c->free_ext.begin() + i);
+  }
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_hot_info(granikv_ctx* c, int32_t sid, int64_t* off, int32_t* L_p) {
+  if (!c || sid < 0 || sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live)
+    return GRANIKV_ERR_INVALID;
+  if (off) *off = c->slabs[sid].off;
+  if (L_p) *L_p = c->slabs[sid].len;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_hot_stats(granikv_ctx* c, int64_t* n_hot, int64_t* largest) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  if (n_hot) *n_hot = c->n_hot;
+  if (largest) {
+    int64_t m = 0;
+    for (auto& e : c->free_ext) m = std::max(m, e.len);
+    *largest = m;
+  }
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_hot_fill(granikv_ctx* c, int32_t layer, int32_t sid, const void* k,
+                                const void* v, granikv_stream_t stream) {
+  if (!c || !k || !v || layer < 0 || layer >= c->cfg.n_layers) return GRANIKV_ERR_INVALID;
+  if (sid < 0 || sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  DeviceGuard dg(c->cfg.device);
+  size_t row = (size_t)c->cfg.n_kv * c->cfg.head_dim * elem_size(c->cfg.dtype);
+  size_t off = (size_t)c->slabs[sid].off * row;
+  size_t bytes = (size_t)c->slabs[sid].len * row;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync((char*)c->kpool[layer] + off, k, bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync((char*)c->vpool[layer] + off, v, bytes, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+// ---- COLD pool ------------------------------------------------------------------------------
+
+granikv_status granikv_cold_alloc(granikv_ctx* c, const int32_t* n_new, int32_t B,
+                                  int32_t* req_to_slot, int32_t* suffix_len, int32_t cap,
+                                  int32_t* slots_out, granikv_stream_t stream) {
+  if (!c || !n_new || B <= 0 || !req_to_slot || !suffix_len || cap <= 0) return GRANIKV_ERR_INVALID;
+  if (B > c->cfg.max_batch) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  std::vector<int32_t> excl(B + 1);
+  int64_t tot = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (n_new[b] < 0 || n_new[b] > cap) return GRANIKV_ERR_INVALID;
+    excl[b] = (int32_t)tot;
+    tot += n_new[b];
+  }
+  if (tot > (int64_t)INT32_MAX) return GRANIKV_ERR_INVALID;
+  excl[B] = (int32_t)tot;
+  if (tot > c->tail - c->head) return GRANIKV_ERR_NO_COLD_SPACE;
+  if (tot == 0) return GRANIKV_OK;
+  DeviceGuard dg(c->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(c->d_stage, excl.data(), sizeof(int32_t) * (B + 1),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = launch_cold_alloc(c->d_stage, B, c->d_ring, c->n_cold, c->head, req_to_slot, suffix_len,
+                          cap, slots_out, c->d_err, s);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  c->n_copies += 1;
+  c->n_kernels += 1;
+  c->head += tot;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_cold_free(granikv_ctx* c, const int32_t* slots, int32_t n,
+                                 granikv_stream_t stream) {
+  if (!c || n < 0 || (n > 0 && !slots)) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  if ((c->tail - c->head) + n > c->n_cold) return GRANIKV_ERR_INVALID;
+  if (n == 0) return GRANIKV_OK;
+  DeviceGuard dg(c->cfg.device);
+  cudaError_t e = launch_cold_free(slots, n, c->d_ring, c->n_cold, c->tail, c->n_hot,
+                                   c->cfg.n_slots, c->checks, c->d_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  c->n_kernels += 1;
+  c->tail += n;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_cold_free_count(granikv_ctx* c, int64_t* n_free) {
+  if (!c || !n_free) return GRANIKV_ERR_INVALID;
+  *n_free = c->tail - c->head;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_cold_append(granikv_ctx* c, int32_t layer, const void* k_new,
+                                   const void* v_new, const int32_t* slots, int32_t N,
+                                   granikv_stream_t stream) {
+  if (!c || layer < 0 || layer >= c->cfg.n_layers || N < 0) return GRANIKV_ERR_INVALID;
+  if (N > 0 && (!k_new || !v_new || !slots)) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  if (N == 0) return GRANIKV_OK;
+  DeviceGuard dg(c->cfg.device);
+  cudaError_t e = launch_cold_append(c->cfg.dtype, k_new, v_new, slots, N, c->kpool[layer],
+                                     c->vpool[layer], (int64_t)c->cfg.n_kv * c->cfg.head_dim,
+                                     c->n_hot, c->cfg.n_slots, c->checks, c->d_err,
+                                     (cudaStream_t)stream);
+  if (e == cudaSuccess) c->n_kernels += 1;
+  return cuda_status(e);
+}
+
+// ---- dispatch -------------------------------------------------------------------------------
+
+granikv_status granikv_plan_create(granikv_ctx* c, granikv_plan** out) {
+  if (!c || !out) return GRANIKV_ERR_INVALID;
+  granikv_plan* p = new (std::nothrow) granikv_plan();
+  if (!p) return GRANIKV_ERR_INVALID;
+  p->ctx = c;
+  *out = p;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_plan_destroy(granikv_plan* p) {
+  if (!p) return GRANIKV_ERR_INVALID;
+  delete p;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv_plan* p) {
+  if (!c || !bt || !p || p->ctx != c) return GRANIKV_ERR_INVALID;
+  const int32_t B = bt->B;
+  if (B <= 0 || B > c->cfg.max_batch || !bt->slab_id || !bt->seq_len || bt->cap < 0)
+    return GRANIKV_ERR_INVALID;
+  p->valid = false;
+  const int32_t g = c->g;
+  const int32_t n_kv = c->cfg.n_kv;
+
+  // 1. group requests by slab id, in order of first appearance; members in request order
+  thread_local std::vector<int32_t> slot_of_slab;
+  slot_of_slab.assign(c->slabs.size(), -1);
+  std::vector<int32_t> grp_slab;
+  std::vector<int32_t> grp_count;
+  std::vector<int32_t> req_group(B, -1);
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t sid = bt->slab_id[b];
+    int32_t L = bt->seq_len[b];
+    if (L < 0 || L > bt->cap) return GRANIKV_ERR_INVALID;
+    if (sid < 0) {
+      if (L == 0) return GRANIKV_ERR_INVALID;
+      continue;
+    }
+    if (sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live) return GRANIKV_ERR_INVALID;
+    if (slot_of_slab[sid] < 0) {
+      slot_of_slab[sid] = (int32_t)grp_slab.size();
+      grp_slab.push_back(sid);
+      grp_count.push_back(0);
+    }
+    req_group[b] = slot_of_slab[sid];
+    grp_count[slot_of_slab[sid]]++;
+  }
+  const int32_t G = (int32_t)grp_slab.size();
+
+  // 2. backend per group: M_eff = B_g * n_q / n_kv, dense iff M_eff >= M_sat
+  std::vector<DevGroup> groups(G);
+  p->info.assign(G, granikv_group_info{});
+  int64_t prefix_units = 0;  // sum over groups of n_kv * row_blocks * L_p
+  std::vector<int32_t> begin(G + 1, 0);
+  for (int32_t i = 0; i < G; ++i) begin[i + 1] = begin[i] + grp_count[i];
+  for (int32_t i = 0; i < G; ++i) {
+    DevGroup& dg = groups[i];
+    const Slab& s = c->slabs[grp_slab[i]];
+    int32_t m_eff = grp_count[i] * g;
+    int32_t backend = c->forced != GRANIKV_BACKEND_AUTO
+                          ? c->forced
+                          : (m_eff >= c->m_sat ? GRANIKV_BACKEND_DENSE : GRANIKV_BACKEND_CASCADE);
+    dg.slab_off = s.off;
+    dg.L_p = s.len;
+    dg.n_req = grp_count[i];
+    dg.req_begin = begin[i];
+    dg.backend = backend;
+    dg.impl = prefix_impl_for(c, backend);
+    dg.rows_per_cta = rows_per_cta_for(dg.impl);
+    dg.row_blocks = (m_eff + dg.rows_per_cta - 1) / dg.rows_per_cta;
+    dg.pad = 0;
+    prefix_units += (int64_t)n_kv * dg.row_blocks * dg.L_p;
+  }
+  // 3. prefix split length shared by all groups so the prefix pass fills ~2 waves
+  int64_t target = 2LL * c->num_sms;
+  for (int32_t i = 0; i < G; ++i) {
+    DevGroup& dg = groups[i];
+    int64_t tile = tile_tokens_for(dg.impl);
+    int64_t per = (prefix_units + target - 1) / std::max<int64_t>(target, 1);
+    int64_t split = std::max<int64_t>(tile, (per + tile - 1) / tile * tile);
+    split = std::min<int64_t>(split, (dg.L_p + tile - 1) / tile * tile);
+    dg.split_len = (int32_t)split;
+    dg.n_splits = (int32_t)((dg.L_p + split - 1) / split);
+    granikv_group_info& gi = p->info[i];
+    gi.slab_id = grp_slab[i];
+    gi.n_requests = dg.n_req;
+    gi.m_eff = dg.n_req * g;
+    gi.backend = dg.backend;
+    gi.L_p = dg.L_p;
+    gi.n_splits = dg.n_splits;
+    gi.slot_offset = dg.slab_off;
+  }
+  // 4. suffix chunking: chunk length so that the suffix pass fills ~2 waves
+  int64_t T = 0;
+  for (int32_t b = 0; b < B; ++b) T += bt->seq_len[b];
+  int32_t suffix_impl = kImplGeneric;
+  int64_t chunk = (T + target - 1) / std::max<int64_t>(target, 1);
+  chunk = std::max<int64_t>(64, std::min<int64_t>(2048, (chunk + 31) / 32 * 32));
+
+  // 5. records and work items
+  std::vector<int32_t> group_req(begin[G]);
+  {
+    std::vector<int32_t> fill(begin.begin(), begin.end() - 1);
+    for (int32_t b = 0; b < B; ++b)
+      if (req_group[b] >= 0) group_req[fill[req_group[b]]++] = b;
+  }
+  std::vector<DevReq> reqs(B);
+  int64_t rec = 0;
+  std::vector<DevSuffixItem> sitems;
+  sitems.reserve(B + T / chunk + 1);
+  for (int32_t b = 0; b < B; ++b) {
+    DevReq& r = reqs[b];
+    r.rec_base = (int32_t)rec;
+    r.n_prefix = req_group[b] >= 0 ? groups[req_group[b]].n_splits : 0;
+    int32_t L = bt->seq_len[b];
+    int32_t n_chunks = (int32_t)((L + chunk - 1) / chunk);
+    r.n_parts = r.n_prefix + n_chunks;
+    r.seq_len = L;
+    for (int32_t k = 0; k < n_chunks; ++k) {
+      DevSuffixItem it;
+      it.b = b;
+      it.t0 = (int32_t)(k * chunk);
+      it.t1 = (int32_t)std::min<int64_t>(L, (k + 1) * chunk);
+      it.rec = (int32_t)(rec + r.n_prefix + k);
+      sitems.push_back(it);
+    }
+    rec += r.n_parts;
+  }
+  if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
+  // longest chunks first (a full chunk never follows a shorter one)
+  std::stable_sort(sitems.begin(), sitems.end(), [](const DevSuffixItem& a, const DevSuffixItem& b) {
+    return (a.t1 - a.t0) > (b.t1 - b.t0);
+  });
+  std::vector<DevPrefixItem> pitems;
+  for (int32_t i = 0; i < G; ++i) {
+    const DevGroup& dg = groups[i];
+    for (int32_t j = 0; j < n_kv; ++j)
+      for (int32_t s = 0; s < dg.n_splits; ++s)
+        for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
+  }
+
+  // 6. pack the device image
+  size_t off = 0;
+  p->off_groups = off;
+  off = align_up(off + sizeof(DevGroup) * G, 16);
+  p->off_group_req = off;
+  off = align_up(off + sizeof(int32_t) * group_req.size(), 16);
+  p->off_req = off;
+  off = align_up(off + sizeof(DevReq) * B, 16);
+  p->off_pitems = off;
+  off = align_up(off + sizeof(DevPrefixItem) * pitems.size(), 16);
+  p->off_sitems = off;
+  off = align_up(off + sizeof(DevSuffixItem) * sitems.size(), 256);
+  p->blob.assign(off, 0);
+  if (G) std::memcpy(p->blob.data() + p->off_groups, groups.data(), sizeof(DevGroup) * G);
+  if (!group_req.empty())
+    std::memcpy(p->blob.data() + p->off_group_req, group_req.data(), sizeof(int32_t) * group_req.size());
+  std::memcpy(p->blob.data() + p->off_req, reqs.data(), sizeof(DevReq) * B);
+  if (!pitems.empty())
+    std::memcpy(p->blob.data() + p->off_pitems, pitems.data(), sizeof(DevPrefixItem) * pitems.size());
+  if (!sitems.empty())
+    std::memcpy(p->blob.data() + p->off_sitems, sitems.data(), sizeof(DevSuffixItem) * sitems.size());
+  p->n_groups = G;
+  p->n_pitems = (int32_t)pitems.size();
+  p->n_sitems = (int32_t)sitems.size();
+  p->B = B;
+  p->n_records = (int32_t)rec;
+  p->suffix_impl = suffix_impl;
+  p->group_impl.resize(G);
+  for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
+  p->version++;
+  p->valid = true;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_plan_num_groups(const granikv_plan* p, int32_t* n) {
+  if (!p || !n || !p->valid) return GRANIKV_ERR_INVALID;
+  *n = p->n_groups;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_plan_group(const granikv_plan* p, int32_t i, granikv_group_info* out) {
+  if (!p || !out || !p->valid || i < 0 || i >= p->n_groups) return GRANIKV_ERR_INVALID;
+  *out = p->info[i];
+  return GRANIKV_OK;
+}
+
+namespace {
+size_t workspace_bytes(const granikv_ctx* c, const granikv_plan* p) {
+  size_t off = align_up(p->blob.size(), 256);
+  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q * c->cfg.head_dim, 256);
+  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q, 256);
+  return off;
+}
+}  // namespace
+
+granikv_status granikv_workspace_size(granikv_ctx* c, const granikv_plan* p, size_t* bytes) {
+  if (!c || !p || !bytes || !p->valid || p->ctx != c) return GRANIKV_ERR_INVALID;
+  *bytes = workspace_bytes(c, p);
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_set_msat(granikv_ctx* c, int32_t m) {
+  if (!c || m <= 0) return GRANIKV_ERR_INVALID;
+  c->m_sat = m;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_get_msat(granikv_ctx* c, int32_t* m) {
+  if (!c || !m) return GRANIKV_ERR_INVALID;
+  *m = c->m_sat;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_force_backend(granikv_ctx* c, int32_t backend) {
+  if (!c || backend < GRANIKV_BACKEND_AUTO || backend > GRANIKV_BACKEND_CASCADE)
+    return GRANIKV_ERR_INVALID;
+  c->forced = backend;
+  return GRANIKV_OK;
+}
+
+// ---- decode attention -----------------------------------------------------------------------
+
+granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const void* q,
+                                        const granikv_batch* bt, granikv_plan* p, void* o,
+                                        float* lse, void* ws, size_t ws_bytes,
+                                        granikv_stream_t stream) {
+  if (!c || !bt || !q || !o || !lse || !ws) return GRANIKV_ERR_INVALID;
+  if (layer < 0 || layer >= c->cfg.n_layers) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  if ((uintptr_t)ws % 256) return GRANIKV_ERR_INVALID;
+  if (!bt->req_to_slot) return GRANIKV_ERR_INVALID;
+  if (!p) {
+    if (!c->own_plan) {
+      granikv_status st = granikv_plan_create(c, &c->own_plan);
+      if (st != GRANIKV_OK) return st;
+    }
+    p = c->own_plan;
+    granikv_status st = granikv_dispatch(c, bt, p);
+    if (st != GRANIKV_OK) return st;
+  }
+  if (!p->valid || p->ctx != c || p->B != bt->B) return GRANIKV_ERR_INVALID;
+  if (ws_bytes < workspace_bytes(c, p)) return GRANIKV_ERR_INVALID;
+
+  DeviceGuard dg(c->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned char* wsb = (unsigned char*)ws;
+  if (p->uploaded_ws != ws || p->uploaded_version != p->version) {
+    cudaError_t e = cudaMemcpyAsync(wsb, p->blob.data(), p->blob.size(), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+    c->n_copies += 1;
+    p->uploaded_ws = ws;
+    p->uploaded_version = p->version;
+  }
+  AttnParams a{};
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.kpool = c->kpool[layer];
+  a.vpool = c->vpool[layer];
+  a.req_to_slot = bt->req_to_slot;
+  a.n_slots = c->cfg.n_slots;
+  a.n_hot = c->n_hot;
+  a.cap = bt->cap;
+  a.B = bt->B;
+  a.n_q = c->cfg.n_q;
+  a.n_kv = c->cfg.n_kv;
+  a.d = c->cfg.head_dim;
+  a.g = c->g;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  a.groups = (const DevGroup*)(wsb + p->off_groups);
+  a.group_req = (const int32_t*)(wsb + p->off_group_req);
+  a.reqs = (const DevReq*)(wsb + p->off_req);
+  a.pitems = (const DevPrefixItem*)(wsb + p->off_pitems);
+  a.n_pitems = p->n_pitems;
+  a.sitems = (const DevSuffixItem*)(wsb + p->off_sitems);
+  a.n_sitems = p->n_sitems;
+  size_t off = align_up(p->blob.size(), 256);
+  a.rec_o = (float*)(wsb + off);
+  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q * c->cfg.head_dim, 256);
+  a.rec_lse = (float*)(wsb + off);
+  a.n_records = p->n_records;
+  a.err = c->d_err;
+  a.checks = c->checks;
+
+  cudaError_t e = cudaSuccess;
+  if (p->n_pitems > 0) {
+    e = launch_prefix_generic(c->cfg.dtype, a, 0, p->n_pitems, s);
+    c->n_kernels += 1;
+  }
+  if (e == cudaSuccess && p->n_sitems > 0) {
+    e = launch_suffix_generic(c->cfg.dtype, a, s);
+    c->n_kernels += 1;
+  }
+  if (e == cudaSuccess) {
+    e = launch_merge(c->cfg.dtype, a, s);
+    c->n_kernels += 1;
+  }
+  return cuda_status(e);
+}
+
+// ---- checks ---------------------------------------------------------------------------------
+
+granikv_status granikv_set_checks(granikv_ctx* c, int32_t on) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  c->checks = on ? 1 : 0;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_sync_status(granikv_ctx* c, granikv_stream_t stream) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  DeviceGuard dg(c->cfg.device);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  int32_t h = 0;
+  e = cudaMemcpy(&h, c->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  if (h != 0) {
+    cudaMemset(c->d_err, 0, sizeof(int32_t));
+    return GRANIKV_ERR_DEVICE_CHECK;
+  }
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_launch_count(granikv_ctx* c, int64_t* kernels, int64_t* copies) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  if (kernels) *kernels = c->n_kernels;
+  if (copies) *copies = c->n_copies;
+  return GRANIKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// internal.h -- shared between the host library and the CUDA kernels of libgranikv.
+//
+// The per-step plan built by the dispatcher is a flat image of the structs below.  The host
+// builds it, granikv_decode_attention copies it into the front of the caller's workspace, and
+// the kernels read their work items from there.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace granikv {
+
+// Error codes latched in the device error word (first failure wins).
+enum DevErr : int32_t {
+  kDevOk = 0,
+  kDevBadSlot = 1,        // a COLD slot id outside [n_hot, n_slots)
+  kDevTableOverflow = 2,  // a token table row would pass cap
+  kDevBadSlab = 3,        // a slab range outside [0, n_hot)
+  kDevBadRecord = 4,      // a partial-state record index outside the workspace
+};
+
+// Kernel implementations a prefix group or the suffix pass can run on.
+enum Impl : int32_t {
+  kImplGeneric = 0,   // CUDA-core kernel, any head_dim % 32 == 0 up to 256, f32 or bf16
+  kImplCascadeMma = 1,// bf16, head_dim 128: warp-level tensor-core cascade kernel
+  kImplDenseTc = 2,   // bf16, head_dim 128: tcgen05/TMEM dense kernel
+  kImplSuffixMma = 3, // bf16, head_dim 128, g <= 8: warp-level tensor-core suffix kernel
+};
+
+struct DevGroup {        // one prefix group: the requests sharing one HOT slab
+  int64_t slab_off;      // first slot of the slab
+  int32_t L_p;
+  int32_t n_req;
+  int32_t req_begin;     // index into the group_req array
+  int32_t n_splits;      // pieces along L_p
+  int32_t split_len;     // tokens per piece (last piece may be shorter)
+  int32_t backend;       // GRANIKV_BACKEND_DENSE / _CASCADE
+  int32_t impl;          // Impl
+  int32_t rows_per_cta;  // query rows (request, head-in-group) pairs per CTA
+  int32_t row_blocks;    // ceil(n_req * g / rows_per_cta)
+  int32_t pad;
+};
+static_assert(sizeof(DevGroup) == 48, "DevGroup layout");
+
+struct DevReq {          // per request of the batch
+  int32_t rec_base;      // first partial-state record of this request
+  int32_t n_prefix;      // records written by the prefix pass (0 without a HOT prefix)
+  int32_t n_parts;       // records in total (prefix pieces + suffix chunks)
+  int32_t seq_len;       // tokens in the COLD token table
+};
+
+struct DevPrefixItem {   // one CTA of a prefix kernel
+  int32_t group, kv_head, row_block, split;
+};
+
+struct DevSuffixItem {   // one CTA of a suffix kernel
+  int32_t b, t0, t1, rec;  // request, token range [t0, t1) of its COLD table, record index
+};
+
+// Everything an attention kernel needs, passed by value.
+struct AttnParams {
+  const void* q;          // [B, n_q, d]
+  void* o;                // [B, n_q, d]
+  float* lse;             // [B, n_q]
+  const void* kpool;      // [n_slots, n_kv, d]
+  const void* vpool;
+  const int32_t* req_to_slot;  // [B, cap]
+  int64_t n_slots, n_hot;
+  int32_t cap, B, n_q, n_kv, d, g;
+  float scale_log2;       // softmax scale * log2(e)
+  const DevGroup* groups;
+  const int32_t* group_req;
+  const DevReq* reqs;
+  const DevPrefixItem* pitems;
+  int32_t n_pitems;
+  const DevSuffixItem* sitems;
+  int32_t n_sitems;
+  float* rec_o;           // [n_records, n_q, d]
+  float* rec_lse;         // [n_records, n_q]
+  int32_t n_records;
+  int32_t* err;           // device error word
+  int32_t checks;
+};
+
+// ---- launchers (kernels_*.cu) ------------------------------------------------------------
+cudaError_t launch_cold_alloc(const int32_t* excl /*[B+1]*/, int32_t B, const int32_t* ring,
+                              int64_t n_cold, int64_t head, int32_t* req_to_slot,
+                              int32_t* suffix_len, int32_t cap, int32_t* slots_out,
+                              int32_t* err, cudaStream_t s);
+cudaError_t launch_cold_free(const int32_t* slots, int32_t n, int32_t* ring, int64_t n_cold,
+                             int64_t tail, int64_t n_hot, int64_t n_slots, int32_t checks,
+                             int32_t* err, cudaStream_t s);
+cudaError_t launch_cold_append(int32_t dtype, const void* k_new, const void* v_new,
+                               const int32_t* slots, int32_t N, void* kpool, void* vpool,
+                               int64_t row_elems, int64_t n_hot, int64_t n_slots,
+                               int32_t checks, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_prefix_generic(int32_t dtype, const AttnParams& p, int32_t first_item,
+                                  int32_t n_items, cudaStream_t s);
+cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream_t s);
+cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s);
+
+}  // namespace granikv

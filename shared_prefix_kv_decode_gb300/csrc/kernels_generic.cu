@@ -1,0 +1,252 @@
+// kernels_generic.cu -- CUDA-core decode attention for any head_dim that is a multiple of 32
+// (up to 256), fp32 or bf16: the prefix pass, the COLD suffix pass and the log-sum-exp merge.
+//
+// GraniKV (arXiv:2608.15584), "2 Related Work", prefix-suffix attention: the shared prefix
+// and each request's suffix are attended separately and their partial states merged with
+// log-sum-exp.  One warp owns one query row; each lane holds head_dim/32 consecutive elements
+// of q and of the running output, the q.k dot product is reduced with warp shuffles, and the
+// softmax is the usual online (running max, running sum) form in base 2.
+//
+// These kernels serve the fp32 path and every shape the tensor-core kernels do not cover.
+#include "internal.h"
+
+#include <cuda_bf16.h>
+
+namespace granikv {
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void latch(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
+
+template <typename T, int VPL>
+__device__ __forceinline__ void load_row(const T* p, float (&x)[VPL]);
+
+template <int VPL>
+__device__ __forceinline__ void load_row(const float* p, float (&x)[VPL]) {
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) x[i] = p[i];
+}
+
+template <int VPL>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* p, float (&x)[VPL]) {
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) x[i] = __bfloat162float(p[i]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Online softmax state of one query row, spread over a warp.
+template <int VPL>
+struct RowState {
+  float m = -INFINITY;  // running max of the base-2 logits
+  float l = 0.f;        // running sum of 2^(logit - m)
+  float acc[VPL];
+  __device__ RowState() {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[i] = 0.f;
+  }
+  __device__ __forceinline__ void add(float s2, const float (&v)[VPL]) {
+    const float m_new = fmaxf(m, s2);
+    const float alpha = exp2f(m - m_new);
+    const float p = exp2f(s2 - m_new);
+    l = l * alpha + p;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[i] = acc[i] * alpha + p * v[i];
+    m = m_new;
+  }
+};
+
+template <int VPL>
+__device__ __forceinline__ void store_record(const AttnParams& p, const RowState<VPL>& st, int32_t rec,
+                                             int32_t h, int lane) {
+  if (p.checks && (rec < 0 || rec >= p.n_records)) {
+    if (lane == 0) latch(p.err, kDevBadRecord);
+    return;
+  }
+  float* dst = p.rec_o + ((int64_t)rec * p.n_q + h) * p.d + lane * VPL;
+  const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) dst[i] = st.acc[i] * inv;
+  if (lane == 0) p.rec_lse[(int64_t)rec * p.n_q + h] = st.l > 0.f ? (st.m + log2f(st.l)) * kLn2 : -INFINITY;
+}
+
+// Prefix pass: one CTA per prefix work item (group, KV head, row block, L_p piece).  The
+// slab is contiguous, so token t of the piece is slot slab_off + t.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) prefix_generic_kernel(AttnParams p, int32_t first_item) {
+  const DevPrefixItem it = p.pitems[first_item + blockIdx.x];
+  const DevGroup gr = p.groups[it.group];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t rows = gr.n_req * p.g;
+  const int32_t r0 = it.row_block * gr.rows_per_cta;
+  const int32_t r1 = min(rows, r0 + gr.rows_per_cta);
+  const int32_t t0 = it.split * gr.split_len;
+  const int32_t t1 = min(gr.L_p, t0 + gr.split_len);
+  if (p.checks && (gr.slab_off < 0 || gr.slab_off + gr.L_p > p.n_hot)) {
+    if (threadIdx.x == 0) latch(p.err, kDevBadSlab);
+    return;
+  }
+  const int64_t tok_stride = (int64_t)p.n_kv * p.d;
+  const T* kbase = (const T*)p.kpool + gr.slab_off * tok_stride + (int64_t)it.kv_head * p.d + lane * VPL;
+  const T* vbase = (const T*)p.vpool + gr.slab_off * tok_stride + (int64_t)it.kv_head * p.d + lane * VPL;
+  for (int32_t r = r0 + warp; r < r1; r += blockDim.x >> 5) {
+    const int32_t b = p.group_req[gr.req_begin + r / p.g];
+    const int32_t h = it.kv_head * p.g + r % p.g;
+    float q[VPL];
+    load_row<VPL>((const T*)p.q + ((int64_t)b * p.n_q + h) * p.d + lane * VPL, q);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) q[i] *= p.scale_log2;
+    RowState<VPL> st;
+    for (int32_t t = t0; t < t1; ++t) {
+      float k[VPL], v[VPL];
+      load_row<VPL>(kbase + t * tok_stride, k);
+      load_row<VPL>(vbase + t * tok_stride, v);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) dot += q[i] * k[i];
+      st.add(warp_sum(dot), v);
+    }
+    store_record<VPL>(p, st, p.reqs[b].rec_base + it.split, h, lane);
+  }
+}
+
+// Suffix pass: one CTA per (request, token chunk) of its COLD token table; token t lives at
+// slot req_to_slot[b, t].  Warps take the query heads in turn.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) suffix_generic_kernel(AttnParams p) {
+  const DevSuffixItem it = p.sitems[blockIdx.x];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tok_stride = (int64_t)p.n_kv * p.d;
+  const int32_t* table = p.req_to_slot + (int64_t)it.b * p.cap;
+  for (int32_t h = warp; h < p.n_q; h += blockDim.x >> 5) {
+    const int32_t j = h / p.g;
+    float q[VPL];
+    load_row<VPL>((const T*)p.q + ((int64_t)it.b * p.n_q + h) * p.d + lane * VPL, q);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) q[i] *= p.scale_log2;
+    RowState<VPL> st;
+    for (int32_t t = it.t0; t < it.t1; ++t) {
+      const int32_t slot = table[t];
+      if (slot < p.n_hot || slot >= p.n_slots) {
+        if (lane == 0) latch(p.err, kDevBadSlot);
+        continue;
+      }
+      float k[VPL], v[VPL];
+      load_row<VPL>((const T*)p.kpool + slot * tok_stride + (int64_t)j * p.d + lane * VPL, k);
+      load_row<VPL>((const T*)p.vpool + slot * tok_stride + (int64_t)j * p.d + lane * VPL, v);
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) dot += q[i] * k[i];
+      st.add(warp_sum(dot), v);
+    }
+    store_record<VPL>(p, st, it.rec, h, lane);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_out(T* dst, float v);
+template <>
+__device__ __forceinline__ void store_out<float>(float* dst, float v) { *dst = v; }
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* dst, float v) {
+  *dst = __float2bfloat16_rn(v);
+}
+
+// Merge: one CTA per request, one warp per head in turn.  lse = M + ln sum_i e^(lse_i - M),
+// o = sum_i e^(lse_i - lse) o_i over the request's partial-state records.
+template <typename T>
+__global__ void __launch_bounds__(256) merge_kernel(AttnParams p) {
+  const int32_t b = blockIdx.x;
+  const DevReq r = p.reqs[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int32_t h = warp; h < p.n_q; h += blockDim.x >> 5) {
+    float M = -INFINITY;
+    for (int32_t i = 0; i < r.n_parts; ++i) M = fmaxf(M, p.rec_lse[(int64_t)(r.rec_base + i) * p.n_q + h]);
+    float tot = 0.f;
+    for (int32_t i = 0; i < r.n_parts; ++i)
+      tot += exp2f((p.rec_lse[(int64_t)(r.rec_base + i) * p.n_q + h] - M) * kLog2e);
+    const float lse = M + logf(tot);
+    for (int32_t e = lane; e < p.d; e += 32) {
+      float acc = 0.f;
+      for (int32_t i = 0; i < r.n_parts; ++i) {
+        const int64_t rec = r.rec_base + i;
+        const float w = exp2f((p.rec_lse[rec * p.n_q + h] - lse) * kLog2e);
+        acc += w * p.rec_o[(rec * p.n_q + h) * p.d + e];
+      }
+      store_out<T>((T*)p.o + ((int64_t)b * p.n_q + h) * p.d + e, acc);
+    }
+    if (lane == 0) p.lse[(int64_t)b * p.n_q + h] = lse;
+  }
+}
+
+template <typename T, int VPL>
+cudaError_t launch_prefix_vpl(const AttnParams& p, int32_t first, int32_t n, cudaStream_t s) {
+  prefix_generic_kernel<T, VPL><<<n, 256, 0, s>>>(p, first);
+  return cudaGetLastError();
+}
+
+template <typename T, int VPL>
+cudaError_t launch_suffix_vpl(const AttnParams& p, cudaStream_t s) {
+  suffix_generic_kernel<T, VPL><<<p.n_sitems, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prefix_t(const AttnParams& p, int32_t first, int32_t n, cudaStream_t s) {
+  switch (p.d / 32) {
+    case 1: return launch_prefix_vpl<T, 1>(p, first, n, s);
+    case 2: return launch_prefix_vpl<T, 2>(p, first, n, s);
+    case 3: return launch_prefix_vpl<T, 3>(p, first, n, s);
+    case 4: return launch_prefix_vpl<T, 4>(p, first, n, s);
+    case 5: return launch_prefix_vpl<T, 5>(p, first, n, s);
+    case 6: return launch_prefix_vpl<T, 6>(p, first, n, s);
+    case 7: return launch_prefix_vpl<T, 7>(p, first, n, s);
+    case 8: return launch_prefix_vpl<T, 8>(p, first, n, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_suffix_t(const AttnParams& p, cudaStream_t s) {
+  switch (p.d / 32) {
+    case 1: return launch_suffix_vpl<T, 1>(p, s);
+    case 2: return launch_suffix_vpl<T, 2>(p, s);
+    case 3: return launch_suffix_vpl<T, 3>(p, s);
+    case 4: return launch_suffix_vpl<T, 4>(p, s);
+    case 5: return launch_suffix_vpl<T, 5>(p, s);
+    case 6: return launch_suffix_vpl<T, 6>(p, s);
+    case 7: return launch_suffix_vpl<T, 7>(p, s);
+    case 8: return launch_suffix_vpl<T, 8>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefix_generic(int32_t dtype, const AttnParams& p, int32_t first_item,
+                                  int32_t n_items, cudaStream_t s) {
+  if (n_items <= 0) return cudaSuccess;
+  return dtype == 1 ? launch_prefix_t<__nv_bfloat16>(p, first_item, n_items, s)
+                    : launch_prefix_t<float>(p, first_item, n_items, s);
+}
+
+cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream_t s) {
+  if (p.n_sitems <= 0) return cudaSuccess;
+  return dtype == 1 ? launch_suffix_t<__nv_bfloat16>(p, s) : launch_suffix_t<float>(p, s);
+}
+
+cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s) {
+  if (dtype == 1)
+    merge_kernel<__nv_bfloat16><<<p.B, 256, 0, s>>>(p);
+  else
+    merge_kernel<float><<<p.B, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace granikv

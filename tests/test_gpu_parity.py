@@ -1,0 +1,253 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances, for bf16 inputs with fp32 accumulation: o max-abs <= 1e-2, mean-abs <= 1e-3,
+lse max-abs <= 1e-3, plus relative L2 error <= 1e-2 (the near-uniform softmax of the Llama
+shape makes |o| ~ 0.01, where an absolute bound alone says little).  fp32 inputs: the
+CUDA-core paths within 1e-5; the tensor-core dense path on fp32 is held to the bf16 bounds.
+Indices (COLD token tables) must match the oracle's ring restatement bit for bit.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.allocators as AL
+import oracle.attention as OA
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BACKENDS = ["auto", "dense", "cascade"]
+
+
+def _gb():
+    from shared_prefix_kv_decode_gb300 import _binding as gb
+    return gb
+
+
+def _load(wl, **kw):
+    from shared_prefix_kv_decode_gb300.workload_io import load_workload
+    return load_workload(wl, **kw)
+
+
+def _run(lw, backend="auto", requests=None):
+    import torch
+    gb = _gb()
+    ctx = lw.cache.ctx
+    ctx.force_backend({"auto": gb.BACKEND_AUTO, "dense": gb.BACKEND_DENSE,
+                       "cascade": gb.BACKEND_CASCADE}[backend])
+    o, lse = lw.cache.decode(0, lw.q, lw.batch)
+    ctx.sync_status(lw.cache.stream())
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    return o, lse
+
+
+def assert_close(o, lse, o_ref, lse_ref, dtype, what="", dense=False):
+    err = np.abs(o - o_ref)
+    lerr = np.abs(lse - lse_ref)
+    rel = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
+    info = f"{what}: max {err.max():.3e} mean {err.mean():.3e} lse {lerr.max():.3e} rel {rel:.3e}"
+    if dtype == "f32" and not dense:
+        assert err.max() <= 1e-5 and lerr.max() <= 1e-5, info
+    else:
+        assert err.max() <= 1e-2, info
+        assert err.mean() <= 1e-3, info
+        assert lerr.max() <= 1e-3, info
+        assert rel <= 1e-2, info
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_tiny_fp32(cuda_ok, seed, backend):
+    wl = W.tiny_fp32(seed)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"tiny seed {seed} {backend}", dense=(backend == "dense"))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("backend", BACKENDS)
+@pytest.mark.parametrize("q_scale", [1.0 / math.sqrt(128.0), 1.0])
+def test_small_mixed_bf16(cuda_ok, seed, backend, q_scale):
+    """Ragged prefixes (1000, 333), a prefix that fell back to COLD, a prefix-only request, a
+    prefix-less request, ragged suffixes; near-uniform and peaked queries."""
+    wl = W.small_mixed(seed, dtype="bf16", q_scale=q_scale)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"small_mixed seed {seed} {backend} q {q_scale}")
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_small_mixed_fp32(cuda_ok, backend):
+    wl = W.small_mixed(5, dtype="f32", n_q=8, n_kv=2, d=64, q_scale=1.0)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"small_mixed fp32 {backend}", dense=(backend == "dense"))
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_needles_locate_the_right_token(cuda_ok, backend):
+    """Planted keys in the HOT prefix, in a COLD suffix and in a COLD-resident prefix: the
+    output must be the planted token's value, so any gather or slot error is gross."""
+    needles = [(0, 17, 3, 30.0), (1, 1005, 0, 30.0), (4, 250, 7, 30.0), (6, 100, 5, 30.0),
+               (8, 199, 2, 30.0), (3, 999, 6, 30.0)]
+    wl = W.small_mixed(7, dtype="bf16", q_scale=1.0, needles=needles)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"needles {backend}")
+    for (b, pos, j, _) in needles:
+        K, V = OA.logical_kv(wl, b)
+        for h in range(j * wl.spec.g, (j + 1) * wl.spec.g):
+            assert np.max(np.abs(o[b, h] - V[pos, j])) <= 0.06
+
+
+def test_cold_tables_match_oracle_ring_bit_exact(cuda_ok):
+    wl = W.small_mixed(3, dtype="bf16")
+    lw = _load(wl)
+    ring = AL.ColdRing(wl.cold_order)
+    tables = [[] for _ in range(wl.spec.B)]
+    for r in wl.append_schedule:
+        ring.alloc([int(x) for x in r], tables)
+    got = lw.cache.req_to_slot.cpu().numpy()
+    lens = lw.cache.suffix_len.cpu().numpy()
+    for b in range(wl.spec.B):
+        assert lens[b] == len(tables[b]) == wl.cold_len(b)
+        assert list(got[b, :lens[b]]) == tables[b]
+    assert lw.cache.ctx.cold_free_count() == ring.n_free
+
+
+def test_cold_pool_contents_bit_exact(cuda_ok):
+    """Every appended token sits in its slot byte for byte, in every layer."""
+    import torch
+    wl = W.small_mixed(4, dtype="bf16")
+    lw = _load(wl, n_layers=2)
+    table = lw.cache.req_to_slot.cpu().numpy()
+    for layer in range(2):
+        kp = lw.cache.k_pools[layer].float().cpu().numpy()
+        vp = lw.cache.v_pools[layer].float().cpu().numpy()
+        for b in range(wl.spec.B):
+            L = wl.cold_len(b)
+            assert np.array_equal(kp[table[b, :L]], wl.cold_k(b))
+            assert np.array_equal(vp[table[b, :L]], wl.cold_v(b))
+        for i, L in enumerate(wl.spec.prefix_lens):
+            if not wl.spec.prefix_in_hot[i]:
+                continue
+            sid = lw.slab_ids[wl.spec.req_prefix.index(i)]
+            off, ln = lw.cache.ctx.hot_info(sid)
+            assert ln == L
+            assert np.array_equal(kp[off:off + L], wl.prefix_k(i))
+            assert np.array_equal(vp[off:off + L], wl.prefix_v(i))
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_cold_slot_permutation_invariance(cuda_ok, backend):
+    """Another COLD slot order leaves o and lse unchanged, bit for bit (the kernels' work split
+    depends only on lengths, so the arithmetic is the same)."""
+    wl1 = W.small_mixed(6, dtype="bf16", q_scale=1.0)
+    wl2 = W.small_mixed(6, dtype="bf16", q_scale=1.0)
+    rng = np.random.default_rng(99)
+    s = wl2.spec
+    wl2._cache["cold"] = (s.n_hot + rng.permutation(s.n_slots - s.n_hot)).astype(np.int32)
+    o1, l1 = _run(_load(wl1), backend)
+    o2, l2 = _run(_load(wl2), backend)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_backends_agree(cuda_ok):
+    wl = W.small_mixed(8, dtype="bf16", q_scale=1.0)
+    lw = _load(wl)
+    od, ld = _run(lw, "dense")
+    oc, lc = _run(lw, "cascade")
+    assert np.max(np.abs(od - oc)) <= 1e-2 and np.max(np.abs(ld - lc)) <= 1e-3
+
+
+def test_run_to_run_deterministic(cuda_ok):
+    wl = W.small_mixed(9, dtype="bf16", q_scale=1.0)
+    lw = _load(wl)
+    for backend in BACKENDS:
+        a = _run(lw, backend)
+        b = _run(lw, backend)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_device_check_reports_bad_slot_and_context_survives(cuda_ok):
+    """A token table entry outside the COLD range is skipped by the kernel's own bounds check
+    and reported as a device check failure; the context keeps working afterwards."""
+    gb = _gb()
+    wl = W.small_mixed(10, dtype="bf16")
+    lw = _load(wl)
+    good = lw.cache.req_to_slot.clone()
+    lw.cache.req_to_slot[4, 3] = 0  # slot 0 is HOT, not COLD
+    with pytest.raises(gb.DeviceCheckFailed):
+        _run(lw, "cascade")
+    lw.cache.req_to_slot.copy_(good)
+    o, lse = _run(lw, "cascade")
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", "after device check")
+
+
+def test_cold_exhaustion_is_all_or_nothing(cuda_ok):
+    import torch
+    gb = _gb()
+    from shared_prefix_kv_decode_gb300.cache import GraniKVCache
+    cache = GraniKVCache(n_layers=1, n_q=8, n_kv=2, head_dim=64, dtype=gb.DTYPE_F32, n_slots=100,
+                         max_batch=3, cap=64)
+    free0 = cache.ctx.cold_free_count()
+    assert free0 == 80
+    k = torch.zeros((70, 2, 64), device="cuda")
+    cache.append([30, 0, 40], [k], [k])
+    assert cache.ctx.cold_free_count() == 10
+    with pytest.raises(gb.NoColdSpace):
+        cache.append([5, 5, 5], [k[:15]], [k[:15]])
+    assert cache.ctx.cold_free_count() == 10
+    assert cache.suffix_len.cpu().tolist() == [30, 0, 40]
+
+
+def test_cold_free_returns_slots_fifo(cuda_ok):
+    import torch
+    gb = _gb()
+    from shared_prefix_kv_decode_gb300.cache import GraniKVCache
+    order = list(range(20, 100))[::-1]
+    cache = GraniKVCache(n_layers=1, n_q=8, n_kv=2, head_dim=64, dtype=gb.DTYPE_F32, n_slots=100,
+                         max_batch=2, cap=128, cold_init_order=order)
+    ring = AL.ColdRing(order)
+    tables = [[], []]
+    k = torch.zeros((80, 2, 64), device="cuda")
+    cache.append([50, 30], [k], [k])
+    ring.alloc([50, 30], tables)
+    freed = torch.tensor(tables[0][:20], dtype=torch.int32, device="cuda")
+    cache.ctx.cold_free(freed, 20, cache.stream())
+    ring.free(tables[0][:20])
+    cache.append([0, 15], [k[:15]], [k[:15]])
+    ring.alloc([0, 15], tables)
+    got = cache.req_to_slot.cpu().numpy()
+    assert list(got[1, :45]) == tables[1]
+    cache.ctx.sync_status()
+
+
+FULL = {
+    "llama8b_single_prefix_16k": (W.llama8b_single_prefix_16k, [0, 17, 40, 63]),
+    "hetero_multi_prefix_k8": (W.hetero_multi_prefix_k8, [0, 31, 77, 159]),
+    "qwen_tp1_16k": (W.qwen_tp1_16k, [0, 64, 127]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_full_size_sampled(cuda_ok, name):
+    """Full-size configurations, the same launch configuration the benchmark times, checked on
+    sampled requests the oracle computes one by one, for every backend."""
+    fn, sample = FULL[name]
+    wl = fn(0)
+    lw = _load(wl)
+    refs = {b: OA.request_attention(wl, b) for b in sample}
+    for backend in BACKENDS:
+        o, lse = _run(lw, backend)
+        for b in sample:
+            assert_close(o[b], lse[b], refs[b][0], refs[b][1], "bf16", f"{name} b={b} {backend}")
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
