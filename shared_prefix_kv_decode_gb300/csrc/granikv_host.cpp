@@ -8,6 +8,8 @@
 #include "../../include/granikv.h"
 #include "internal.h"
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -58,14 +60,19 @@ struct granikv_ctx {
   granikv_plan* own_plan = nullptr;
   // enqueued work, for attribution
   int64_t n_kernels = 0, n_copies = 0;
+  // TMA descriptors of each layer's K and V pools (dense backend), valid when has_tmaps
+  std::vector<CUtensorMap> tmap_k, tmap_v;
+  bool has_tmaps = false;
 };
 
 struct granikv_plan {
   granikv_ctx* ctx = nullptr;
   std::vector<unsigned char> blob;  // device image of the plan
-  size_t off_groups = 0, off_group_req = 0, off_req = 0, off_pitems = 0, off_sitems = 0;
-  int32_t n_groups = 0, n_pitems = 0, n_sitems = 0, B = 0, n_records = 0;
+  size_t off_groups = 0, off_group_req = 0, off_req = 0, off_pitems = 0, off_sitems = 0, off_scta = 0;
+  int32_t n_groups = 0, n_pitems = 0, n_sitems = 0, n_scta = 0, B = 0, n_records = 0;
   int32_t suffix_impl = kImplGeneric;
+  int32_t pitem_first[kNumImpl] = {0, 0, 0, 0};  // prefix items are ordered by implementation
+  int32_t pitem_count[kNumImpl] = {0, 0, 0, 0};
   std::vector<granikv_group_info> info;
   std::vector<int32_t> group_impl;
   uint64_t version = 0;
@@ -102,9 +109,42 @@ bool has_device(const granikv_ctx* c) { return c && !c->cfg.host_only && c->d_ri
 
 // Which prefix implementation serves a group of this shape and backend.
 int32_t prefix_impl_for(const granikv_ctx* c, int32_t backend) {
-  (void)backend;
-  (void)c;
+  if (c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128) {
+    if (backend == GRANIKV_BACKEND_DENSE && (c->has_tmaps || c->cfg.host_only)) return kImplDenseTc;
+    return kImplCascadeMma;
+  }
   return kImplGeneric;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// A pool [n_slots, n_kv, 128] bf16 as a 3-D tensor (dim, head, slot) with 64 x 1 x 128 boxes and
+// the 128-byte swizzle the tcgen05 operand descriptors expect.
+bool encode_pool_map(CUtensorMap* m, void* base, int64_t n_slots, int32_t n_kv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)n_kv, (cuuint64_t)n_slots};
+  cuuint64_t strides[2] = {256, (cuuint64_t)n_kv * 256};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 int32_t rows_per_cta_for(int32_t impl) {
@@ -216,6 +256,17 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
     if (e == cudaSuccess)
       e = cudaMemcpy(c->d_ring, init.data(), sizeof(int32_t) * c->n_cold, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int32_t) * 4);
+    if (e == cudaSuccess && cfg->dtype == GRANIKV_DTYPE_BF16 && cfg->head_dim == 128 && c->cc_major == 10) {
+      c->tmap_k.resize(cfg->n_layers);
+      c->tmap_v.resize(cfg->n_layers);
+      bool ok = true;
+      for (int32_t l = 0; l < cfg->n_layers && ok; ++l) {
+        ok = ((uintptr_t)c->kpool[l] % 16 == 0) && ((uintptr_t)c->vpool[l] % 16 == 0) &&
+             encode_pool_map(&c->tmap_k[l], c->kpool[l], cfg->n_slots, cfg->n_kv) &&
+             encode_pool_map(&c->tmap_v[l], c->vpool[l], cfg->n_slots, cfg->n_kv);
+      }
+      c->has_tmaps = ok;
+    }
     if (e != cudaSuccess) {
       if (c->d_ring) cudaFree(c->d_ring);
       if (c->d_err) cudaFree(c->d_err);
@@ -471,8 +522,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     dg.pad = 0;
     prefix_units += (int64_t)n_kv * dg.row_blocks * dg.L_p;
   }
-  // 3. prefix split length shared by all groups so the prefix pass fills ~2 waves
+  // 3. prefix split length shared by all groups so the prefix pass fills the GPU
   int64_t target = 2LL * c->num_sms;
+  for (int32_t i = 0; i < G; ++i)
+    if (groups[i].impl != kImplGeneric) target = c->num_sms;
   for (int32_t i = 0; i < G; ++i) {
     DevGroup& dg = groups[i];
     int64_t tile = tile_tokens_for(dg.impl);
@@ -490,12 +543,18 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     gi.n_splits = dg.n_splits;
     gi.slot_offset = dg.slab_off;
   }
-  // 4. suffix chunking: chunk length so that the suffix pass fills ~2 waves
+  // 4. suffix: cut the concatenation of all requests' COLD tokens into one equal run per
+  //    token-CTA (stream-K); each request segment inside a run is one work item and record
   int64_t T = 0;
   for (int32_t b = 0; b < B; ++b) T += bt->seq_len[b];
-  int32_t suffix_impl = kImplGeneric;
-  int64_t chunk = (T + target - 1) / std::max<int64_t>(target, 1);
-  chunk = std::max<int64_t>(64, std::min<int64_t>(2048, (chunk + 31) / 32 * 32));
+  const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
+  const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
+  int32_t n_scta = 0;
+  int64_t quota = 1;
+  if (T > 0) {
+    n_scta = (int32_t)std::min<int64_t>(c->num_sms, (T + 15) / 16);
+    quota = (T + n_scta - 1) / n_scta;
+  }
 
   // 5. records and work items
   std::vector<int32_t> group_req(begin[G]);
@@ -505,38 +564,54 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       if (req_group[b] >= 0) group_req[fill[req_group[b]]++] = b;
   }
   std::vector<DevReq> reqs(B);
-  int64_t rec = 0;
   std::vector<DevSuffixItem> sitems;
-  sitems.reserve(B + T / chunk + 1);
+  std::vector<int32_t> scta_begin(n_scta + 1, 0);
+  sitems.reserve(B + n_scta + 1);
+  int64_t rec = 0;
+  int32_t cta = 0;
+  int64_t used = 0;
   for (int32_t b = 0; b < B; ++b) {
     DevReq& r = reqs[b];
     r.rec_base = (int32_t)rec;
     r.n_prefix = req_group[b] >= 0 ? groups[req_group[b]].n_splits : 0;
-    int32_t L = bt->seq_len[b];
-    int32_t n_chunks = (int32_t)((L + chunk - 1) / chunk);
-    r.n_parts = r.n_prefix + n_chunks;
+    const int32_t L = bt->seq_len[b];
     r.seq_len = L;
-    for (int32_t k = 0; k < n_chunks; ++k) {
+    int32_t k = 0;
+    for (int64_t t = 0; t < L;) {
+      const int64_t take = std::min<int64_t>(L - t, quota - used);
       DevSuffixItem it;
       it.b = b;
-      it.t0 = (int32_t)(k * chunk);
-      it.t1 = (int32_t)std::min<int64_t>(L, (k + 1) * chunk);
+      it.t0 = (int32_t)t;
+      it.t1 = (int32_t)(t + take);
       it.rec = (int32_t)(rec + r.n_prefix + k);
       sitems.push_back(it);
+      ++k;
+      t += take;
+      used += take;
+      if (used == quota) {
+        ++cta;
+        if (cta <= n_scta) scta_begin[std::min(cta, n_scta)] = (int32_t)sitems.size();
+        used = 0;
+      }
     }
+    r.n_parts = r.n_prefix + k;
     rec += r.n_parts;
   }
+  for (int32_t i = std::min(cta + 1, n_scta); i <= n_scta; ++i) scta_begin[i] = (int32_t)sitems.size();
   if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
-  // longest chunks first (a full chunk never follows a shorter one)
-  std::stable_sort(sitems.begin(), sitems.end(), [](const DevSuffixItem& a, const DevSuffixItem& b) {
-    return (a.t1 - a.t0) > (b.t1 - b.t0);
-  });
+  // prefix items grouped by kernel; within a group the row blocks of one (KV head, piece)
+  // are adjacent so they share the piece's K/V through L2
   std::vector<DevPrefixItem> pitems;
-  for (int32_t i = 0; i < G; ++i) {
-    const DevGroup& dg = groups[i];
-    for (int32_t j = 0; j < n_kv; ++j)
-      for (int32_t s = 0; s < dg.n_splits; ++s)
-        for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
+  for (int32_t impl = 0; impl < kNumImpl; ++impl) {
+    p->pitem_first[impl] = (int32_t)pitems.size();
+    for (int32_t i = 0; i < G; ++i) {
+      const DevGroup& dg = groups[i];
+      if (dg.impl != impl) continue;
+      for (int32_t j = 0; j < n_kv; ++j)
+        for (int32_t s = 0; s < dg.n_splits; ++s)
+          for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
+    }
+    p->pitem_count[impl] = (int32_t)pitems.size() - p->pitem_first[impl];
   }
 
   // 6. pack the device image
@@ -550,7 +625,9 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->off_pitems = off;
   off = align_up(off + sizeof(DevPrefixItem) * pitems.size(), 16);
   p->off_sitems = off;
-  off = align_up(off + sizeof(DevSuffixItem) * sitems.size(), 256);
+  off = align_up(off + sizeof(DevSuffixItem) * sitems.size(), 16);
+  p->off_scta = off;
+  off = align_up(off + sizeof(int32_t) * scta_begin.size(), 256);
   p->blob.assign(off, 0);
   if (G) std::memcpy(p->blob.data() + p->off_groups, groups.data(), sizeof(DevGroup) * G);
   if (!group_req.empty())
@@ -560,11 +637,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     std::memcpy(p->blob.data() + p->off_pitems, pitems.data(), sizeof(DevPrefixItem) * pitems.size());
   if (!sitems.empty())
     std::memcpy(p->blob.data() + p->off_sitems, sitems.data(), sizeof(DevSuffixItem) * sitems.size());
+  std::memcpy(p->blob.data() + p->off_scta, scta_begin.data(), sizeof(int32_t) * scta_begin.size());
   p->n_groups = G;
   p->n_pitems = (int32_t)pitems.size();
   p->n_sitems = (int32_t)sitems.size();
   p->B = B;
   p->n_records = (int32_t)rec;
+  p->n_scta = n_scta;
   p->suffix_impl = suffix_impl;
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
@@ -675,6 +754,8 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.n_pitems = p->n_pitems;
   a.sitems = (const DevSuffixItem*)(wsb + p->off_sitems);
   a.n_sitems = p->n_sitems;
+  a.scta_begin = (const int32_t*)(wsb + p->off_scta);
+  a.n_scta = p->n_scta;
   size_t off = align_up(p->blob.size(), 256);
   a.rec_o = (float*)(wsb + off);
   off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q * c->cfg.head_dim, 256);
@@ -684,12 +765,23 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.checks = c->checks;
 
   cudaError_t e = cudaSuccess;
-  if (p->n_pitems > 0) {
-    e = launch_prefix_generic(c->cfg.dtype, a, 0, p->n_pitems, s);
+  if (p->pitem_count[kImplGeneric] > 0) {
+    e = launch_prefix_generic(c->cfg.dtype, a, p->pitem_first[kImplGeneric], p->pitem_count[kImplGeneric], s);
+    c->n_kernels += 1;
+  }
+  if (e == cudaSuccess && p->pitem_count[kImplCascadeMma] > 0) {
+    e = launch_cascade_mma(a, p->pitem_first[kImplCascadeMma], p->pitem_count[kImplCascadeMma], s);
+    c->n_kernels += 1;
+  }
+  if (e == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
+    if (!c->has_tmaps) return GRANIKV_ERR_UNSUPPORTED;
+    e = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
+                        c->tmap_v[layer], s);
     c->n_kernels += 1;
   }
   if (e == cudaSuccess && p->n_sitems > 0) {
-    e = launch_suffix_generic(c->cfg.dtype, a, s);
+    e = p->suffix_impl == kImplSuffixMma ? launch_suffix_mma(a, a.scta_begin, p->n_scta, s)
+                                         : launch_suffix_generic(c->cfg.dtype, a, s);
     c->n_kernels += 1;
   }
   if (e == cudaSuccess) {

@@ -8,6 +8,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace granikv {
@@ -77,6 +78,8 @@ struct AttnParams {
   int32_t n_pitems;
   const DevSuffixItem* sitems;
   int32_t n_sitems;
+  const int32_t* scta_begin;  // [n_scta + 1]: first suffix item of each suffix token-CTA
+  int32_t n_scta;
   float* rec_o;           // [n_records, n_q, d]
   float* rec_lse;         // [n_records, n_q]
   int32_t n_records;
@@ -101,5 +104,11 @@ cudaError_t launch_prefix_generic(int32_t dtype, const AttnParams& p, int32_t fi
                                   int32_t n_items, cudaStream_t s);
 cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s);
+cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int32_t n_cta, cudaStream_t s);
+cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
+cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
+                            const CUtensorMap& tmv, cudaStream_t s);
+
+constexpr int kNumImpl = 4;
 
 }  // namespace granikv

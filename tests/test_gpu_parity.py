@@ -91,6 +91,18 @@ def test_small_mixed_fp32(cuda_ok, backend):
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
+@pytest.mark.parametrize("q_scale", [1.0 / math.sqrt(128.0), 1.0, 3.0])
+def test_medium_shared_prefix(cuda_ok, backend, q_scale):
+    """280 query rows per KV head (three 128-row blocks, the last partial) over a 3000-token
+    prefix (several pieces, ragged last tile); q_scale 3 makes the running max jump often."""
+    wl = W.medium_shared(1, q_scale=q_scale)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"medium {backend} q {q_scale}")
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
 def test_needles_locate_the_right_token(cuda_ok, backend):
     """Planted keys in the HOT prefix, in a COLD suffix and in a COLD-resident prefix: the
     output must be the planted token's value, so any gather or slot error is gross."""

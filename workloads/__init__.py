@@ -17,5 +17,6 @@ from .synth import (  # noqa: F401
     qwen_tp1_16k,
     dispatch_sweep_cell,
     small_mixed,
+    medium_shared,
     NAMED,
 )

@@ -381,10 +381,24 @@ def small_mixed(seed: int = 0, dtype: str = "bf16", n_q: int = 32, n_kv: int = 8
     return Workload(spec, seed)
 
 
+def medium_shared(seed: int = 0, B: int = 70, L_p: int = 3000, q_scale: float = 1.0,
+                  needles: Sequence[tuple] = ()) -> Workload:
+    """One ragged prefix shared by enough requests for several 128-row blocks (B*g rows, the
+    last block partial) and several L_p pieces, plus short ragged suffixes."""
+    rng = _struct_rng(seed, "medium")
+    spec = WorkloadSpec(
+        name="medium_shared", dtype="bf16", n_q=32, n_kv=8, d=128,
+        prefix_lens=[L_p], req_prefix=[0] * B,
+        suffix_lens=[int(x) for x in rng.integers(1, 100, size=B)],
+        q_scale=q_scale, n_slots=32768, needles=list(needles), schedule_max_chunk=64)
+    return Workload(spec, seed)
+
+
 NAMED: Dict[str, Callable[..., Workload]] = {
     "tiny_fp32": tiny_fp32,
     "llama8b_single_prefix_16k": llama8b_single_prefix_16k,
     "hetero_multi_prefix_k8": hetero_multi_prefix_k8,
     "qwen_tp1_16k": qwen_tp1_16k,
     "small_mixed": small_mixed,
+    "medium_shared": medium_shared,
 }
