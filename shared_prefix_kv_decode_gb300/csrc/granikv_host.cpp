@@ -70,6 +70,7 @@ struct granikv_plan {
   std::vector<unsigned char> blob;  // device image of the plan
   size_t off_groups = 0, off_group_req = 0, off_req = 0, off_pitems = 0, off_sitems = 0, off_scta = 0;
   int32_t n_groups = 0, n_pitems = 0, n_sitems = 0, n_scta = 0, B = 0, n_records = 0;
+  int64_t n_prefix_records = 0;
   int32_t suffix_impl = kImplGeneric;
   int32_t pitem_first[kNumImpl] = {0, 0, 0, 0};  // prefix items are ordered by implementation
   int32_t pitem_count[kNumImpl] = {0, 0, 0, 0};
@@ -643,6 +644,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->n_sitems = (int32_t)sitems.size();
   p->B = B;
   p->n_records = (int32_t)rec;
+  p->n_prefix_records = 0;
+  for (int32_t b = 0; b < B; ++b) p->n_prefix_records += reqs[b].n_prefix;
   p->n_scta = n_scta;
   p->suffix_impl = suffix_impl;
   p->group_impl.resize(G);
@@ -665,11 +668,32 @@ granikv_status granikv_plan_group(const granikv_plan* p, int32_t i, granikv_grou
 }
 
 namespace {
+// Workspace bound that depends only on the batch size, the prefix pieces and the SM count, so a
+// workspace sized once stays large enough while the suffixes grow step after step: the plan
+// holds at most B + n_sm suffix segments (each token-CTA boundary adds at most one), and each
+// request has one record per prefix piece and per suffix segment.
 size_t workspace_bytes(const granikv_ctx* c, const granikv_plan* p) {
-  size_t off = align_up(p->blob.size(), 256);
-  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q * c->cfg.head_dim, 256);
-  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q, 256);
+  const size_t max_sitems = (size_t)p->B + (size_t)c->num_sms + 1;
+  size_t blob = p->off_sitems + align_up(sizeof(DevSuffixItem) * max_sitems, 16) +
+                align_up(sizeof(int32_t) * ((size_t)c->num_sms + 1), 256);
+  blob = std::max(blob, p->blob.size());
+  const size_t max_records = (size_t)p->n_prefix_records + max_sitems;
+  size_t off = align_up(blob, 256);
+  off += align_up(sizeof(float) * max_records * c->cfg.n_q * c->cfg.head_dim, 256);
+  off += align_up(sizeof(float) * max_records * c->cfg.n_q, 256);
   return off;
+}
+size_t records_offset(const granikv_ctx* c, const granikv_plan* p) {
+  (void)c;
+  const size_t max_sitems = (size_t)p->B + (size_t)c->num_sms + 1;
+  size_t blob = p->off_sitems + align_up(sizeof(DevSuffixItem) * max_sitems, 16) +
+                align_up(sizeof(int32_t) * ((size_t)c->num_sms + 1), 256);
+  blob = std::max(blob, p->blob.size());
+  return align_up(blob, 256);
+}
+size_t lse_offset(const granikv_ctx* c, const granikv_plan* p) {
+  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + (size_t)c->num_sms + 1;
+  return records_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q * c->cfg.head_dim, 256);
 }
 }  // namespace
 
@@ -756,10 +780,8 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.n_sitems = p->n_sitems;
   a.scta_begin = (const int32_t*)(wsb + p->off_scta);
   a.n_scta = p->n_scta;
-  size_t off = align_up(p->blob.size(), 256);
-  a.rec_o = (float*)(wsb + off);
-  off += align_up(sizeof(float) * (size_t)p->n_records * c->cfg.n_q * c->cfg.head_dim, 256);
-  a.rec_lse = (float*)(wsb + off);
+  a.rec_o = (float*)(wsb + records_offset(c, p));
+  a.rec_lse = (float*)(wsb + lse_offset(c, p));
   a.n_records = p->n_records;
   a.err = c->d_err;
   a.checks = c->checks;

@@ -158,31 +158,62 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* dst, flo
   *dst = __float2bfloat16_rn(v);
 }
 
-// Merge: one CTA per request, one warp per head in turn.  lse = M + ln sum_i e^(lse_i - M),
-// o = sum_i e^(lse_i - lse) o_i over the request's partial-state records.
-template <typename T>
+// Merge: one warp per (request, head).  lse = M + ln sum_i e^(lse_i - M) and
+// o = sum_i e^(lse_i - lse) o_i over the request's partial-state records; each lane owns
+// head_dim/32 consecutive elements, so every record row is read with coalesced accesses, and
+// the records loop is unrolled so several rows are in flight at once.
+template <typename T, int VPL>
 __global__ void __launch_bounds__(256) merge_kernel(AttnParams p) {
-  const int32_t b = blockIdx.x;
-  const DevReq r = p.reqs[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int32_t h = warp; h < p.n_q; h += blockDim.x >> 5) {
-    float M = -INFINITY;
-    for (int32_t i = 0; i < r.n_parts; ++i) M = fmaxf(M, p.rec_lse[(int64_t)(r.rec_base + i) * p.n_q + h]);
-    float tot = 0.f;
-    for (int32_t i = 0; i < r.n_parts; ++i)
-      tot += exp2f((p.rec_lse[(int64_t)(r.rec_base + i) * p.n_q + h] - M) * kLog2e);
-    const float lse = M + logf(tot);
-    for (int32_t e = lane; e < p.d; e += 32) {
-      float acc = 0.f;
-      for (int32_t i = 0; i < r.n_parts; ++i) {
-        const int64_t rec = r.rec_base + i;
-        const float w = exp2f((p.rec_lse[rec * p.n_q + h] - lse) * kLog2e);
-        acc += w * p.rec_o[(rec * p.n_q + h) * p.d + e];
-      }
-      store_out<T>((T*)p.o + ((int64_t)b * p.n_q + h) * p.d + e, acc);
-    }
-    if (lane == 0) p.lse[(int64_t)b * p.n_q + h] = lse;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // b * n_q + h
+  if (row >= (int64_t)p.B * p.n_q) return;
+  const int32_t b = (int32_t)(row / p.n_q);
+  const int32_t h = (int32_t)(row % p.n_q);
+  const DevReq r = p.reqs[b];
+  const float* lse_rec = p.rec_lse + (int64_t)r.rec_base * p.n_q + h;
+  float M = -INFINITY;
+  for (int32_t i = lane; i < r.n_parts; i += 32) M = fmaxf(M, lse_rec[(int64_t)i * p.n_q]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  T* dst = (T*)p.o + row * p.d + lane * VPL;
+  if (M == -INFINITY) {  // no tokens at all (only reachable after a latched device check)
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) store_out<T>(dst + k, 0.f);
+    if (lane == 0) p.lse[row] = -INFINITY;
+    return;
   }
+  float tot = 0.f;
+  for (int32_t i = lane; i < r.n_parts; i += 32) tot += exp2f((lse_rec[(int64_t)i * p.n_q] - M) * kLog2e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float lse = M + logf(tot);
+  float acc[VPL];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
+  const float* orec = p.rec_o + ((int64_t)r.rec_base * p.n_q + h) * p.d + lane * VPL;
+  const int64_t rec_stride = (int64_t)p.n_q * p.d;
+  int32_t i = 0;
+  for (; i + 4 <= r.n_parts; i += 4) {
+    float w[4], x[4][VPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      w[u] = exp2f((lse_rec[(int64_t)(i + u) * p.n_q] - lse) * kLog2e);
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) x[u][k] = orec[(i + u) * rec_stride + k];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < VPL; ++k) acc[k] += w[u] * x[u][k];
+  }
+  for (; i < r.n_parts; ++i) {
+    const float w = exp2f((lse_rec[(int64_t)i * p.n_q] - lse) * kLog2e);
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) acc[k] += w * orec[i * rec_stride + k];
+  }
+#pragma unroll
+  for (int k = 0; k < VPL; ++k) store_out<T>(dst + k, acc[k]);
+  if (lane == 0) p.lse[row] = lse;
 }
 
 template <typename T, int VPL>
@@ -241,12 +272,31 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
   return dtype == 1 ? launch_suffix_t<__nv_bfloat16>(p, s) : launch_suffix_t<float>(p, s);
 }
 
-cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s) {
-  if (dtype == 1)
-    merge_kernel<__nv_bfloat16><<<p.B, 256, 0, s>>>(p);
-  else
-    merge_kernel<float><<<p.B, 256, 0, s>>>(p);
+template <typename T, int VPL>
+cudaError_t launch_merge_vpl(const AttnParams& p, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.n_q;
+  const int grid = (int)((rows + 7) / 8);
+  merge_kernel<T, VPL><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
+  switch (p.d / 32) {
+    case 1: return launch_merge_vpl<T, 1>(p, s);
+    case 2: return launch_merge_vpl<T, 2>(p, s);
+    case 3: return launch_merge_vpl<T, 3>(p, s);
+    case 4: return launch_merge_vpl<T, 4>(p, s);
+    case 5: return launch_merge_vpl<T, 5>(p, s);
+    case 6: return launch_merge_vpl<T, 6>(p, s);
+    case 7: return launch_merge_vpl<T, 7>(p, s);
+    case 8: return launch_merge_vpl<T, 8>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s) {
+  return dtype == 1 ? launch_merge_t<__nv_bfloat16>(p, s) : launch_merge_t<float>(p, s);
 }
 
 }  // namespace granikv

@@ -1,0 +1,127 @@
+"""Re-fit the dense/cascade crossover M_sat on this GPU.
+
+GraniKV (arXiv:2608.15584), "3 GraniKV" per-step dispatch and "B.4 Per-Step Dispatch
+Trace": the dispatcher runs the dense backend when M_eff = B * n_q / n_kv >= M_sat; the pages
+measure M_sat = 1024 on A100 and say other GPUs need a re-fit ("Limitations").
+
+This sweeps the Llama-3.1-8B attention shape (32/8/128, bf16) over
+L_p in {512, 2048, 8192, 16384, 32768} x B in {1, 8, 32, 128, 256, 512} with 256 COLD tokens
+per request, timing decode attention with the backend forced to DENSE, forced to CASCADE, and
+dispatched (AUTO).  The L2 is flushed before every timed call.  M_sat is the smallest grid
+M_eff at which dense is no slower than cascade for every L_p >= 2048, at that M_eff and at
+every larger one.
+
+  python -m shared_prefix_kv_decode_gb300.msat_fit [--reps 20] [--json out.json]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import statistics
+import sys
+
+LPS = [512, 2048, 8192, 16384, 32768]
+BS = [1, 8, 32, 128, 256, 512]
+SUFFIX = 256
+
+
+def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch):
+    from .cache import GraniKVCache
+
+    n_q, n_kv, d = 32, 8, 128
+    n_cold = B * SUFFIX + 1024
+    n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil(n_cold / 0.8)) + 8)
+    cache = GraniKVCache(n_layers=1, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
+                         max_batch=B, cap=SUFFIX + 64)
+    dev = cache.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(L_p * 1000 + B)
+    k = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+    sid = cache.admit_prefix(L_p, [k], [v])
+    kn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+    vn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+    cache.append([SUFFIX] * B, [kn], [vn])
+    q = (torch.randn((B, n_q, d), generator=gen, device=dev) / math.sqrt(d)).to(torch.bfloat16)
+    batch = cache.batch([sid] * B)
+    out = {}
+    stream = cache.stream()
+    for name, backend in (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE), ("auto", gb.BACKEND_AUTO)):
+        cache.ctx.force_backend(backend)
+        plan = cache.ctx.dispatch(batch)
+        o, lse = cache.decode(0, q, batch, plan)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            cache.decode(0, q, batch, plan, o, lse)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1000.0)
+        out[name] = statistics.median(times)
+        out[name + "_backend"] = gb.BACKEND_NAMES[plan.groups()[0]["backend"]]
+    cache.ctx.sync_status(stream)
+    return out
+
+
+def fit_msat(rows, g=4):
+    """Smallest grid M_eff such that dense <= cascade for every L_p >= 2048 at that M_eff and all
+    larger grid M_eff; None if dense never wins that way."""
+    meffs = sorted({r["B"] * g for r in rows})
+    ok = {}
+    for me in meffs:
+        cells = [r for r in rows if r["B"] * g == me and r["L_p"] >= 2048]
+        ok[me] = all(r["dense_us"] <= r["cascade_us"] for r in cells)
+    for i, me in enumerate(meffs):
+        if all(ok[m] for m in meffs[i:]):
+            return me
+    return None
+
+
+def main(argv=None):
+    import torch
+    from . import _binding as gb
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--reps", type=int, default=15)
+    ap.add_argument("--json", default=None)
+    ap.add_argument("--lps", default=",".join(map(str, LPS)))
+    ap.add_argument("--bs", default=",".join(map(str, BS)))
+    a = ap.parse_args(argv)
+    torch.cuda.set_device(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    scratch = torch.empty((max(2 * l2, 256 << 20),), dtype=torch.uint8, device="cuda")
+
+    def flush():
+        scratch.fill_(1)
+
+    rows = []
+    for L_p in [int(x) for x in a.lps.split(",")]:
+        for B in [int(x) for x in a.bs.split(",")]:
+            r = _time_cell(L_p, B, a.reps, None, flush, gb, torch)
+            row = {"L_p": L_p, "B": B, "m_eff": 4 * B, "dense_us": r["dense"], "cascade_us": r["cascade"],
+                   "auto_us": r["auto"], "auto_backend": r["auto_backend"]}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+            torch.cuda.empty_cache()
+    m_sat = fit_msat(rows)
+    print(f"# fitted M_sat = {m_sat}")
+    print("| L_p | B | M_eff | dense us | cascade us | auto us | auto -> | best/auto |")
+    print("|---|---|---|---|---|---|---|---|")
+    for r in rows:
+        best = min(r["dense_us"], r["cascade_us"])
+        print(f"| {r['L_p']} | {r['B']} | {r['m_eff']} | {r['dense_us']:.1f} | {r['cascade_us']:.1f} | "
+              f"{r['auto_us']:.1f} | {r['auto_backend']} | {best / r['auto_us']:.3f} |")
+    if a.json:
+        with open(a.json, "w") as f:
+            json.dump({"rows": rows, "m_sat": m_sat}, f, indent=1)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -44,7 +44,10 @@ def _run(lw, backend="auto", requests=None):
     return o, lse
 
 
-def assert_close(o, lse, o_ref, lse_ref, dtype, what="", dense=False):
+def assert_close(o, lse, o_ref, lse_ref, dtype, what="", dense=False, vmax=None):
+    """vmax: for stress inputs far more peaked than the configured workloads, the max-abs bound
+    becomes the one bf16 arithmetic guarantees: P and o are each rounded once to bf16 (unit
+    roundoff 2^-8), so |o - o_ref| <= 2^-8 (|o_ref| + max|v|)."""
     err = np.abs(o - o_ref)
     lerr = np.abs(lse - lse_ref)
     rel = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
@@ -52,7 +55,8 @@ def assert_close(o, lse, o_ref, lse_ref, dtype, what="", dense=False):
     if dtype == "f32" and not dense:
         assert err.max() <= 1e-5 and lerr.max() <= 1e-5, info
     else:
-        assert err.max() <= 1e-2, info
+        max_abs = 1e-2 if vmax is None else max(1e-2, 2.0 ** -8 * (np.abs(o_ref).max() + vmax))
+        assert err.max() <= max_abs, info
         assert err.mean() <= 1e-3, info
         assert lerr.max() <= 1e-3, info
         assert rel <= 1e-2, info
@@ -99,7 +103,10 @@ def test_medium_shared_prefix(cuda_ok, backend, q_scale):
     lw = _load(wl)
     o, lse = _run(lw, backend)
     o_ref, lse_ref = OA.decode_attention(wl)
-    assert_close(o, lse, o_ref, lse_ref, "bf16", f"medium {backend} q {q_scale}")
+    vmax = None
+    if q_scale > 1.0:  # stress: far more peaked than any configured workload
+        vmax = max(np.abs(wl.prefix_v(0)).max(), max(np.abs(wl.suffix_v(b)).max() for b in range(wl.spec.B)))
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"medium {backend} q {q_scale}", vmax=vmax)
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
