@@ -150,17 +150,17 @@ bool encode_pool_map(CUtensorMap* m, void* base, int64_t n_slots, int32_t n_kv) 
 
 int32_t rows_per_cta_for(int32_t impl) {
   switch (impl) {
-    case kImplDenseTc: return 128;
-    case kImplCascadeMma: return 64;
-    default: return 16;
+    case kImplDenseTc: return kDenseRows;
+    case kImplCascadeMma: return kCascadeRows;
+    default: return kGenericRows;
   }
 }
 
 int32_t tile_tokens_for(int32_t impl) {
   switch (impl) {
-    case kImplDenseTc: return 128;
-    case kImplCascadeMma: return 64;
-    default: return 32;
+    case kImplDenseTc: return kDenseTile;
+    case kImplCascadeMma: return kCascadeTile;
+    default: return kGenericTile;
   }
 }
 
@@ -502,7 +502,6 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   // 2. backend per group: M_eff = B_g * n_q / n_kv, dense iff M_eff >= M_sat
   std::vector<DevGroup> groups(G);
   p->info.assign(G, granikv_group_info{});
-  int64_t prefix_units = 0;  // sum over groups of n_kv * row_blocks * L_p
   std::vector<int32_t> begin(G + 1, 0);
   for (int32_t i = 0; i < G; ++i) begin[i + 1] = begin[i] + grp_count[i];
   for (int32_t i = 0; i < G; ++i) {
@@ -520,21 +519,49 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     dg.impl = prefix_impl_for(c, backend);
     dg.rows_per_cta = rows_per_cta_for(dg.impl);
     dg.row_blocks = (m_eff + dg.rows_per_cta - 1) / dg.rows_per_cta;
-    dg.pad = 0;
-    prefix_units += (int64_t)n_kv * dg.row_blocks * dg.L_p;
   }
-  // 3. prefix split length shared by all groups so the prefix pass fills the GPU
+  // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
+  //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
+  //    kernels run one CTA per SM, so their target is one full wave.
   int64_t target = 2LL * c->num_sms;
   for (int32_t i = 0; i < G; ++i)
     if (groups[i].impl != kImplGeneric) target = c->num_sms;
+  {
+    int64_t max_tiles = 1;
+    for (int32_t i = 0; i < G; ++i) {
+      const int64_t tile = tile_tokens_for(groups[i].impl);
+      max_tiles = std::max<int64_t>(max_tiles, (groups[i].L_p + tile - 1) / tile);
+    }
+    auto ctas_for = [&](int64_t piece_tiles) {
+      int64_t n = 0;
+      for (int32_t i = 0; i < G; ++i) {
+        const int64_t tile = tile_tokens_for(groups[i].impl);
+        const int64_t t = (groups[i].L_p + tile - 1) / tile;
+        n += (int64_t)n_kv * groups[i].row_blocks * ((t + piece_tiles - 1) / piece_tiles);
+      }
+      return n;
+    };
+    int64_t lo = 1, hi = max_tiles;  // smallest piece length with ctas_for <= target
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (ctas_for(mid) <= target) hi = mid;
+      else lo = mid + 1;
+    }
+    for (int32_t i = 0; i < G; ++i) {
+      DevGroup& dg = groups[i];
+      const int64_t tile = tile_tokens_for(dg.impl);
+      const int64_t t = (dg.L_p + tile - 1) / tile;
+      const int64_t n_splits = (t + lo - 1) / lo;
+      const int64_t base = t / n_splits;
+      dg.n_splits = (int32_t)n_splits;
+      dg.tile = (int32_t)tile;
+      dg.split_len = (int32_t)(base * tile);
+      dg.n_long = (int32_t)(t - base * n_splits);
+      dg.pad[0] = dg.pad[1] = dg.pad[2] = 0;
+    }
+  }
   for (int32_t i = 0; i < G; ++i) {
-    DevGroup& dg = groups[i];
-    int64_t tile = tile_tokens_for(dg.impl);
-    int64_t per = (prefix_units + target - 1) / std::max<int64_t>(target, 1);
-    int64_t split = std::max<int64_t>(tile, (per + tile - 1) / tile * tile);
-    split = std::min<int64_t>(split, (dg.L_p + tile - 1) / tile * tile);
-    dg.split_len = (int32_t)split;
-    dg.n_splits = (int32_t)((dg.L_p + split - 1) / split);
+    const DevGroup& dg = groups[i];
     granikv_group_info& gi = p->info[i];
     gi.slab_id = grp_slab[i];
     gi.n_requests = dg.n_req;

@@ -30,20 +30,37 @@ enum Impl : int32_t {
   kImplSuffixMma = 3, // bf16, head_dim 128, g <= 8: warp-level tensor-core suffix kernel
 };
 
+// Geometry of each prefix kernel: query rows per CTA and tokens per tile.  The planner and the
+// kernels both use these.
+constexpr int kGenericRows = 16, kGenericTile = 32;
+constexpr int kCascadeRows = 128, kCascadeTile = 64;
+constexpr int kDenseRows = 128, kDenseTile = 128;
+
 struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int64_t slab_off;      // first slot of the slab
   int32_t L_p;
   int32_t n_req;
   int32_t req_begin;     // index into the group_req array
   int32_t n_splits;      // pieces along L_p
-  int32_t split_len;     // tokens per piece (last piece may be shorter)
+  int32_t split_len;     // tokens of a short piece (a multiple of `tile`)
   int32_t backend;       // GRANIKV_BACKEND_DENSE / _CASCADE
   int32_t impl;          // Impl
   int32_t rows_per_cta;  // query rows (request, head-in-group) pairs per CTA
   int32_t row_blocks;    // ceil(n_req * g / rows_per_cta)
-  int32_t pad;
+  int32_t n_long;        // the first n_long pieces are one tile longer than split_len
+  int32_t tile;          // token granularity of the pieces
+  int32_t pad[3];
 };
-static_assert(sizeof(DevGroup) == 48, "DevGroup layout");
+static_assert(sizeof(DevGroup) == 64, "DevGroup layout");
+
+// Token range [t0, t1) of piece `split` of a group's prefix: pieces of split_len or
+// split_len + tile tokens (the longer ones first), clipped to L_p.
+__host__ __device__ inline void piece_range(const DevGroup& g, int32_t split, int32_t& t0, int32_t& t1) {
+  const int32_t lo = split < g.n_long ? split : g.n_long;
+  t0 = split * g.split_len + lo * g.tile;
+  const int32_t len = g.split_len + (split < g.n_long ? g.tile : 0);
+  t1 = t0 + len < g.L_p ? t0 + len : g.L_p;
+}
 
 struct DevReq {          // per request of the batch
   int32_t rec_base;      // first partial-state record of this request

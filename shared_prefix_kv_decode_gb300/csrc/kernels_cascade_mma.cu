@@ -20,10 +20,11 @@ namespace granikv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTok = 64;                        // tokens per tile
+constexpr int kTok = kCascadeTile;              // 64 tokens per tile
 constexpr int kStages = 3;
 constexpr int kWarps = 8;
 constexpr int kRows = kWarps * 16;              // 128 query rows per CTA
+static_assert(kRows == kCascadeRows, "planner and kernel disagree on rows per CTA");
 constexpr int kRowBytes = kD * 2;               // 256 B
 constexpr int kTileBytes = kTok * kRowBytes;    // 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;     // K + V
@@ -44,8 +45,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
   const int g = p.g;
   const int j = it.kv_head;
   const int32_t rows = gr.n_req * g;
-  const int32_t t0 = it.split * gr.split_len;
-  const int32_t t1 = min(gr.L_p, t0 + gr.split_len);
+  int32_t t0, t1;
+  piece_range(gr, it.split, t0, t1);
   if (gr.slab_off < 0 || gr.slab_off + gr.L_p > p.n_hot) {
     if (tid == 0) latch_err(p.err, kDevBadSlab);
     return;

@@ -28,8 +28,8 @@ namespace granikv {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kM = 128;                       // query rows per CTA
-constexpr int kN = 128;                       // tokens per tile
+constexpr int kM = kDenseRows;                // 128 query rows per CTA
+constexpr int kN = kDenseTile;                // 128 tokens per tile
 constexpr int kStages = 2;                    // K/V tile ring
 constexpr int kThreads = 192;
 constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 16 KB
@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = p.g;
   const int j = it.kv_head;
   const int32_t rows = gr.n_req * g;
-  const int32_t t0 = it.split * gr.split_len;
-  const int32_t t1 = min(gr.L_p, t0 + gr.split_len);
+  int32_t t0, t1;
+  piece_range(gr, it.split, t0, t1);
   const int n_tiles = (t1 - t0 + kN - 1) / kN;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
 
@@ -225,14 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int valid = min(kN, t1 - t0 - i * kN);
       float s[128];
       {
-        uint32_t u[32];
+        uint32_t u[4][32];
+        const uint32_t ts = tmem + lane_off + (uint32_t)((i & 1) * 128);
+        GRANIKV_TMEM_LD32(ts, u[0]);
+        GRANIKV_TMEM_LD32(ts + 32, u[1]);
+        GRANIKV_TMEM_LD32(ts + 64, u[2]);
+        GRANIKV_TMEM_LD32(ts + 96, u[3]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          GRANIKV_TMEM_LD32(tmem + lane_off + (uint32_t)((i & 1) * 128 + c * 32), u);
-          tmem_wait_ld();
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[k]);
-        }
+          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[c][k]);
       }
       float mx = -INFINITY;
 #pragma unroll

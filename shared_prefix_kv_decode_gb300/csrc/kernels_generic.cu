@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(256) prefix_generic_kernel(AttnParams p, int32
   const int32_t rows = gr.n_req * p.g;
   const int32_t r0 = it.row_block * gr.rows_per_cta;
   const int32_t r1 = min(rows, r0 + gr.rows_per_cta);
-  const int32_t t0 = it.split * gr.split_len;
-  const int32_t t1 = min(gr.L_p, t0 + gr.split_len);
+  int32_t t0, t1;
+  piece_range(gr, it.split, t0, t1);
   if (p.checks && (gr.slab_off < 0 || gr.slab_off + gr.L_p > p.n_hot)) {
     if (threadIdx.x == 0) latch(p.err, kDevBadSlab);
     return;
