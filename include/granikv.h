@@ -177,6 +177,13 @@ granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_g
 /* Workspace bytes granikv_decode_attention needs for this plan (256-byte aligned pointer). */
 granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan, size_t* bytes);
 
+/* Prefix/suffix concurrency of the tensor-core path: when on (the default), the suffix kernel
+ * runs on a library-owned stream forked from and joined back into the caller's stream, next to
+ * the prefix kernel, and the two split the SMs: the prefix work list is sized for
+ * prefix_sm_share of the SMs and the suffix for the rest (share in (0, 1]; 1 = prefix first on
+ * all SMs).  Takes effect at the next granikv_dispatch. */
+granikv_status granikv_set_concurrency(granikv_ctx* ctx, int32_t on, float prefix_sm_share);
+
 granikv_status granikv_set_msat(granikv_ctx* ctx, int32_t m_sat);
 granikv_status granikv_get_msat(granikv_ctx* ctx, int32_t* m_sat);
 granikv_status granikv_force_backend(granikv_ctx* ctx, int32_t backend);

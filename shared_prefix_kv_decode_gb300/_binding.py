@@ -99,6 +99,7 @@ _SIGNATURES = [
     ("granikv_plan_num_groups", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_plan_group", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(GroupInfo)]),
     ("granikv_workspace_size", C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(C.c_size_t)]),
+    ("granikv_set_concurrency", C.c_int32, [C.c_void_p, C.c_int32, C.c_float]),
     ("granikv_set_msat", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_get_msat", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_force_backend", C.c_int32, [C.c_void_p, C.c_int32]),
@@ -305,6 +306,10 @@ class Context:
         n = C.c_size_t()
         _check(self._lib.granikv_workspace_size(self.handle, plan.handle, C.byref(n)), "granikv_workspace_size")
         return n.value
+
+    def set_concurrency(self, on: bool, prefix_sm_share: float = 0.5):
+        _check(self._lib.granikv_set_concurrency(self.handle, 1 if on else 0, prefix_sm_share),
+               "granikv_set_concurrency")
 
     def set_msat(self, m_sat: int):
         _check(self._lib.granikv_set_msat(self.handle, m_sat), "granikv_set_msat")

@@ -60,6 +60,14 @@ struct granikv_ctx {
   granikv_plan* own_plan = nullptr;
   // enqueued work, for attribution
   int64_t n_kernels = 0, n_copies = 0;
+  // prefix/suffix concurrency: an auxiliary stream forked from / joined into the caller's
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  int32_t concurrent = 1;
+  float prefix_share = 0.5f;
+  // tickets of the last call (zeroed again after a device check failure)
+  void* last_tickets = nullptr;
+  size_t last_tickets_bytes = 0;
   // TMA descriptors of each layer's K and V pools (dense backend), valid when has_tmaps
   std::vector<CUtensorMap> tmap_k, tmap_v;
   bool has_tmaps = false;
@@ -71,6 +79,8 @@ struct granikv_plan {
   size_t off_groups = 0, off_group_req = 0, off_req = 0, off_pitems = 0, off_sitems = 0, off_scta = 0;
   int32_t n_groups = 0, n_pitems = 0, n_sitems = 0, n_scta = 0, B = 0, n_records = 0;
   int64_t n_prefix_records = 0;
+  bool fused = false;       // the last producer of a row merges it (no merge kernel)
+  bool concurrent = false;  // suffix kernel on the auxiliary stream next to the prefix kernel
   int32_t suffix_impl = kImplGeneric;
   int32_t pitem_first[kNumImpl] = {0, 0, 0, 0};  // prefix items are ordered by implementation
   int32_t pitem_count[kNumImpl] = {0, 0, 0, 0};
@@ -133,14 +143,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A pool [n_slots, n_kv, 128] bf16 as a 3-D tensor (dim, head, slot) with 64 x 1 x 128 boxes and
+// A pool [n_slots, n_kv, 128] bf16 as a 3-D tensor (dim, head, slot) with 64 x 1 x 64 boxes and
 // the 128-byte swizzle the tcgen05 operand descriptors expect.
 bool encode_pool_map(CUtensorMap* m, void* base, int64_t n_slots, int32_t n_kv) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {128, (cuuint64_t)n_kv, (cuuint64_t)n_slots};
   cuuint64_t strides[2] = {256, (cuuint64_t)n_kv * 256};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kDenseTile};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -257,6 +267,9 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
     if (e == cudaSuccess)
       e = cudaMemcpy(c->d_ring, init.data(), sizeof(int32_t) * c->n_cold, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming);
     if (e == cudaSuccess && cfg->dtype == GRANIKV_DTYPE_BF16 && cfg->head_dim == 128 && c->cc_major == 10) {
       c->tmap_k.resize(cfg->n_layers);
       c->tmap_v.resize(cfg->n_layers);
@@ -272,6 +285,9 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
       if (c->d_ring) cudaFree(c->d_ring);
       if (c->d_err) cudaFree(c->d_err);
       if (c->d_stage) cudaFree(c->d_stage);
+      if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+      if (c->ev_join) cudaEventDestroy(c->ev_join);
+      if (c->aux) cudaStreamDestroy(c->aux);
       delete c;
       return GRANIKV_ERR_CUDA;
     }
@@ -288,6 +304,9 @@ granikv_status granikv_destroy(granikv_ctx* c) {
     if (c->d_ring) cudaFree(c->d_ring);
     if (c->d_err) cudaFree(c->d_err);
     if (c->d_stage) cudaFree(c->d_stage);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->aux) cudaStreamDestroy(c->aux);
   }
   delete c;
   return GRANIKV_OK;
@@ -520,12 +539,24 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     dg.rows_per_cta = rows_per_cta_for(dg.impl);
     dg.row_blocks = (m_eff + dg.rows_per_cta - 1) / dg.rows_per_cta;
   }
+  // Fused merge when every kernel of the step is a tensor-core kernel; then the suffix may run
+  // next to the prefix on its own share of the SMs.
+  int64_t T_all = 0;
+  for (int32_t b = 0; b < B; ++b) T_all += bt->seq_len[b];
+  const bool fast_suffix_pre = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
+  bool fused = fast_suffix_pre || T_all == 0;
+  for (int32_t i = 0; i < G; ++i)
+    if (groups[i].impl == kImplGeneric) fused = false;
+  const bool concurrent = fused && c->concurrent && G > 0 && T_all > 0 && c->prefix_share < 0.999f;
+  const int32_t prefix_sms = concurrent ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
+  const int32_t suffix_sms = concurrent ? std::max(1, c->num_sms - prefix_sms) : c->num_sms;
+
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
   //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
-  //    kernels run one CTA per SM, so their target is one full wave.
+  //    kernels run one CTA per SM, so their target is one wave over their SMs.
   int64_t target = 2LL * c->num_sms;
   for (int32_t i = 0; i < G; ++i)
-    if (groups[i].impl != kImplGeneric) target = c->num_sms;
+    if (groups[i].impl != kImplGeneric) target = prefix_sms;
   {
     int64_t max_tiles = 1;
     for (int32_t i = 0; i < G; ++i) {
@@ -580,7 +611,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int32_t n_scta = 0;
   int64_t quota = 1;
   if (T > 0) {
-    n_scta = (int32_t)std::min<int64_t>(c->num_sms, (T + 15) / 16);
+    n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + 15) / 16);
     quota = (T + n_scta - 1) / n_scta;
   }
 
@@ -675,6 +706,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   for (int32_t b = 0; b < B; ++b) p->n_prefix_records += reqs[b].n_prefix;
   p->n_scta = n_scta;
   p->suffix_impl = suffix_impl;
+  p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
+  p->concurrent = p->fused && concurrent;
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
   p->version++;
@@ -708,6 +741,7 @@ size_t workspace_bytes(const granikv_ctx* c, const granikv_plan* p) {
   size_t off = align_up(blob, 256);
   off += align_up(sizeof(float) * max_records * c->cfg.n_q * c->cfg.head_dim, 256);
   off += align_up(sizeof(float) * max_records * c->cfg.n_q, 256);
+  off += align_up(sizeof(int32_t) * (size_t)p->B * c->cfg.n_q, 256);  // tickets
   return off;
 }
 size_t records_offset(const granikv_ctx* c, const granikv_plan* p) {
@@ -722,11 +756,22 @@ size_t lse_offset(const granikv_ctx* c, const granikv_plan* p) {
   const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + (size_t)c->num_sms + 1;
   return records_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q * c->cfg.head_dim, 256);
 }
+size_t tickets_offset(const granikv_ctx* c, const granikv_plan* p) {
+  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + (size_t)c->num_sms + 1;
+  return lse_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q, 256);
+}
 }  // namespace
 
 granikv_status granikv_workspace_size(granikv_ctx* c, const granikv_plan* p, size_t* bytes) {
   if (!c || !p || !bytes || !p->valid || p->ctx != c) return GRANIKV_ERR_INVALID;
   *bytes = workspace_bytes(c, p);
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_set_concurrency(granikv_ctx* c, int32_t on, float share) {
+  if (!c || !(share > 0.f && share <= 1.f)) return GRANIKV_ERR_INVALID;
+  c->concurrent = on ? 1 : 0;
+  c->prefix_share = share;
   return GRANIKV_OK;
 }
 
@@ -775,8 +820,11 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   DeviceGuard dg(c->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
   unsigned char* wsb = (unsigned char*)ws;
+  int32_t* tickets = (int32_t*)(wsb + tickets_offset(c, p));
+  const size_t tickets_bytes = sizeof(int32_t) * (size_t)p->B * c->cfg.n_q;
   if (p->uploaded_ws != ws || p->uploaded_version != p->version) {
     cudaError_t e = cudaMemcpyAsync(wsb, p->blob.data(), p->blob.size(), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && p->fused) e = cudaMemsetAsync(tickets, 0, tickets_bytes, s);
     if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
     c->n_copies += 1;
     p->uploaded_ws = ws;
@@ -812,31 +860,53 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.n_records = p->n_records;
   a.err = c->d_err;
   a.checks = c->checks;
+  a.tickets = tickets;
+  a.fused_merge = p->fused ? 1 : 0;
+  c->last_tickets = tickets;
+  c->last_tickets_bytes = tickets_bytes;
 
   cudaError_t e = cudaSuccess;
-  if (p->pitem_count[kImplGeneric] > 0) {
-    e = launch_prefix_generic(c->cfg.dtype, a, p->pitem_first[kImplGeneric], p->pitem_count[kImplGeneric], s);
+  auto launch_suffix = [&](cudaStream_t st) -> cudaError_t {
+    if (p->n_sitems <= 0) return cudaSuccess;
     c->n_kernels += 1;
+    return p->suffix_impl == kImplSuffixMma ? launch_suffix_mma(a, a.scta_begin, p->n_scta, st)
+                                            : launch_suffix_generic(c->cfg.dtype, a, st);
+  };
+  auto launch_prefix = [&](cudaStream_t st) -> cudaError_t {
+    cudaError_t r = cudaSuccess;
+    if (p->pitem_count[kImplGeneric] > 0) {
+      r = launch_prefix_generic(c->cfg.dtype, a, p->pitem_first[kImplGeneric], p->pitem_count[kImplGeneric], st);
+      c->n_kernels += 1;
+    }
+    if (r == cudaSuccess && p->pitem_count[kImplCascadeMma] > 0) {
+      r = launch_cascade_mma(a, p->pitem_first[kImplCascadeMma], p->pitem_count[kImplCascadeMma], st);
+      c->n_kernels += 1;
+    }
+    if (r == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
+      if (!c->has_tmaps) return cudaErrorNotSupported;
+      r = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
+                          c->tmap_v[layer], st);
+      c->n_kernels += 1;
+    }
+    return r;
+  };
+  if (p->concurrent) {
+    // fork: the suffix kernel runs on the auxiliary stream next to the prefix kernel; join
+    e = cudaEventRecord(c->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->aux, c->ev_fork, 0);
+    if (e == cudaSuccess) e = launch_suffix(c->aux);
+    if (e == cudaSuccess) e = cudaEventRecord(c->ev_join, c->aux);
+    if (e == cudaSuccess) e = launch_prefix(s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_join, 0);
+  } else {
+    e = launch_prefix(s);
+    if (e == cudaSuccess) e = launch_suffix(s);
+    if (e == cudaSuccess && !p->fused) {
+      e = launch_merge(c->cfg.dtype, a, s);
+      c->n_kernels += 1;
+    }
   }
-  if (e == cudaSuccess && p->pitem_count[kImplCascadeMma] > 0) {
-    e = launch_cascade_mma(a, p->pitem_first[kImplCascadeMma], p->pitem_count[kImplCascadeMma], s);
-    c->n_kernels += 1;
-  }
-  if (e == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
-    if (!c->has_tmaps) return GRANIKV_ERR_UNSUPPORTED;
-    e = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
-                        c->tmap_v[layer], s);
-    c->n_kernels += 1;
-  }
-  if (e == cudaSuccess && p->n_sitems > 0) {
-    e = p->suffix_impl == kImplSuffixMma ? launch_suffix_mma(a, a.scta_begin, p->n_scta, s)
-                                         : launch_suffix_generic(c->cfg.dtype, a, s);
-    c->n_kernels += 1;
-  }
-  if (e == cudaSuccess) {
-    e = launch_merge(c->cfg.dtype, a, s);
-    c->n_kernels += 1;
-  }
+  if (e == cudaErrorNotSupported) return GRANIKV_ERR_UNSUPPORTED;
   return cuda_status(e);
 }
 
@@ -859,6 +929,8 @@ granikv_status granikv_sync_status(granikv_ctx* c, granikv_stream_t stream) {
   if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
   if (h != 0) {
     cudaMemset(c->d_err, 0, sizeof(int32_t));
+    // a failed call may have left row tickets part-way: start the next call from zero
+    if (c->last_tickets) cudaMemset(c->last_tickets, 0, c->last_tickets_bytes);
     return GRANIKV_ERR_DEVICE_CHECK;
   }
   return GRANIKV_OK;

@@ -34,7 +34,7 @@ enum Impl : int32_t {
 // kernels both use these.
 constexpr int kGenericRows = 16, kGenericTile = 32;
 constexpr int kCascadeRows = 128, kCascadeTile = 64;
-constexpr int kDenseRows = 128, kDenseTile = 128;
+constexpr int kDenseRows = 128, kDenseTile = 64;
 
 struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int64_t slab_off;      // first slot of the slab
@@ -102,6 +102,8 @@ struct AttnParams {
   int32_t n_records;
   int32_t* err;           // device error word
   int32_t checks;
+  int32_t* tickets;       // [B, n_q] arrivals per row (fused merge), zero between calls
+  int32_t fused_merge;    // 1: the last producer of a row merges it (no merge kernel)
 };
 
 // ---- launchers (kernels_*.cu) ------------------------------------------------------------

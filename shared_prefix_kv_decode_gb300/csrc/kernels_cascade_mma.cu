@@ -14,6 +14,7 @@
 // XOR-swizzled so ldmatrix reads are conflict-free.  The piece's partial state (normalised o
 // and lse per row) goes to the request's record for that piece.
 #include "internal.h"
+#include "merge_util.cuh"
 #include "mma_util.cuh"
 
 namespace granikv {
@@ -212,9 +213,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
   const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
   const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
   const int dcol = 2 * (lane & 3);
+  int32_t rec_lo = -1, rec_hi = -1;
   if (b_lo >= 0) {
     const int32_t rec = p.reqs[b_lo].rec_base + it.split;
     if (rec >= 0 && rec < p.n_records) {
+      rec_lo = rec;
       float* dst = p.rec_o + ((int64_t)rec * p.n_q + h_lo) * kD + dcol;
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt)
@@ -228,6 +231,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
   if (b_hi >= 0) {
     const int32_t rec = p.reqs[b_hi].rec_base + it.split;
     if (rec >= 0 && rec < p.n_records) {
+      rec_hi = rec;
       float* dst = p.rec_o + ((int64_t)rec * p.n_q + h_hi) * kD + dcol;
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt)
@@ -237,6 +241,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
     } else if ((lane & 3) == 0) {
       latch_err(p.err, kDevBadRecord);
     }
+  }
+  if (p.fused_merge) {
+    __threadfence();
+    __syncwarp();
+    const bool lead = (lane & 3) == 0;
+    const bool last_lo = lead && rec_lo >= 0 && arrive_row(p, b_lo, h_lo);
+    const bool last_hi = lead && rec_hi >= 0 && arrive_row(p, b_hi, h_hi);
+    warp_merge_completed(p, last_lo, b_lo, h_lo, lane);
+    warp_merge_completed(p, last_hi, b_hi, h_hi, lane);
   }
 }
 

@@ -7,13 +7,14 @@
 //
 // One CTA takes one (prefix group, KV head j, 128-row block, L_p piece).  Rows are the group's
 // (request, head-in-group) pairs of KV head j, so M = 128 query rows share every K/V tile.
-// Per 128-token tile:
-//     S = Q K^T   (M=128, N=128, K=128: 8 tcgen05.mma, fp32 accumulator in TMEM)
+// Per 64-token tile:
+//     S = Q K^T   (M=128, N=64, K=128: 8 tcgen05.mma, fp32 accumulator in TMEM)
 //     P = 2^(S*scale*log2e - m)   (softmax warps, one row per thread, P -> shared memory)
-//     O += P V    (M=128, N=128, K=128: 8 tcgen05.mma, O stays in TMEM for the whole piece)
+//     O += P V    (M=128, N=128, K=64: 4 tcgen05.mma, O stays in TMEM for the whole piece)
 // Roles: warps 0-3 do the softmax and the epilogue (thread r owns row r, TMEM lane r), warp 4
-// issues the TMA loads of K/V tiles (two 64-dim halves each, 128-byte swizzle), warp 5 issues
-// the MMAs.  S is double-buffered in TMEM so S(i+1) overlaps the softmax of tile i.  The
+// issues the TMA loads of K/V tiles (two 64-dim halves each, 128-byte swizzle) into a 5-stage
+// ring, so up to four tiles (128 KB) are in flight per SM, warp 5 issues the MMAs.  S is
+// double-buffered in TMEM so S(i+1) overlaps the softmax of tile i.  The
 // running max is only moved (and O rescaled in TMEM) when it grows by more than 2^8, so most
 // tiles skip the rescale; the final normalisation uses the same max, so the result is exact.
 // Every mbarrier wait is bounded in time; on expiry the CTA raises an abort flag, latches an
@@ -21,6 +22,7 @@
 #include <cuda.h>
 
 #include "internal.h"
+#include "merge_util.cuh"
 #include "mma_util.cuh"
 #include "tc_util.cuh"
 
@@ -29,27 +31,37 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = kDenseRows;                // 128 query rows per CTA
-constexpr int kN = kDenseTile;                // 128 tokens per tile
-constexpr int kStages = 2;                    // K/V tile ring
+constexpr int kN = kDenseTile;                // 64 tokens per tile
+static_assert(kN == 64, "the P layout and the MMA shapes below assume 64-token tiles");
+constexpr int kStages = 5;                    // K/V tile ring
 constexpr int kThreads = 192;
-constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 16 KB
-constexpr int kTile = 2 * kHalf;              // 32 KB
+constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 8 KB
+constexpr int kTile = 2 * kHalf;              // 16 KB
 constexpr int kQBytes = kM * kD * 2;          // 32 KB (two 64-dim K-blocks)
-constexpr int kPBytes = kM * kN * 2;          // 32 KB (two 64-token K-blocks)
+constexpr int kPBytes = kM * kN * 2;          // 16 KB (one 64-token K-block)
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffKV = kOffP + kPBytes;       // stage s: K at kOffKV + s*2*kTile, V after it
 constexpr int kOffBar = kOffKV + kStages * 2 * kTile;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;           // S0 [0,128), S1 [128,256), O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 256;           // S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kColO = 128;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;     // log2 of the largest growth tolerated in P
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int32_t kDevTimeout = 6;
 
 // barrier slots (8 bytes each) inside the barrier area
-enum : int { kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 7, kBarDrain = 9, kNumBars = 10 };
+enum : int {
+  kBarKvFull = 0,                  // [kStages] TMA -> MMA
+  kBarKvEmpty = kStages,           // [kStages] MMA (PV done) -> TMA
+  kBarSFull = 2 * kStages,         // [2] S(i) in TMEM -> softmax
+  kBarPFull = 2 * kStages + 2,     // P(i) in shared memory -> MMA (128 arrivals)
+  kBarPvDone = 2 * kStages + 3,    // [2] PV(i) done -> softmax
+  kBarDrain = 2 * kStages + 5,     // all MMAs done -> teardown
+  kNumBars = 2 * kStages + 6
+};
+static_assert(8 * kNumBars + 16 <= 256, "barrier area");
 
 __global__ void __launch_bounds__(kThreads, 1)
     dense_tc_kernel(AttnParams p, int32_t first_item, const __grid_constant__ CUtensorMap tmk,
@@ -160,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         tc_fence_after();
         const uint32_t kst = sKV + st * 2 * kTile;
-        const uint32_t dS = tmem + (uint32_t)((i & 1) * 128);
+        const uint32_t dS = tmem + (uint32_t)((i & 1) * kN);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
@@ -186,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = i % kStages;
         const uint32_t vst = sKV + st * 2 * kTile + kTile;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = smem_desc_sw128(sP + (ks >> 2) * (kM * 128) + (ks & 3) * 32, 16, 1024);
+        for (int ks = 0; ks < kN / 16; ++ks) {
+          const uint64_t a = smem_desc_sw128(sP + ks * 32, 16, 1024);
           // V tile as an MN-major B operand: 16 tokens per step (2048 bytes), the two 64-dim
           // halves kHalf apart (leading offset), 8-token groups 1024 bytes apart (stride)
           const uint64_t b = smem_desc_sw128(vst + ks * 2048, kHalf, 1024);
@@ -223,25 +235,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int valid = min(kN, t1 - t0 - i * kN);
-      float s[128];
+      float s[kN];
       {
-        uint32_t u[4][32];
-        const uint32_t ts = tmem + lane_off + (uint32_t)((i & 1) * 128);
+        uint32_t u[2][32];
+        const uint32_t ts = tmem + lane_off + (uint32_t)((i & 1) * kN);
         GRANIKV_TMEM_LD32(ts, u[0]);
         GRANIKV_TMEM_LD32(ts + 32, u[1]);
-        GRANIKV_TMEM_LD32(ts + 64, u[2]);
-        GRANIKV_TMEM_LD32(ts + 96, u[3]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[c][k]);
       }
       float mx = -INFINITY;
+      if (valid == kN) {
 #pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        s[k] = k < valid ? s[k] * scale : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+        for (int k = 0; k < kN; ++k) {
+          s[k] *= scale;
+          mx = fmaxf(mx, s[k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kN; ++k) {
+          s[k] = k < valid ? s[k] * scale : -INFINITY;
+          mx = fmaxf(mx, s[k]);
+        }
       }
       // move the running max only when it grows by more than 2^kRescaleThreshold
       const bool first = (i == 0);
@@ -275,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
       }
       float psum = 0.f;
-      uint32_t pk[64];
+      uint32_t pk[kN / 2];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
+      for (int k = 0; k < kN / 2; ++k) {
         const float a = ex2_approx(s[2 * k] - m_used);
         const float b = ex2_approx(s[2 * k + 1] - m_used);
         psum += a + b;
@@ -291,16 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      // row r of P: 16 chunks of 8 tokens, chunk c in 64-token block c/8, swizzled
+      // row r of P: 8 chunks of 8 tokens in one 64-token K-block, swizzled
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t dst = sP + (c >> 3) * (kM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      for (int c = 0; c < kN / 8; ++c) {
+        const uint32_t dst = sP + r * 128 + (((c & 7) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
                      "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       }
       // zero V rows past the piece in the last tile so 0 * garbage cannot reach O
-      if (valid < kN && r >= valid) {
+      if (valid < kN && r >= valid && r < kN) {
         const uint32_t vst = sKV + (i % kStages) * 2 * kTile + kTile;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -349,6 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (rec >= 0) p.rec_lse[(int64_t)rec * p.n_q + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (p.fused_merge) {
+        __threadfence();
+        __syncwarp();
+        const bool last = rec >= 0 && arrive_row(p, b, h);
+        warp_merge_completed(p, last, b, h, lane);
+      }
     }
   }
 

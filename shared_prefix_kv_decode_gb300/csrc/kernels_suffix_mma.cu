@@ -20,6 +20,7 @@
 // table, each token's 256-byte K and V rows are copied into a 16-byte-chunk-swizzled tile, and
 // the pipeline runs on across segment boundaries.
 #include "internal.h"
+#include "merge_util.cuh"
 #include "mma_util.cuh"
 
 namespace granikv {
@@ -59,20 +60,27 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
   const float scale = p.scale_log2;
   const int g = p.g;
 
-  // ---- producer cursor: next tile to stage -----------------------------------------------
+  // ---- producer cursor: next tile to stage ---------------------------------------------
+  // The slot ids of the next tile are loaded one tile ahead (pf_slot), so the table load's
+  // latency is hidden behind a tile of compute instead of stalling the copy issue.
   int is = seg_begin;
   int it0 = p.sitems[is].t0;
+  constexpr int32_t kNoToken = INT32_MIN;  // rows past the segment: zero-filled, masked
+  int32_t pf_slot = kNoToken;
+  auto load_slots = [&]() {
+    pf_slot = kNoToken;
+    if (is < seg_end) {
+      const DevSuffixItem seg = p.sitems[is];
+      if (lane < min(kTile, seg.t1 - it0)) pf_slot = p.req_to_slot[(int64_t)seg.b * p.cap + it0 + lane];
+    }
+  };
   auto issue = [&](int stage) {
     if (is < seg_end) {
       const DevSuffixItem seg = p.sitems[is];
-      const int n = min(kTile, seg.t1 - it0);
-      int32_t slot = -1;
-      if (lane < n) {
-        slot = p.req_to_slot[(int64_t)seg.b * p.cap + it0 + lane];
-        if (slot < p.n_hot || slot >= p.n_slots) {
-          latch_err(p.err, kDevBadSlot);
-          slot = -1;
-        }
+      int32_t slot = pf_slot;
+      if (slot != kNoToken && (slot < p.n_hot || slot >= p.n_slots)) {
+        latch_err(p.err, kDevBadSlot);
+        slot = kNoToken;
       }
       const uint32_t kdst = wsm + stage * kStageBytes;
       const uint32_t vdst = kdst + kTileBytes;
@@ -81,9 +89,9 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
         const int c = lane + 32 * i;
         const int row = c >> 4;
         const int piece = c & 15;
-        const int32_t s = __shfl_sync(0xffffffffu, slot, row);
-        const bool ok = s >= 0;
-        const int64_t off = ok ? (int64_t)s * tok_bytes + piece * 16 : 0;
+        const int32_t sl = __shfl_sync(0xffffffffu, slot, row);
+        const bool ok = sl >= 0;
+        const int64_t off = ok ? (int64_t)sl * tok_bytes + piece * 16 : 0;
         cp_async16(kdst + swz(row, piece), kbase + off, ok ? 16 : 0);
         cp_async16(vdst + swz(row, piece), vbase + off, ok ? 16 : 0);
       }
@@ -92,10 +100,12 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
         ++is;
         if (is < seg_end) it0 = p.sitems[is].t0;
       }
+      load_slots();
     }
     cp_async_commit();  // an empty group at the tail keeps the group count uniform
   };
 
+  load_slots();
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) issue(s);
 
@@ -222,6 +232,17 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
       float* ldst = p.rec_lse + (int64_t)rec * p.n_q + hq0;
       if (w0) ldst[0] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
       if (w1) ldst[1] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+    }
+    if (p.fused_merge) {
+      __threadfence();
+      __syncwarp();
+      bool last0 = false, last1 = false;
+      if (lane < 4) {
+        if (w0) last0 = arrive_row(p, seg.b, hq0);
+        if (w1) last1 = arrive_row(p, seg.b, hq0 + 1);
+      }
+      warp_merge_completed(p, last0, seg.b, hq0, lane);
+      warp_merge_completed(p, last1, seg.b, hq0 + 1, lane);
     }
   }
   cp_async_wait<0>();

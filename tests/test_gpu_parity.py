@@ -186,6 +186,23 @@ def test_backends_agree(cuda_ok):
     assert np.max(np.abs(od - oc)) <= 1e-2 and np.max(np.abs(ld - lc)) <= 1e-3
 
 
+@pytest.mark.parametrize("backend", ["dense", "cascade"])
+@pytest.mark.parametrize("setting", [(False, 0.5), (True, 0.3), (True, 0.5), (True, 1.0)])
+def test_concurrency_settings(cuda_ok, backend, setting):
+    """The suffix kernel on its own stream next to the prefix kernel, with several SM shares,
+    or serial: every setting matches the oracle and repeats bit for bit (the last producer of
+    a row merges its records in record order, whichever producer that is)."""
+    wl = W.medium_shared(2, q_scale=1.0)
+    lw = _load(wl)
+    on, share = setting
+    lw.cache.ctx.set_concurrency(on, share)
+    o, lse = _run(lw, backend)
+    o2, lse2 = _run(lw, backend)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"concurrency {setting} {backend}")
+
+
 def test_run_to_run_deterministic(cuda_ok):
     wl = W.small_mixed(9, dtype="bf16", q_scale=1.0)
     lw = _load(wl)
