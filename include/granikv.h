@@ -48,7 +48,8 @@ enum {
   GRANIKV_ERR_CUDA = 4,           /* a CUDA runtime call failed                              */
   GRANIKV_ERR_DEVICE_CHECK = 5,   /* a kernel's bounds check failed (see granikv_set_checks) */
   GRANIKV_ERR_UNSUPPORTED = 6,    /* shape or dtype this build has no kernel for             */
-  GRANIKV_ERR_NO_DEVICE = 7       /* the call needs device resources the context lacks       */
+  GRANIKV_ERR_NO_DEVICE = 7,      /* the call needs device resources the context lacks       */
+  GRANIKV_ERR_STATIC_WORKSPACE_TOO_SMALL = 8 /* the plan needs more than the built-in workspace */
 };
 
 enum { GRANIKV_DTYPE_F32 = 0, GRANIKV_DTYPE_BF16 = 1 };
@@ -203,6 +204,26 @@ granikv_status granikv_decode_attention(granikv_ctx* ctx, int32_t layer, const v
                                         const granikv_batch* batch, granikv_plan* plan,
                                         void* o, float* lse, void* workspace, size_t ws_bytes,
                                         granikv_stream_t stream);
+
+/* Decode attention without a caller workspace.  The paper has no counterpart: this is for
+ * callers that cannot allocate device memory for a workspace, such as a serving engine that has
+ * already reserved nearly all of the GPU's memory for its own pools and allocator, or a plain C
+ * host that only holds pointers to buffers someone else owns.  It computes exactly what
+ * granikv_decode_attention computes, using a workspace that lives in a file-scope device array
+ * of the library (16 MiB per GPU, held by every GPU that loads the library until the process
+ * exits).  It allocates nothing.
+ *   plan:  required (from granikv_dispatch on this batch); no internal dispatch.
+ *   q, o, lse, batch: as for granikv_decode_attention.
+ * Errors: GRANIKV_ERR_STATIC_WORKSPACE_TOO_SMALL when granikv_workspace_size(plan) exceeds
+ * 16 MiB (nothing is enqueued); otherwise as granikv_decode_attention.
+ * The first call on each device looks up the array's device address (with that device made
+ * current for the lookup); make that first call before any stream capture.  All calls on a device
+ * share the one array, and each call re-copies its work list and re-zeroes its merge tickets, so
+ * calls that may overlap on the GPU (different streams, different threads) race and must be
+ * ordered by the caller. */
+granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int32_t layer, const void* q,
+                                               const granikv_batch* batch, granikv_plan* plan,
+                                               void* o, float* lse, granikv_stream_t stream);
 
 /* ---- checks -------------------------------------------------------------------------- */
 

@@ -23,6 +23,7 @@ ERR_CUDA = 4
 ERR_DEVICE_CHECK = 5
 ERR_UNSUPPORTED = 6
 ERR_NO_DEVICE = 7
+ERR_STATIC_WORKSPACE_TOO_SMALL = 8
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
@@ -106,6 +107,8 @@ _SIGNATURES = [
     ("granikv_decode_attention", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                              C.c_size_t, C.c_void_p]),
+    ("granikv_decode_attention_static", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
+                                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("granikv_set_checks", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_sync_status", C.c_int32, [C.c_void_p, C.c_void_p]),
     ("granikv_launch_count", C.c_int32, [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
@@ -329,6 +332,13 @@ class Context:
                                                   plan.handle if plan is not None else None, _ptr(o),
                                                   _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
                "granikv_decode_attention")
+
+    def decode_attention_static(self, layer: int, q, batch: Batch, plan: Plan, o, lse, stream=None):
+        """Decode attention on the library's built-in workspace (no caller workspace, nothing
+        allocated); see granikv_decode_attention_static in include/granikv.h."""
+        _check(self._lib.granikv_decode_attention_static(self.handle, layer, _ptr(q), C.byref(batch.c),
+                                                         plan.handle, _ptr(o), _ptr(lse), _stream(stream)),
+               "granikv_decode_attention_static")
 
     # checks
     def set_checks(self, on: bool):

@@ -188,6 +188,8 @@ const char* granikv_status_string(granikv_status s) {
     case GRANIKV_ERR_DEVICE_CHECK: return "device bounds check failed";
     case GRANIKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case GRANIKV_ERR_NO_DEVICE: return "context has no device resources";
+    case GRANIKV_ERR_STATIC_WORKSPACE_TOO_SMALL:
+      return "the plan needs more workspace than the library's built-in 16 MiB array";
     default: return "unknown status";
   }
 }
@@ -944,3 +946,18 @@ granikv_status granikv_launch_count(granikv_ctx* c, int64_t* kernels, int64_t* c
 }
 
 }  // extern "C"
+
+namespace granikv {
+
+int32_t granikv_internal_device(const granikv_ctx* c, int* device) {
+  if (!c || !device) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  *device = c->cfg.device;
+  return GRANIKV_OK;
+}
+
+void granikv_internal_plan_forget_upload(granikv_plan* p) {
+  if (p) p->uploaded_ws = nullptr;
+}
+
+}  // namespace granikv

@@ -131,3 +131,13 @@ cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_i
 constexpr int kNumImpl = 4;
 
 }  // namespace granikv
+
+struct granikv_ctx;
+struct granikv_plan;
+
+namespace granikv {
+// Host-side helpers shared between the library's translation units (not part of the C ABI).
+int32_t granikv_internal_device(const granikv_ctx* ctx, int* device);        // a granikv_status
+void granikv_internal_plan_forget_upload(granikv_plan* plan);
+
+}  // namespace granikv
