@@ -48,6 +48,10 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--impl", choices=["granikv", "reference"], default="granikv")
     ap.add_argument("--backend", choices=["auto", "dense", "cascade"], default="auto")
+    ap.add_argument("--serial", action="store_true",
+                    help="run the prefix and suffix kernels one after the other on the caller's stream")
+    ap.add_argument("--prefix-share", type=float, default=1.0,
+                    help="share of the SMs the prefix work list is sized for when running concurrently")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="rough bound on the CPU-baseline sample's run time")
@@ -313,6 +317,7 @@ def run_granikv(args):
     ctx.force_backend({"auto": gb.BACKEND_AUTO, "dense": gb.BACKEND_DENSE,
                        "cascade": gb.BACKEND_CASCADE}[args.backend])
     ctx.set_checks(True)
+    ctx.set_concurrency(not args.serial, args.prefix_share)
     stream = torch.cuda.current_stream(dev)
     qs = [lw.q] + [(torch.randn((B, spec.n_q, spec.d), generator=gen, device=dev) / math.sqrt(spec.d)
                     ).to(torch.bfloat16) for _ in range(L - 1)]
@@ -438,6 +443,7 @@ def run_granikv(args):
                    "L_p": spec.prefix_lens[0], "B": B,
                    "suffix": "log-normal median 300, sigma 1, clipped [32, 2048]",
                    "layers_per_step": L, "backend": args.backend,
+                   "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                "n_splits": g["n_splits"]} for g in groups],
                    "l2": (f"inputs larger than L2: each step reads {L} distinct layers' pools, "

@@ -180,10 +180,16 @@ granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan
 
 /* Prefix/suffix concurrency of the tensor-core path: when on (the default), the suffix kernel
  * runs on a library-owned stream forked from and joined back into the caller's stream, next to
- * the prefix kernel, and the two split the SMs: the prefix work list is sized for
- * prefix_sm_share of the SMs and the suffix for the rest (share in (0, 1]; 1 = prefix first on
- * all SMs).  Takes effect at the next granikv_dispatch. */
+ * the prefix kernel.  prefix_sm_share in (0, 1) splits the SMs: the prefix work list is sized
+ * for that share and the suffix for the rest; 1 (the default) sizes both for all SMs, and the
+ * suffix fills SMs as the prefix frees them.  Takes effect at the next granikv_dispatch. */
 granikv_status granikv_set_concurrency(granikv_ctx* ctx, int32_t on, float prefix_sm_share);
+
+/* Merge strategy of the tensor-core path ("2 Related Work": partial states merged by
+ * log-sum-exp).  0 (the default): a merge kernel runs after the prefix and suffix kernels.
+ * 1: no merge kernel; every (request, head) row counts its producers with a ticket and the
+ * producer that finishes last merges the row.  Takes effect at the next granikv_dispatch. */
+granikv_status granikv_set_fused_merge(granikv_ctx* ctx, int32_t on);
 
 granikv_status granikv_set_msat(granikv_ctx* ctx, int32_t m_sat);
 granikv_status granikv_get_msat(granikv_ctx* ctx, int32_t* m_sat);

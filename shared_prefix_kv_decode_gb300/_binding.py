@@ -101,6 +101,7 @@ _SIGNATURES = [
     ("granikv_plan_group", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(GroupInfo)]),
     ("granikv_workspace_size", C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(C.c_size_t)]),
     ("granikv_set_concurrency", C.c_int32, [C.c_void_p, C.c_int32, C.c_float]),
+    ("granikv_set_fused_merge", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_set_msat", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_get_msat", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_force_backend", C.c_int32, [C.c_void_p, C.c_int32]),
@@ -313,6 +314,9 @@ class Context:
     def set_concurrency(self, on: bool, prefix_sm_share: float = 0.5):
         _check(self._lib.granikv_set_concurrency(self.handle, 1 if on else 0, prefix_sm_share),
                "granikv_set_concurrency")
+
+    def set_fused_merge(self, on: bool):
+        _check(self._lib.granikv_set_fused_merge(self.handle, 1 if on else 0), "granikv_set_fused_merge")
 
     def set_msat(self, m_sat: int):
         _check(self._lib.granikv_set_msat(self.handle, m_sat), "granikv_set_msat")

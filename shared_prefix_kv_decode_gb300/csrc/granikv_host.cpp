@@ -64,7 +64,8 @@ struct granikv_ctx {
   cudaStream_t aux = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int32_t concurrent = 1;
-  float prefix_share = 0.5f;
+  float prefix_share = 1.0f;
+  int32_t fused_merge = 0;  // merge by the last producer instead of a merge kernel
   // tickets of the last call (zeroed again after a device check failure)
   void* last_tickets = nullptr;
   size_t last_tickets_bytes = 0;
@@ -546,12 +547,16 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int64_t T_all = 0;
   for (int32_t b = 0; b < B; ++b) T_all += bt->seq_len[b];
   const bool fast_suffix_pre = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
-  bool fused = fast_suffix_pre || T_all == 0;
+  bool fused = c->fused_merge && (fast_suffix_pre || T_all == 0);
   for (int32_t i = 0; i < G; ++i)
     if (groups[i].impl == kImplGeneric) fused = false;
-  const bool concurrent = fused && c->concurrent && G > 0 && T_all > 0 && c->prefix_share < 0.999f;
-  const int32_t prefix_sms = concurrent ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
-  const int32_t suffix_sms = concurrent ? std::max(1, c->num_sms - prefix_sms) : c->num_sms;
+  bool fast_all = fast_suffix_pre || T_all == 0;
+  for (int32_t i = 0; i < G; ++i)
+    if (groups[i].impl == kImplGeneric) fast_all = false;
+  const bool concurrent = fast_all && c->concurrent && G > 0 && T_all > 0;
+  const bool split_sms = concurrent && c->prefix_share < 0.999f;
+  const int32_t prefix_sms = split_sms ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
+  const int32_t suffix_sms = split_sms ? std::max(1, c->num_sms - prefix_sms) : c->num_sms;
 
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
   //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
@@ -613,7 +618,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int32_t n_scta = 0;
   int64_t quota = 1;
   if (T > 0) {
+    // one wave over the suffix's SMs, unless a CTA would then stream more tokens than it can
+    // stage slot ids for
     n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + 15) / 16);
+    n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens - 1) / kSuffixMaxCtaTokens);
     quota = (T + n_scta - 1) / n_scta;
   }
 
@@ -709,7 +717,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->n_scta = n_scta;
   p->suffix_impl = suffix_impl;
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
-  p->concurrent = p->fused && concurrent;
+  p->concurrent = concurrent;
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
   p->version++;
@@ -735,9 +743,10 @@ namespace {
 // holds at most B + n_sm suffix segments (each token-CTA boundary adds at most one), and each
 // request has one record per prefix piece and per suffix segment.
 size_t workspace_bytes(const granikv_ctx* c, const granikv_plan* p) {
-  const size_t max_sitems = (size_t)p->B + (size_t)c->num_sms + 1;
+  const size_t n_cta = (size_t)std::max<int32_t>(c->num_sms, p->n_scta);
+  const size_t max_sitems = (size_t)p->B + n_cta + 1;
   size_t blob = p->off_sitems + align_up(sizeof(DevSuffixItem) * max_sitems, 16) +
-                align_up(sizeof(int32_t) * ((size_t)c->num_sms + 1), 256);
+                align_up(sizeof(int32_t) * (n_cta + 1), 256);
   blob = std::max(blob, p->blob.size());
   const size_t max_records = (size_t)p->n_prefix_records + max_sitems;
   size_t off = align_up(blob, 256);
@@ -747,19 +756,21 @@ size_t workspace_bytes(const granikv_ctx* c, const granikv_plan* p) {
   return off;
 }
 size_t records_offset(const granikv_ctx* c, const granikv_plan* p) {
-  (void)c;
-  const size_t max_sitems = (size_t)p->B + (size_t)c->num_sms + 1;
+  const size_t n_cta = (size_t)std::max<int32_t>(c->num_sms, p->n_scta);
+  const size_t max_sitems = (size_t)p->B + n_cta + 1;
   size_t blob = p->off_sitems + align_up(sizeof(DevSuffixItem) * max_sitems, 16) +
-                align_up(sizeof(int32_t) * ((size_t)c->num_sms + 1), 256);
+                align_up(sizeof(int32_t) * (n_cta + 1), 256);
   blob = std::max(blob, p->blob.size());
   return align_up(blob, 256);
 }
 size_t lse_offset(const granikv_ctx* c, const granikv_plan* p) {
-  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + (size_t)c->num_sms + 1;
+  const size_t n_cta = (size_t)std::max<int32_t>(c->num_sms, p->n_scta);
+  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + n_cta + 1;
   return records_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q * c->cfg.head_dim, 256);
 }
 size_t tickets_offset(const granikv_ctx* c, const granikv_plan* p) {
-  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + (size_t)c->num_sms + 1;
+  const size_t n_cta = (size_t)std::max<int32_t>(c->num_sms, p->n_scta);
+  const size_t max_records = (size_t)p->n_prefix_records + (size_t)p->B + n_cta + 1;
   return lse_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q, 256);
 }
 }  // namespace
@@ -774,6 +785,12 @@ granikv_status granikv_set_concurrency(granikv_ctx* c, int32_t on, float share) 
   if (!c || !(share > 0.f && share <= 1.f)) return GRANIKV_ERR_INVALID;
   c->concurrent = on ? 1 : 0;
   c->prefix_share = share;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_set_fused_merge(granikv_ctx* c, int32_t on) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  c->fused_merge = on ? 1 : 0;
   return GRANIKV_OK;
 }
 
@@ -893,13 +910,18 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     return r;
   };
   if (p->concurrent) {
-    // fork: the suffix kernel runs on the auxiliary stream next to the prefix kernel; join
+    // fork: the suffix kernel runs on the auxiliary stream next to the prefix kernel (enqueued
+    // first, so the longer prefix work starts first); join before anything else on the stream
     e = cudaEventRecord(c->ev_fork, s);
+    if (e == cudaSuccess) e = launch_prefix(s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->aux, c->ev_fork, 0);
     if (e == cudaSuccess) e = launch_suffix(c->aux);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_join, c->aux);
-    if (e == cudaSuccess) e = launch_prefix(s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_join, 0);
+    if (e == cudaSuccess && !p->fused) {
+      e = launch_merge(c->cfg.dtype, a, s);
+      c->n_kernels += 1;
+    }
   } else {
     e = launch_prefix(s);
     if (e == cudaSuccess) e = launch_suffix(s);

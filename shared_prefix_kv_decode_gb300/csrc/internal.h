@@ -35,6 +35,8 @@ enum Impl : int32_t {
 constexpr int kGenericRows = 16, kGenericTile = 32;
 constexpr int kCascadeRows = 128, kCascadeTile = 64;
 constexpr int kDenseRows = 128, kDenseTile = 64;
+// Largest number of COLD tokens one suffix CTA streams (its slot ids are staged in shared memory).
+constexpr int kSuffixMaxCtaTokens = 4096;
 
 struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int64_t slab_off;      // first slot of the slab

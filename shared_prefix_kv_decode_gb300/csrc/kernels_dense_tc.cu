@@ -7,18 +7,26 @@
 //
 // One CTA takes one (prefix group, KV head j, 128-row block, L_p piece).  Rows are the group's
 // (request, head-in-group) pairs of KV head j, so M = 128 query rows share every K/V tile.
-// Per 64-token tile:
-//     S = Q K^T   (M=128, N=64, K=128: 8 tcgen05.mma, fp32 accumulator in TMEM)
-//     P = 2^(S*scale*log2e - m)   (softmax warps, one row per thread, P -> shared memory)
-//     O += P V    (M=128, N=128, K=64: 4 tcgen05.mma, O stays in TMEM for the whole piece)
-// Roles: warps 0-3 do the softmax and the epilogue (thread r owns row r, TMEM lane r), warp 4
-// issues the TMA loads of K/V tiles (two 64-dim halves each, 128-byte swizzle) into a 5-stage
-// ring, so up to four tiles (128 KB) are in flight per SM, warp 5 issues the MMAs.  S is
-// double-buffered in TMEM so S(i+1) overlaps the softmax of tile i.  The
-// running max is only moved (and O rescaled in TMEM) when it grows by more than 2^8, so most
-// tiles skip the rescale; the final normalisation uses the same max, so the result is exact.
-// Every mbarrier wait is bounded in time; on expiry the CTA raises an abort flag, latches an
-// error, drains what it issued and frees its TMEM.
+// Per 64-token tile i:
+//     S(i) = Q K(i)^T   (M=128, N=64, K=128: 8 tcgen05.mma, fp32 accumulator in TMEM)
+//     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps -> shared memory, bf16)
+//     O   += P(i) V(i)  (M=128, N=128, K=64: 4 tcgen05.mma, O stays in TMEM for the whole piece)
+// Roles:
+//  * warps 0-7, softmax and epilogue: warp w reads TMEM lanes 32*(w%4).. (row r = TMEM lane r).
+//    Both warps of a row read the whole tile row for its maximum (an exact value, so they agree
+//    without talking) and each exponentiates its column half w/4; two softmax warps per SM
+//    sub-partition keep the exponential units and issue slots busy.  The halves' row sums are
+//    added once per piece, through per-row-quarter mbarriers.
+//  * warps 8 and 9, TMA loads (two 64-dim halves per tile, 128-byte swizzle), each in a warp of
+//    its own so neither waits on the other: warp 8 fills a 5-slot K ring whose slots free up as
+//    soon as S(i) completes, warp 9 a 4-slot V ring freed by PV(i).
+//  * warp 10, the MMAs.  S runs three tiles ahead of the softmax (four TMEM buffers) and P has
+//    three shared-memory buffers, so the hand-off latency between the softmax warps and the MMA
+//    thread stays off the per-tile loop.
+// The running max is only moved (and O rescaled in TMEM) when it grows by more than 2^8; the
+// final normalisation uses the same max, so the result is the exact softmax.  Every mbarrier
+// wait is bounded in time; on expiry the CTA raises an abort flag, latches an error, drains what
+// it issued and frees its TMEM.
 #include <cuda.h>
 
 #include "internal.h"
@@ -33,35 +41,51 @@ constexpr int kD = 128;
 constexpr int kM = kDenseRows;                // 128 query rows per CTA
 constexpr int kN = kDenseTile;                // 64 tokens per tile
 static_assert(kN == 64, "the P layout and the MMA shapes below assume 64-token tiles");
-constexpr int kStages = 5;                    // K/V tile ring
-constexpr int kThreads = 192;
+constexpr int kHalfCols = kN / 2;             // columns of a tile per softmax thread
+constexpr int kKSlots = 5;                    // slots of the K ring
+constexpr int kVSlots = 4;                    // slots of the V ring
+constexpr int kSBufs = 4;                     // S buffers in TMEM
+constexpr int kAhead = kSBufs - 1;            // S(i + kAhead) is issued right after PV(i)
+constexpr int kPBufs = 3;                     // P buffers in shared memory
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kWarpTmaK = 8, kWarpTmaV = 9, kWarpMma = 10;
+constexpr int kThreads = 352;
 constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 8 KB
 constexpr int kTile = 2 * kHalf;              // 16 KB
 constexpr int kQBytes = kM * kD * 2;          // 32 KB (two 64-dim K-blocks)
-constexpr int kPBytes = kM * kN * 2;          // 16 KB (one 64-token K-block)
+constexpr int kPBytes = kM * kN * 2;          // 16 KB per P buffer (one 64-token K-block)
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffKV = kOffP + kPBytes;       // stage s: K at kOffKV + s*2*kTile, V after it
-constexpr int kOffBar = kOffKV + kStages * 2 * kTile;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-constexpr uint32_t kTmemCols = 256;           // S0 [0,64), S1 [64,128), O [128,256)
-constexpr uint32_t kColO = 128;
+constexpr int kOffK = kOffP + kPBufs * kPBytes;  // K slot s at kOffK + s*kTile
+constexpr int kOffV = kOffK + kKSlots * kTile;   // V slot s at kOffV + s*kTile
+constexpr int kOffRed = kOffV + kVSlots * kTile; // [2 halves][128 rows] partial row sums
+constexpr int kOffBar = kOffRed + 2 * kM * 4;
+constexpr int kBarArea = 512;
+constexpr int kSmemBytes = kOffBar + kBarArea + 1024;  // barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr uint32_t kTmemCols = 512;           // S0..S3 at 0, 64, 128, 192; O at 256
+constexpr uint32_t kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;     // log2 of the largest growth tolerated in P
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int32_t kDevTimeout = 6;
 
-// barrier slots (8 bytes each) inside the barrier area
 enum : int {
-  kBarKvFull = 0,                  // [kStages] TMA -> MMA
-  kBarKvEmpty = kStages,           // [kStages] MMA (PV done) -> TMA
-  kBarSFull = 2 * kStages,         // [2] S(i) in TMEM -> softmax
-  kBarPFull = 2 * kStages + 2,     // P(i) in shared memory -> MMA (128 arrivals)
-  kBarPvDone = 2 * kStages + 3,    // [2] PV(i) done -> softmax
-  kBarDrain = 2 * kStages + 5,     // all MMAs done -> teardown
-  kNumBars = 2 * kStages + 6
+  kBarKFull = 0,                            // [kKSlots] TMA -> MMA (K)
+  kBarKEmpty = kBarKFull + kKSlots,         // [kKSlots] MMA (S done) -> TMA
+  kBarVFull = kBarKEmpty + kKSlots,         // [kVSlots] TMA -> MMA and last-tile softmax (V)
+  kBarVEmpty = kBarVFull + kVSlots,         // [kVSlots] MMA (PV done) -> TMA
+  kBarSFull = kBarVEmpty + kVSlots,         // [kSBufs] S(i) in TMEM -> softmax
+  kBarPFull = kBarSFull + kSBufs,           // [kPBufs] P(i) in shared memory -> MMA (256 arrivals)
+  kBarPvDone = kBarPFull + kPBufs,          // [kPBufs] PV(i) done -> softmax (P buffer i%kPBufs free)
+  kBarDrain = kBarPvDone + kPBufs,          // all MMAs done -> teardown
+  kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter (64 arrivals)
+  kNumBars = kBarPair + 4
 };
-static_assert(8 * kNumBars + 16 <= 256, "barrier area");
+static_assert(8 * kNumBars + 16 <= kBarArea, "barrier area");
+
+__device__ __forceinline__ float max4(float a, float b, float c, float d) { return fmaxf(fmaxf(a, b), fmaxf(c, d)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     dense_tc_kernel(AttnParams p, int32_t first_item, const __grid_constant__ CUtensorMap tmk,
@@ -71,7 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base = (raw_u + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw_u);
-  const uint32_t sQ = base + kOffQ, sP = base + kOffP, sKV = base + kOffKV;
+  const uint32_t sQ = base + kOffQ, sP = base + kOffP, sK = base + kOffK, sV = base + kOffV;
+  float* red = reinterpret_cast<float*>(smem + kOffRed);  // red[half*kM + row]
   const uint32_t sBar = base + kOffBar;
   auto bar = [&](int i) { return sBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars);
@@ -91,7 +116,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
 
   if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i == kBarPFull ? 128u : 1u);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1u;
+      if (i >= kBarPFull && i < kBarPFull + kPBufs) count = kSoftmaxThreads;
+      if (i >= kBarPair) count = 64u;
+      mbar_init(bar(i), count);
+    }
     *abort_flag = slab_ok ? 0 : 1;
     if (!slab_ok) atomicCAS(p.err, 0, (int32_t)kDevBadSlab);
     mbar_fence_init();
@@ -100,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kWarpTmaK && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
@@ -127,31 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    // ---------------- TMA producer ----------------
+  if (warp == kWarpTmaK || warp == kWarpTmaV) {
+    // ---------------- TMA producers: warp 8 the K ring, warp 9 the V ring ----------------
     if (lane == 0 && !*abort_flag) {
+      const bool is_k = warp == kWarpTmaK;
+      const CUtensorMap* tm = is_k ? &tmk : &tmv;
+      const uint32_t ring = is_k ? sK : sV;
+      const int full = is_k ? kBarKFull : kBarVFull;
+      const int empty = is_k ? kBarKEmpty : kBarVEmpty;
+      const int slots = is_k ? kKSlots : kVSlots;
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages &&
-            !mbar_wait_bounded(bar(kBarKvEmpty + st), ((i / kStages) - 1) & 1, abort_flag, p.err, kDevTimeout,
-                               kWaitLimitNs))
+        const int st = i % slots;
+        if (i >= slots && !mbar_wait_bounded(bar(empty + st), ((i / slots) - 1) & 1, abort_flag, p.err,
+                                             kDevTimeout, kWaitLimitNs))
           break;
-        const uint32_t kdst = sKV + st * 2 * kTile;
-        const uint32_t vdst = kdst + kTile;
+        const uint32_t dst = ring + st * kTile;
         const int32_t z = (int32_t)(gr.slab_off + t0 + i * kN);
-        mbar_arrive_expect_tx(bar(kBarKvFull + st), 2 * kTile);
-        tma_load_3d(kdst, &tmk, 0, j, z, bar(kBarKvFull + st));
-        tma_load_3d(kdst + kHalf, &tmk, 64, j, z, bar(kBarKvFull + st));
-        tma_load_3d(vdst, &tmv, 0, j, z, bar(kBarKvFull + st));
-        tma_load_3d(vdst + kHalf, &tmv, 64, j, z, bar(kBarKvFull + st));
+        mbar_arrive_expect_tx(bar(full + st), kTile);
+        tma_load_3d(dst, tm, 0, j, z, bar(full + st));
+        tma_load_3d(dst + kHalf, tm, 64, j, z, bar(full + st));
         issued = i + 1;
       }
       // never leave with a copy in flight: wait for every issued tile to land
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        const int st = i % kStages;
+      for (int i = max(0, issued - slots); i < issued; ++i) {
+        const int st = i % slots;
         const uint64_t t_start = globaltimer_ns();
-        while (!mbar_try_wait(bar(kBarKvFull + st), (i / kStages) & 1)) {
+        while (!mbar_try_wait(bar(full + st), (i / slots) & 1)) {
           if (globaltimer_ns() - t_start > kWaitLimitNs) {
             atomicCAS(p.err, 0, kDevTimeout);
             break;
@@ -159,55 +191,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ---------------- MMA issuer ----------------
     if (lane == 0 && !*abort_flag) {
       constexpr uint32_t idS = idesc_bf16_f32(kM, kN, false);
       constexpr uint32_t idO = idesc_bf16_f32(kM, kD, true);
-      bool ok = true;
-      int committed = 0;  // tcgen05 commits issued, for the drain below
+      // descriptors are built once; a byte offset into shared memory moves the start-address
+      // field (bits 0..13, in 16-byte units), which never carries out for addresses < 256 KB
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dp0 = smem_desc_sw128(sP, 16, 1024);
+      // V tile as an MN-major B operand: 16 tokens per step (2048 bytes), the two 64-dim halves
+      // kHalf apart (leading offset), 8-token groups 1024 bytes apart (stride)
+      const uint64_t dv0 = smem_desc_sw128(sV, kHalf, 1024);
+      int committed = 0;
       auto issue_s = [&](int i) -> bool {
-        const int st = i % kStages;
-        if (!mbar_wait_bounded(bar(kBarKvFull + st), (i / kStages) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs))
+        const int st = i % kKSlots;
+        if (!mbar_wait_bounded(bar(kBarKFull + st), (i / kKSlots) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs))
           return false;
         tc_fence_after();
-        const uint32_t kst = sKV + st * 2 * kTile;
-        const uint32_t dS = tmem + (uint32_t)((i & 1) * kN);
+        const uint32_t dS = tmem + (uint32_t)((i % kSBufs) * kN);
+        const uint64_t dk = dk0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sQ + off, 16, 1024);
-          const uint64_t b = smem_desc_sw128(kst + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t a = dq0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t b = dk + (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
           umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(kBarSFull + (i & 1)));
-        ++committed;
+        umma_commit(bar(kBarSFull + i % kSBufs));
+        umma_commit(bar(kBarKEmpty + st));
+        committed += 2;
         return true;
       };
-      ok = issue_s(0);
+      // PV(i) then S(i+kAhead): S(i+kAhead) goes into the buffer S(i-1) used; the softmax
+      // finished reading it before it produced P(i-1), which this loop waited for one iteration
+      // earlier.
+      bool ok = true;
+      for (int i = 0; ok && i < kAhead && i < n_tiles; ++i) ok = issue_s(i);
       for (int i = 0; ok && i < n_tiles; ++i) {
-        if (i + 1 < n_tiles && !issue_s(i + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_bounded(bar(kBarPFull), i & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs)) {
+        const int st = i % kVSlots;
+        const int pb = i % kPBufs;
+        if (!mbar_wait_bounded(bar(kBarPFull + pb), (i / kPBufs) & 1, abort_flag, p.err, kDevTimeout,
+                               kWaitLimitNs) ||
+            !mbar_wait_bounded(bar(kBarVFull + st), (i / kVSlots) & 1, abort_flag, p.err, kDevTimeout,
+                               kWaitLimitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int st = i % kStages;
-        const uint32_t vst = sKV + st * 2 * kTile + kTile;
+        const uint64_t dp = dp0 + (uint64_t)((pb * kPBytes) >> 4);
+        const uint64_t dv = dv0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(sP + ks * 32, 16, 1024);
-          // V tile as an MN-major B operand: 16 tokens per step (2048 bytes), the two 64-dim
-          // halves kHalf apart (leading offset), 8-token groups 1024 bytes apart (stride)
-          const uint64_t b = smem_desc_sw128(vst + ks * 2048, kHalf, 1024);
-          umma_f16(tmem + kColO, a, b, idO, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(kBarKvEmpty + st));
-        umma_commit(bar(kBarPvDone + (i & 1)));
+        for (int ks = 0; ks < kN / 16; ++ks)
+          umma_f16(tmem + kColO, dp + (uint64_t)((ks * 32) >> 4), dv + (uint64_t)((ks * 2048) >> 4), idO,
+                   (i > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(bar(kBarVEmpty + st));
+        umma_commit(bar(kBarPvDone + pb));
         committed += 2;
+        if (i + kAhead < n_tiles && !issue_s(i + kAhead)) ok = false;
       }
       // drain: every tcgen05 op this thread issued completes before the CTA frees TMEM
       if (committed > 0) {
@@ -222,57 +263,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- softmax warps 0-3: thread r owns row r ----------------
-    const int r = tid;  // 0..127, TMEM lane r
-    const uint32_t lane_off = (uint32_t)((warp * 32) << 16);
+    // ---------------- softmax warps 0-7: row r, column half `half` ----------------
+    const int quad = warp & 3;
+    const int half = warp >> 2;
+    const int r = quad * 32 + lane;                 // row = TMEM lane
+    const uint32_t lane_off = (uint32_t)((quad * 32) << 16);
+    const int pair_bar = kBarPair + quad;           // mbarrier of the two warps sharing rows
     const float scale = p.scale_log2;
-    float m_used = -INFINITY;
-    float l = 0.f;
+    float m_used = -INFINITY;  // running max in scaled (base-2) units, identical in both halves
+    float l = 0.f;             // this half's share of the row sum
     bool ok = !*abort_flag;
     for (int i = 0; ok && i < n_tiles; ++i) {
-      ok = mbar_wait_bounded(bar(kBarSFull + (i & 1)), (i >> 1) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+      ok = mbar_wait_bounded(bar(kBarSFull + i % kSBufs), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
+                             kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
       if (!ok) break;
       tc_fence_after();
       const int valid = min(kN, t1 - t0 - i * kN);
-      float s[kN];
+      // the whole tile row (for the maximum), of which this warp exponentiates one half
+      float s[kHalfCols], o_[kHalfCols];
       {
         uint32_t u[2][32];
-        const uint32_t ts = tmem + lane_off + (uint32_t)((i & 1) * kN);
-        GRANIKV_TMEM_LD32(ts, u[0]);
-        GRANIKV_TMEM_LD32(ts + 32, u[1]);
+        const uint32_t ts = tmem + lane_off + (uint32_t)((i % kSBufs) * kN);
+        GRANIKV_TMEM_LD32(ts + half * kHalfCols, u[0]);
+        GRANIKV_TMEM_LD32(ts + (1 - half) * kHalfCols, u[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[c][k]);
-      }
-      float mx = -INFINITY;
-      if (valid == kN) {
-#pragma unroll
-        for (int k = 0; k < kN; ++k) {
-          s[k] *= scale;
-          mx = fmaxf(mx, s[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < kN; ++k) {
-          s[k] = k < valid ? s[k] * scale : -INFINITY;
-          mx = fmaxf(mx, s[k]);
+        for (int k = 0; k < kHalfCols; ++k) {
+          s[k] = __uint_as_float(u[0][k]);
+          o_[k] = __uint_as_float(u[1][k]);
         }
       }
-      // move the running max only when it grows by more than 2^kRescaleThreshold
+      if (valid < kN) {
+#pragma unroll
+        for (int k = 0; k < kHalfCols; ++k) {
+          s[k] = half * kHalfCols + k < valid ? s[k] : -INFINITY;
+          o_[k] = (1 - half) * kHalfCols + k < valid ? o_[k] : -INFINITY;
+        }
+      }
+      // row max of the raw logits (scale > 0 commutes with max), as a tree
+      float mx;
+      {
+        float t[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = max4(s[k], s[k + 8], s[k + 16], s[k + 24]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], max4(o_[k], o_[k + 8], o_[k + 16], o_[k + 24]));
+        mx = fmaxf(max4(t[0], t[1], t[2], t[3]), max4(t[4], t[5], t[6], t[7])) * scale;
+      }
+      // move the running max only when it grows by more than 2^kRescaleThreshold (both halves
+      // see the same row maxima, so both warps of a pair decide alike)
       const bool first = (i == 0);
-      const bool need = first ? true : (mx > m_used + kRescaleThreshold);
-      const bool warp_need = __any_sync(0xffffffffu, need && !first);
+      const bool warp_need = !first && __any_sync(0xffffffffu, mx > m_used + kRescaleThreshold);
       if (first) {
         m_used = mx;
       } else if (warp_need) {
-        // O must hold PV(i-1) before it is rescaled
-        if (!mbar_wait_bounded(bar(kBarPvDone + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, p.err, kDevTimeout,
-                               kWaitLimitNs)) {
-          ok = false;
-        }
+        // O must hold PV(i-1) before it is rescaled; each half rescales its 64 columns of O
+        ok = mbar_wait_bounded(bar(kBarPvDone + (i - 1) % kPBufs), ((i - 1) / kPBufs) & 1, abort_flag, p.err,
+                               kDevTimeout, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -282,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         uint32_t u[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t ta = tmem + lane_off + kColO + c * 32;
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t ta = tmem + lane_off + kColO + half * 64 + c * 32;
           GRANIKV_TMEM_LD32(ta, u);
           tmem_wait_ld();
 #pragma unroll
@@ -292,54 +340,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      float psum = 0.f;
-      uint32_t pk[kN / 2];
+      // P = 2^(s*scale - m) for this half's 32 columns; partial row sum as a small tree
+      const float nm = -m_used;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kHalfCols / 2];
 #pragma unroll
-      for (int k = 0; k < kN / 2; ++k) {
-        const float a = ex2_approx(s[2 * k] - m_used);
-        const float b = ex2_approx(s[2 * k + 1] - m_used);
-        psum += a + b;
+      for (int k = 0; k < kHalfCols / 2; ++k) {
+        const float a = ex2_approx(fmaf(s[2 * k], scale, nm));
+        const float b = ex2_approx(fmaf(s[2 * k + 1], scale, nm));
+        ps[k & 3] += a + b;
         pk[k] = pack_bf16(a, b);
       }
-      l += psum;
-      // P(i) overwrites P(i-1): PV(i-1) must be done
-      if (i > 0 && !mbar_wait_bounded(bar(kBarPvDone + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, p.err,
-                                      kDevTimeout, kWaitLimitNs)) {
-        ok = false;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // P(i) goes into buffer i%kPBufs, which PV(i-kPBufs) read: it must be done
+      if (i >= kPBufs) {
+        ok = mbar_wait_bounded(bar(kBarPvDone + i % kPBufs), ((i - kPBufs) / kPBufs) & 1, abort_flag, p.err,
+                               kDevTimeout, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
       }
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      // row r of P: 8 chunks of 8 tokens in one 64-token K-block, swizzled
+      const uint32_t pb = sP + (i % kPBufs) * kPBytes;
+      // row r of P: this half's 4 chunks of 8 tokens in the 64-token K-block, swizzled
 #pragma unroll
-      for (int c = 0; c < kN / 8; ++c) {
-        const uint32_t dst = sP + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+      for (int c = 0; c < kHalfCols / 8; ++c) {
+        const int chunk = half * (kHalfCols / 8) + c;
+        const uint32_t dst = pb + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
                      "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       }
-      // zero V rows past the piece in the last tile so 0 * garbage cannot reach O
-      if (valid < kN && r >= valid && r < kN) {
-        const uint32_t vst = sKV + (i % kStages) * 2 * kTile + kTile;
+      // zero V rows past the piece in the last tile so 0 * garbage cannot reach O (the V tile
+      // must have landed first); half h clears the 64-dim half h of those rows
+      if (valid < kN) {
+        ok = mbar_wait_bounded(bar(kBarVFull + i % kVSlots), (i / kVSlots) & 1, abort_flag, p.err, kDevTimeout,
+                               kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (r >= valid && r < kN) {
+          const uint32_t vrow = sV + (i % kVSlots) * kTile + half * kHalf + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vst + r * 128 + c * 16), "r"(0u) : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vst + kHalf + r * 128 + c * 16), "r"(0u)
-                       : "memory");
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u) : "memory");
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
+      mbar_arrive(bar(kBarPFull + i % kPBufs));
     }
-    // epilogue: wait for the last PV, normalise, write this row's record
+    // epilogue: wait for the last PV, add the two halves' row sums, normalise, write the record
     if (ok) {
       const int last = n_tiles - 1;
-      ok = mbar_wait_bounded(bar(kBarPvDone + (last & 1)), (last >> 1) & 1, abort_flag, p.err, kDevTimeout,
+      ok = mbar_wait_bounded(bar(kBarPvDone + last % kPBufs), (last / kPBufs) & 1, abort_flag, p.err, kDevTimeout,
                              kWaitLimitNs);
     }
     ok = __all_sync(0xffffffffu, ok);
+    // swap the partial row sums with the other half (phase 0 of the pair barrier)
+    red[half * kM + r] = ok ? l : -1.f;
+    mbar_arrive(bar(pair_bar));
+    bool pair_ok = mbar_wait_bounded(bar(pair_bar), 0, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+    pair_ok = __all_sync(0xffffffffu, pair_ok);
+    const float l0 = pair_ok ? red[r] : -1.f, l1 = pair_ok ? red[kM + r] : -1.f;
+    ok = __all_sync(0xffffffffu, l0 >= 0.f && l1 >= 0.f);
     if (ok) {
       tc_fence_after();
+      const float lt = l0 + l1;
       const int32_t row = rbase + r;
       int32_t b = -1, h = 0, rec = -1;
       if (row < rows) {
@@ -347,38 +411,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         h = j * g + row % g;
         rec = p.reqs[b].rec_base + it.split;
         if (rec < 0 || rec >= p.n_records) {
-          atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
+          if (half == 0) atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
           rec = -1;
         }
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* dst = rec >= 0 ? p.rec_o + ((int64_t)rec * p.n_q + h) * kD : nullptr;
-      uint32_t u[32];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      float* dst = rec >= 0 ? p.rec_o + ((int64_t)rec * p.n_q + h) * kD + half * 64 : nullptr;
+      uint32_t u[2][32];
+      GRANIKV_TMEM_LD32(tmem + lane_off + kColO + half * 64, u[0]);
+      GRANIKV_TMEM_LD32(tmem + lane_off + kColO + half * 64 + 32, u[1]);
+      tmem_wait_ld();
+      if (dst) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        GRANIKV_TMEM_LD32(tmem + lane_off + kColO + c * 32, u);
-        tmem_wait_ld();
-        if (dst) {
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<float4*>(dst + c * 32 + k) =
-                make_float4(__uint_as_float(u[k]) * inv, __uint_as_float(u[k + 1]) * inv,
-                            __uint_as_float(u[k + 2]) * inv, __uint_as_float(u[k + 3]) * inv);
-        }
+                make_float4(__uint_as_float(u[c][k]) * inv, __uint_as_float(u[c][k + 1]) * inv,
+                            __uint_as_float(u[c][k + 2]) * inv, __uint_as_float(u[c][k + 3]) * inv);
       }
-      if (rec >= 0) p.rec_lse[(int64_t)rec * p.n_q + h] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (rec >= 0 && half == 0)
+        p.rec_lse[(int64_t)rec * p.n_q + h] = lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
       if (p.fused_merge) {
+        // both halves' parts of the record are stored before the row's ticket moves (phase 1)
         __threadfence();
-        __syncwarp();
-        const bool last = rec >= 0 && arrive_row(p, b, h);
-        warp_merge_completed(p, last, b, h, lane);
+        mbar_arrive(bar(pair_bar));
+        bool stored = mbar_wait_bounded(bar(pair_bar), 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+        stored = __all_sync(0xffffffffu, stored);
+        if (half == 0 && stored) {
+          const bool last_arrival = rec >= 0 && arrive_row(p, b, h);
+          warp_merge_completed(p, last_arrival, b, h, lane);
+        }
       }
     }
   }
 
   // ---------------- teardown ----------------
-  // If the CTA aborted, wait (bounded) until every MMA this CTA issued has completed: the last
-  // commit of each kind is observed through the PV barriers.  Then free TMEM.
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

@@ -272,6 +272,63 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
   return dtype == 1 ? launch_suffix_t<__nv_bfloat16>(p, s) : launch_suffix_t<float>(p, s);
 }
 
+// bf16, head_dim 128: one warp per (request, head), lane owns 4 elements; one pass over the
+// records with a running log-sum-exp, up to sixteen records' loads in flight at a time (a
+// typical row has a dozen records, so it is merged in one memory round trip).  Records are read
+// with streaming loads (they are not read again).
+constexpr int kMergeBatch = 16;
+
+__global__ void __launch_bounds__(256) merge_bf16_d128_kernel(AttnParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // b * n_q + h
+  if (row >= (int64_t)p.B * p.n_q) return;
+  const int32_t b = (int32_t)(row / p.n_q);
+  const int32_t h = (int32_t)(row % p.n_q);
+  const DevReq r = p.reqs[b];
+  const float* lse_rec = p.rec_lse + (int64_t)r.rec_base * p.n_q + h;
+  const float4* orec = reinterpret_cast<const float4*>(p.rec_o + ((int64_t)r.rec_base * p.n_q + h) * 128) + lane;
+  const int64_t lstride = p.n_q;
+  const int64_t ostride = (int64_t)p.n_q * 32;  // float4s between consecutive records of a row
+  float m = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int32_t i = 0; i < r.n_parts; i += kMergeBatch) {
+    float l[kMergeBatch];
+    float4 x[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const bool ok = i + u < r.n_parts;
+      l[u] = ok ? __ldcs(lse_rec + (i + u) * lstride) : -INFINITY;
+      x[u] = ok ? __ldcs(orec + (i + u) * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mb = m;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, l[u]);
+    if (mb == -INFINITY) continue;
+    const float a = exp2f((m - mb) * kLog2e);  // 0 while m is still -inf
+    den *= a;
+    acc.x *= a;
+    acc.y *= a;
+    acc.z *= a;
+    acc.w *= a;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float w = exp2f((l[u] - mb) * kLog2e);  // 0 for absent records
+      den += w;
+      acc.x += w * x[u].x;
+      acc.y += w * x[u].y;
+      acc.z += w * x[u].z;
+      acc.w += w * x[u].w;
+    }
+    m = mb;
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * 128)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  if (lane == 0) p.lse[row] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
 template <typename T, int VPL>
 cudaError_t launch_merge_vpl(const AttnParams& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.B * p.n_q;
@@ -296,6 +353,11 @@ cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s) {
+  if (dtype == 1 && p.d == 128) {
+    const int64_t rows = (int64_t)p.B * p.n_q;
+    merge_bf16_d128_kernel<<<(int)((rows + 7) / 8), 256, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   return dtype == 1 ? launch_merge_t<__nv_bfloat16>(p, s) : launch_merge_t<float>(p, s);
 }
 

@@ -16,7 +16,8 @@
 // Work split: the plan cuts the concatenation of all requests' COLD tokens into one contiguous
 // run per token-CTA (stream-K style), so every CTA streams the same number of tokens; each
 // request segment inside a run writes one partial-state record.  blockIdx.y picks a group of
-// four KV heads.  Each warp runs its own 3-stage cp.async pipeline: slot ids are read from the
+// eight KV heads (one group for the Llama and Qwen shapes), so the warps of a CTA fetch all
+// heads of a slot's K and V rows (2 KB each) at the same time.  Each warp runs its own 3-stage cp.async pipeline: slot ids are read from the
 // table, each token's 256-byte K and V rows are copied into a 16-byte-chunk-swizzled tile, and
 // the pipeline runs on across segment boundaries.
 #include "internal.h"
@@ -29,12 +30,13 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTile = 16;                     // tokens per tile (MMA M)
 constexpr int kStages = 3;
-constexpr int kWarps = 4;                     // KV heads per CTA
+constexpr int kWarps = 8;                     // KV heads per CTA (all of them for n_kv <= 8)
 constexpr int kRowBytes = kD * 2;             // one head's K (or V) row: 256 B
 constexpr int kTileBytes = kTile * kRowBytes; // 4 KB
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V
 constexpr int kWarpSmem = kStages * kStageBytes;
-constexpr int kSmemBytes = kWarps * kWarpSmem;  // 96 KB
+constexpr int kSlotBytes = kSuffixMaxCtaTokens * 4;  // the CTA's slot ids, loaded once
+constexpr int kSmemBytes = kWarps * kWarpSmem + kSlotBytes;  // 192 KB + 16 KB
 constexpr float kLn2 = 0.6931471805599453f;
 
 // byte offset of 16-byte chunk c of row r in a tile of 256-byte rows (XOR swizzle so the 8
@@ -48,10 +50,27 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.y * kWarps + warp;  // KV head of this warp
-  if (j >= p.n_kv) return;                   // no CTA-wide barrier is used below
   const int seg_begin = cta_begin[blockIdx.x];
   const int seg_end = cta_begin[blockIdx.x + 1];
   if (seg_begin >= seg_end) return;
+  // The slot ids of all of this CTA's tokens (its segments back to back) go to shared memory
+  // once, so the copy issue never waits on a table load.  The plan keeps a CTA's tokens within
+  // kSuffixMaxCtaTokens.
+  int32_t* sslot = reinterpret_cast<int32_t*>(smem + kWarps * kWarpSmem);
+  {
+    int base = 0;
+    for (int sg = seg_begin; sg < seg_end; ++sg) {
+      const DevSuffixItem seg = p.sitems[sg];
+      const int len = seg.t1 - seg.t0;
+      const int32_t* row = p.req_to_slot + (int64_t)seg.b * p.cap + seg.t0;
+      for (int k = threadIdx.x; k < len && base + k < kSuffixMaxCtaTokens; k += blockDim.x) sslot[base + k] = row[k];
+      base += len;
+    }
+    if (base > kSuffixMaxCtaTokens && threadIdx.x == 0) latch_err(p.err, kDevBadRecord);
+    __syncthreads();
+    if (base > kSuffixMaxCtaTokens) return;
+  }
+  if (j >= p.n_kv) return;  // no CTA-wide barrier is used below
 
   const uint32_t wsm = smem_u32(smem) + warp * kWarpSmem;
   const int64_t tok_bytes = (int64_t)p.n_kv * kRowBytes;
@@ -61,23 +80,14 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
   const int g = p.g;
 
   // ---- producer cursor: next tile to stage ---------------------------------------------
-  // The slot ids of the next tile are loaded one tile ahead (pf_slot), so the table load's
-  // latency is hidden behind a tile of compute instead of stalling the copy issue.
   int is = seg_begin;
   int it0 = p.sitems[is].t0;
+  int is_base = 0;  // position of segment `is` in sslot
   constexpr int32_t kNoToken = INT32_MIN;  // rows past the segment: zero-filled, masked
-  int32_t pf_slot = kNoToken;
-  auto load_slots = [&]() {
-    pf_slot = kNoToken;
-    if (is < seg_end) {
-      const DevSuffixItem seg = p.sitems[is];
-      if (lane < min(kTile, seg.t1 - it0)) pf_slot = p.req_to_slot[(int64_t)seg.b * p.cap + it0 + lane];
-    }
-  };
   auto issue = [&](int stage) {
     if (is < seg_end) {
       const DevSuffixItem seg = p.sitems[is];
-      int32_t slot = pf_slot;
+      int32_t slot = lane < min(kTile, seg.t1 - it0) ? sslot[is_base + (it0 - seg.t0) + lane] : kNoToken;
       if (slot != kNoToken && (slot < p.n_hot || slot >= p.n_slots)) {
         latch_err(p.err, kDevBadSlot);
         slot = kNoToken;
@@ -97,39 +107,47 @@ __global__ void __launch_bounds__(kWarps * 32) suffix_mma_kernel(AttnParams p, c
       }
       it0 += kTile;
       if (it0 >= seg.t1) {
+        is_base += seg.t1 - seg.t0;
         ++is;
         if (is < seg_end) it0 = p.sitems[is].t0;
       }
-      load_slots();
     }
     cp_async_commit();  // an empty group at the tail keeps the group count uniform
   };
 
-  load_slots();
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) issue(s);
 
   int tile = 0;  // tiles consumed so far
   const int h0 = 2 * (lane & 3);  // this thread's two head columns: h0, h0 + 1
+  // Q^T as B fragments (column n = lane/4 is head j*g + n); the next segment's are loaded one
+  // segment ahead so their latency hides behind the current segment's tiles
+  uint32_t qn[8][2];
+  auto load_q = [&](int sg) {
+    const int n = lane >> 2;
+    if (sg < seg_end && n < g) {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)p.sitems[sg].b * p.n_q + j * g + n) * kD);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qn[kk][0] = qrow[kk * 8 + (lane & 3)];
+        qn[kk][1] = qrow[kk * 8 + 4 + (lane & 3)];
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) qn[kk][0] = qn[kk][1] = 0u;
+    }
+  };
+  load_q(seg_begin);
   for (int sg = seg_begin; sg < seg_end; ++sg) {
     const DevSuffixItem seg = p.sitems[sg];
-    // Q^T as B fragments: column n = lane/4 is head j*g + n
     uint32_t qf[8][2];
-    {
-      const int n = lane >> 2;
-      if (n < g) {
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)seg.b * p.n_q + j * g + n) * kD);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          qf[kk][0] = qrow[kk * 8 + (lane & 3)];
-          qf[kk][1] = qrow[kk * 8 + 4 + (lane & 3)];
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) qf[kk][0] = qf[kk][1] = 0u;
-      }
+    for (int kk = 0; kk < 8; ++kk) {
+      qf[kk][0] = qn[kk][0];
+      qf[kk][1] = qn[kk][1];
     }
+    load_q(sg + 1);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[8][4];
 #pragma unroll

@@ -187,15 +187,18 @@ def test_backends_agree(cuda_ok):
 
 
 @pytest.mark.parametrize("backend", ["dense", "cascade"])
-@pytest.mark.parametrize("setting", [(False, 0.5), (True, 0.3), (True, 0.5), (True, 1.0)])
-def test_concurrency_settings(cuda_ok, backend, setting):
-    """The suffix kernel on its own stream next to the prefix kernel, with several SM shares,
-    or serial: every setting matches the oracle and repeats bit for bit (the last producer of
-    a row merges its records in record order, whichever producer that is)."""
+@pytest.mark.parametrize("setting", [(False, 0.5, False), (True, 0.3, False), (True, 1.0, False),
+                                     (False, 0.5, True), (True, 0.3, True), (True, 0.5, True),
+                                     (True, 1.0, True)])
+def test_concurrency_and_merge_settings(cuda_ok, backend, setting):
+    """The suffix kernel on its own stream next to the prefix kernel (several SM shares) or
+    serial, with the merge kernel or the last-producer merge: every setting matches the oracle
+    and repeats bit for bit (records are merged in record order, whoever merges them)."""
     wl = W.medium_shared(2, q_scale=1.0)
     lw = _load(wl)
-    on, share = setting
+    on, share, fused = setting
     lw.cache.ctx.set_concurrency(on, share)
+    lw.cache.ctx.set_fused_merge(fused)
     o, lse = _run(lw, backend)
     o2, lse2 = _run(lw, backend)
     assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
@@ -287,3 +290,24 @@ def test_full_size_sampled(cuda_ok, name):
         for b in sample:
             assert_close(o[b], lse[b], refs[b][0], refs[b][1], "bf16", f"{name} b={b} {backend}")
         assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+@pytest.mark.parametrize("backend", ["dense", "cascade"])
+def test_hot_layout_equals_paged_equivalent_layout(cuda_ok, backend):
+    """The same logical batch stored with the prefix in one HOT slab, or copied at the head of
+    every request's COLD token table (the paged-equivalent layout), gives the same attention
+    ("Ethics Statement": the layer changes layout and kernel choice, not outputs)."""
+    import torch
+    gb = _gb()
+    from shared_prefix_kv_decode_gb300.layout_bench import build
+    cache_h, batch_h, q = build(1000, 8, 50, paged=False, seed=3)
+    cache_h.ctx.force_backend({"dense": gb.BACKEND_DENSE, "cascade": gb.BACKEND_CASCADE}[backend])
+    o_h, l_h = cache_h.decode(0, q, batch_h)
+    cache_h.ctx.sync_status(cache_h.stream())
+    cache_p, batch_p, q2 = build(1000, 8, 50, paged=True, seed=3)
+    assert torch.equal(q, q2)
+    o_p, l_p = cache_p.decode(0, q2, batch_p)
+    cache_p.ctx.sync_status(cache_p.stream())
+    assert_close(o_h.float().cpu().numpy().astype(np.float64), l_h.cpu().numpy().astype(np.float64),
+                 o_p.float().cpu().numpy().astype(np.float64), l_p.cpu().numpy().astype(np.float64),
+                 "bf16", f"hot vs paged {backend}")
