@@ -34,7 +34,7 @@ enum Impl : int32_t {
 // kernels both use these.
 constexpr int kGenericRows = 16, kGenericTile = 32;
 constexpr int kCascadeRows = 128, kCascadeTile = 64;
-constexpr int kDenseRows = 128, kDenseTile = 64;
+constexpr int kDenseRows = 128, kDenseTile = 128;
 // Largest number of COLD tokens one suffix CTA streams (its slot ids are staged in shared memory).
 constexpr int kSuffixMaxCtaTokens = 4096;
 

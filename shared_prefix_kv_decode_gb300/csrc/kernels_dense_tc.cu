@@ -7,22 +7,21 @@
 //
 // One CTA takes one (prefix group, KV head j, 128-row block, L_p piece).  Rows are the group's
 // (request, head-in-group) pairs of KV head j, so M = 128 query rows share every K/V tile.
-// Per 64-token tile i:
-//     S(i) = Q K(i)^T   (M=128, N=64, K=128: 8 tcgen05.mma, fp32 accumulator in TMEM)
-//     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps -> shared memory, bf16)
-//     O   += P(i) V(i)  (M=128, N=128, K=64: 4 tcgen05.mma, O stays in TMEM for the whole piece)
+// Per 128-token tile i:
+//     S(i) = Q K(i)^T   (M=128, N=128, K=128: 8 tcgen05.mma from shared memory, fp32 in TMEM)
+//     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps; bf16, written back over S(i) in TMEM)
+//     O   += P(i) V(i)  (M=128, N=128, K=128: 8 tcgen05.mma with A = P(i) read from TMEM)
+// Every MMA is 128x128x16, so one issuing thread keeps the tensor core fed.
 // Roles:
-//  * warps 0-7, softmax and epilogue: warp w reads TMEM lanes 32*(w%4).. (row r = TMEM lane r).
-//    Both warps of a row read the whole tile row for its maximum (an exact value, so they agree
-//    without talking) and each exponentiates its column half w/4; two softmax warps per SM
-//    sub-partition keep the exponential units and issue slots busy.  The halves' row sums are
-//    added once per piece, through per-row-quarter mbarriers.
+//  * warps 0-7, softmax and epilogue: warp w serves TMEM lanes 32*(w%4).. (row r = lane r) and
+//    column half w/4 of each tile.  The two warps of a row quarter swap their half-row maxima
+//    through shared memory at a time-bounded mbarrier, so both apply the same running max; once
+//    both have read their half of S(i), each writes its half of P(i) over S(i)'s columns.  Two
+//    softmax warps per SM sub-partition keep the exponential units and issue slots busy.
 //  * warps 8 and 9, TMA loads (two 64-dim halves per tile, 128-byte swizzle), each in a warp of
-//    its own so neither waits on the other: warp 8 fills a 5-slot K ring whose slots free up as
-//    soon as S(i) completes, warp 9 a 4-slot V ring freed by PV(i).
-//  * warp 10, the MMAs.  S runs three tiles ahead of the softmax (four TMEM buffers) and P has
-//    three shared-memory buffers, so the hand-off latency between the softmax warps and the MMA
-//    thread stays off the per-tile loop.
+//    its own: warp 8 fills a 2-slot K ring whose slots free up as soon as S(i) completes, warp 9
+//    a 3-slot V ring freed by PV(i).
+//  * warp 10, the MMAs: PV(i), then S(i+2) (three S/P buffers in TMEM).
 // The running max is only moved (and O rescaled in TMEM) when it grows by more than 2^8; the
 // final normalisation uses the same max, so the result is the exact softmax.  Every mbarrier
 // wait is bounded in time; on expiry the CTA raises an abort flag, latches an error, drains what
@@ -39,33 +38,30 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = kDenseRows;                // 128 query rows per CTA
-constexpr int kN = kDenseTile;                // 64 tokens per tile
-static_assert(kN == 64, "the P layout and the MMA shapes below assume 64-token tiles");
-constexpr int kHalfCols = kN / 2;             // columns of a tile per softmax thread
-constexpr int kKSlots = 5;                    // slots of the K ring
-constexpr int kVSlots = 4;                    // slots of the V ring
-constexpr int kSBufs = 4;                     // S buffers in TMEM
+constexpr int kN = kDenseTile;                // 128 tokens per tile
+static_assert(kN == 128, "the TMEM layout and the MMA shapes below assume 128-token tiles");
+constexpr int kHalfCols = kN / 2;             // S columns per softmax thread
+constexpr int kKSlots = 2;                    // slots of the K ring
+constexpr int kVSlots = 3;                    // slots of the V ring
+constexpr int kSBufs = 3;                     // S/P buffers in TMEM
 constexpr int kAhead = kSBufs - 1;            // S(i + kAhead) is issued right after PV(i)
-constexpr int kPBufs = 3;                     // P buffers in shared memory
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kWarpTmaK = 8, kWarpTmaV = 9, kWarpMma = 10;
 constexpr int kThreads = 352;
-constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 8 KB
-constexpr int kTile = 2 * kHalf;              // 16 KB
+constexpr int kHalf = kN * 128;               // one 64-dim half of a K or V tile: 16 KB
+constexpr int kTile = 2 * kHalf;              // 32 KB
 constexpr int kQBytes = kM * kD * 2;          // 32 KB (two 64-dim K-blocks)
-constexpr int kPBytes = kM * kN * 2;          // 16 KB per P buffer (one 64-token K-block)
 constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffK = kOffP + kPBufs * kPBytes;  // K slot s at kOffK + s*kTile
+constexpr int kOffK = kOffQ + kQBytes;           // K slot s at kOffK + s*kTile
 constexpr int kOffV = kOffK + kKSlots * kTile;   // V slot s at kOffV + s*kTile
-constexpr int kOffRed = kOffV + kVSlots * kTile; // [2 halves][128 rows] partial row sums
-constexpr int kOffBar = kOffRed + 2 * kM * 4;
+constexpr int kOffRed = kOffV + kVSlots * kTile; // [2 parities][2 halves][128 rows] partial values
+constexpr int kOffBar = kOffRed + 2 * 2 * kM * 4;
 constexpr int kBarArea = 512;
 constexpr int kSmemBytes = kOffBar + kBarArea + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr uint32_t kTmemCols = 512;           // S0..S3 at 0, 64, 128, 192; O at 256
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;           // S/P buffers at 0, 128, 256; O at 384
+constexpr uint32_t kColO = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;     // log2 of the largest growth tolerated in P
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -77,9 +73,9 @@ enum : int {
   kBarVFull = kBarKEmpty + kKSlots,         // [kVSlots] TMA -> MMA and last-tile softmax (V)
   kBarVEmpty = kBarVFull + kVSlots,         // [kVSlots] MMA (PV done) -> TMA
   kBarSFull = kBarVEmpty + kVSlots,         // [kSBufs] S(i) in TMEM -> softmax
-  kBarPFull = kBarSFull + kSBufs,           // [kPBufs] P(i) in shared memory -> MMA (256 arrivals)
-  kBarPvDone = kBarPFull + kPBufs,          // [kPBufs] PV(i) done -> softmax (P buffer i%kPBufs free)
-  kBarDrain = kBarPvDone + kPBufs,          // all MMAs done -> teardown
+  kBarPFull = kBarSFull + kSBufs,           // [kSBufs] P(i) in TMEM -> MMA (256 arrivals)
+  kBarPvDone = kBarPFull + kSBufs,          // [kSBufs] PV(i) done -> softmax
+  kBarDrain = kBarPvDone + kSBufs,          // all MMAs done -> teardown
   kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter (64 arrivals)
   kNumBars = kBarPair + 4
 };
@@ -95,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base = (raw_u + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw_u);
-  const uint32_t sQ = base + kOffQ, sP = base + kOffP, sK = base + kOffK, sV = base + kOffV;
-  float* red = reinterpret_cast<float*>(smem + kOffRed);  // red[half*kM + row]
+  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+  float* red = reinterpret_cast<float*>(smem + kOffRed);  // red[(parity*2 + half)*kM + row]
   const uint32_t sBar = base + kOffBar;
   auto bar = [&](int i) { return sBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars);
@@ -118,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1u;
-      if (i >= kBarPFull && i < kBarPFull + kPBufs) count = kSoftmaxThreads;
+      if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxThreads;
       if (i >= kBarPair) count = 64u;
       mbar_init(bar(i), count);
     }
@@ -200,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // field (bits 0..13, in 16-byte units), which never carries out for addresses < 256 KB
       const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dp0 = smem_desc_sw128(sP, 16, 1024);
       // V tile as an MN-major B operand: 16 tokens per step (2048 bytes), the two 64-dim halves
       // kHalf apart (leading offset), 8-token groups 1024 bytes apart (stride)
       const uint64_t dv0 = smem_desc_sw128(sV, kHalf, 1024);
@@ -223,15 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         committed += 2;
         return true;
       };
-      // PV(i) then S(i+kAhead): S(i+kAhead) goes into the buffer S(i-1) used; the softmax
-      // finished reading it before it produced P(i-1), which this loop waited for one iteration
-      // earlier.
+      // PV(i) then S(i+kAhead): S(i+kAhead) overwrites the TMEM buffer of S(i-1)/P(i-1); the
+      // softmax finished with S(i-1) before it produced P(i-1) (waited for one iteration
+      // earlier), and PV(i-1), which reads P(i-1), was issued before it, and tcgen05 MMAs of
+      // one thread execute in order.
       bool ok = true;
       for (int i = 0; ok && i < kAhead && i < n_tiles; ++i) ok = issue_s(i);
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int st = i % kVSlots;
-        const int pb = i % kPBufs;
-        if (!mbar_wait_bounded(bar(kBarPFull + pb), (i / kPBufs) & 1, abort_flag, p.err, kDevTimeout,
+        const int sb = i % kSBufs;
+        if (!mbar_wait_bounded(bar(kBarPFull + sb), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
                                kWaitLimitNs) ||
             !mbar_wait_bounded(bar(kBarVFull + st), (i / kVSlots) & 1, abort_flag, p.err, kDevTimeout,
                                kWaitLimitNs)) {
@@ -239,14 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t dp = dp0 + (uint64_t)((pb * kPBytes) >> 4);
+        const uint32_t pa = tmem + (uint32_t)(sb * kN);  // P(i): 64 columns, two tokens per column
         const uint64_t dv = dv0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kN / 16; ++ks)
-          umma_f16(tmem + kColO, dp + (uint64_t)((ks * 32) >> 4), dv + (uint64_t)((ks * 2048) >> 4), idO,
-                   (i > 0 || ks > 0) ? 1u : 0u);
+          umma_f16_ts(tmem + kColO, pa + (uint32_t)(ks * 8), dv + (uint64_t)((ks * 2048) >> 4), idO,
+                      (i > 0 || ks > 0) ? 1u : 0u);
         umma_commit(bar(kBarVEmpty + st));
-        umma_commit(bar(kBarPvDone + pb));
+        umma_commit(bar(kBarPvDone + sb));
         committed += 2;
         if (i + kAhead < n_tiles && !issue_s(i + kAhead)) ok = false;
       }
@@ -272,45 +268,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = p.scale_log2;
     float m_used = -INFINITY;  // running max in scaled (base-2) units, identical in both halves
     float l = 0.f;             // this half's share of the row sum
+    int pair_phase = 0;
     bool ok = !*abort_flag;
     for (int i = 0; ok && i < n_tiles; ++i) {
-      ok = mbar_wait_bounded(bar(kBarSFull + i % kSBufs), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
-                             kWaitLimitNs);
+      const int sb = i % kSBufs;
+      ok = mbar_wait_bounded(bar(kBarSFull + sb), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
       if (!ok) break;
       tc_fence_after();
       const int valid = min(kN, t1 - t0 - i * kN);
-      // the whole tile row (for the maximum), of which this warp exponentiates one half
-      float s[kHalfCols], o_[kHalfCols];
+      const uint32_t ts = tmem + lane_off + (uint32_t)(sb * kN + half * kHalfCols);
+      float s[kHalfCols];
       {
         uint32_t u[2][32];
-        const uint32_t ts = tmem + lane_off + (uint32_t)((i % kSBufs) * kN);
-        GRANIKV_TMEM_LD32(ts + half * kHalfCols, u[0]);
-        GRANIKV_TMEM_LD32(ts + (1 - half) * kHalfCols, u[1]);
+        GRANIKV_TMEM_LD32(ts, u[0]);
+        GRANIKV_TMEM_LD32(ts + 32, u[1]);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < kHalfCols; ++k) {
+        for (int k = 0; k < 32; ++k) {
           s[k] = __uint_as_float(u[0][k]);
-          o_[k] = __uint_as_float(u[1][k]);
+          s[32 + k] = __uint_as_float(u[1][k]);
         }
       }
       if (valid < kN) {
 #pragma unroll
-        for (int k = 0; k < kHalfCols; ++k) {
-          s[k] = half * kHalfCols + k < valid ? s[k] : -INFINITY;
-          o_[k] = (1 - half) * kHalfCols + k < valid ? o_[k] : -INFINITY;
-        }
+        for (int k = 0; k < kHalfCols; ++k) s[k] = half * kHalfCols + k < valid ? s[k] : -INFINITY;
       }
-      // row max of the raw logits (scale > 0 commutes with max), as a tree
+      // half-row max (scale > 0 commutes with max), swapped with the other half
       float mx;
       {
-        float t[8];
+        float t[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] = max4(s[k], s[k + 8], s[k + 16], s[k + 24]);
+        for (int k = 0; k < 16; ++k) t[k] = max4(s[k], s[k + 16], s[k + 32], s[k + 48]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], max4(o_[k], o_[k + 8], o_[k + 16], o_[k + 24]));
-        mx = fmaxf(max4(t[0], t[1], t[2], t[3]), max4(t[4], t[5], t[6], t[7])) * scale;
+        for (int k = 0; k < 4; ++k) t[k] = max4(t[k], t[k + 4], t[k + 8], t[k + 12]);
+        mx = max4(t[0], t[1], t[2], t[3]);
       }
+      float* red_i = red + (i & 1) * 2 * kM;
+      red_i[half * kM + r] = mx;
+      mbar_arrive(bar(pair_bar));
+      ok = mbar_wait_bounded(bar(pair_bar), pair_phase & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+      ++pair_phase;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      mx = fmaxf(red_i[r], red_i[kM + r]) * scale;
       // move the running max only when it grows by more than 2^kRescaleThreshold (both halves
       // see the same row maxima, so both warps of a pair decide alike)
       const bool first = (i == 0);
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = mx;
       } else if (warp_need) {
         // O must hold PV(i-1) before it is rescaled; each half rescales its 64 columns of O
-        ok = mbar_wait_bounded(bar(kBarPvDone + (i - 1) % kPBufs), ((i - 1) / kPBufs) & 1, abort_flag, p.err,
+        ok = mbar_wait_bounded(bar(kBarPvDone + (i - 1) % kSBufs), ((i - 1) / kSBufs) & 1, abort_flag, p.err,
                                kDevTimeout, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -340,35 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s*scale - m) for this half's 32 columns; partial row sum as a small tree
+      // P = 2^(s*scale - m) for this half's 64 columns, packed two per 32-bit column and written
+      // over columns [32*half, 32*half + 32) of the S(i) buffer (both halves have read S(i))
       const float nm = -m_used;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kHalfCols / 2];
+      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < kHalfCols / 2; ++k) {
+      for (int k = 0; k < 32; ++k) {
         const float a = ex2_approx(fmaf(s[2 * k], scale, nm));
         const float b = ex2_approx(fmaf(s[2 * k + 1], scale, nm));
         ps[k & 3] += a + b;
         pk[k] = pack_bf16(a, b);
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P(i) goes into buffer i%kPBufs, which PV(i-kPBufs) read: it must be done
-      if (i >= kPBufs) {
-        ok = mbar_wait_bounded(bar(kBarPvDone + i % kPBufs), ((i - kPBufs) / kPBufs) & 1, abort_flag, p.err,
-                               kDevTimeout, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      const uint32_t pb = sP + (i % kPBufs) * kPBytes;
-      // row r of P: this half's 4 chunks of 8 tokens in the 64-token K-block, swizzled
-#pragma unroll
-      for (int c = 0; c < kHalfCols / 8; ++c) {
-        const int chunk = half * (kHalfCols / 8) + c;
-        const uint32_t dst = pb + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
-                     "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
+      GRANIKV_TMEM_ST32(tmem + lane_off + (uint32_t)(sb * kN + half * 32), pk);
       // zero V rows past the piece in the last tile so 0 * garbage cannot reach O (the V tile
       // must have landed first); half h clears the 64-dim half h of those rows
       if (valid < kN) {
@@ -376,30 +362,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        if (r >= valid && r < kN) {
+        if (r >= valid) {
           const uint32_t vrow = sV + (i % kVSlots) * kTile + half * kHalf + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u) : "memory");
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull + i % kPBufs));
+      mbar_arrive(bar(kBarPFull + sb));
     }
     // epilogue: wait for the last PV, add the two halves' row sums, normalise, write the record
     if (ok) {
       const int last = n_tiles - 1;
-      ok = mbar_wait_bounded(bar(kBarPvDone + last % kPBufs), (last / kPBufs) & 1, abort_flag, p.err, kDevTimeout,
+      ok = mbar_wait_bounded(bar(kBarPvDone + last % kSBufs), (last / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
                              kWaitLimitNs);
     }
     ok = __all_sync(0xffffffffu, ok);
-    // swap the partial row sums with the other half (phase 0 of the pair barrier)
-    red[half * kM + r] = ok ? l : -1.f;
+    // swap the partial row sums with the other half at the pair barrier's next phase; a warp
+    // that left the tile loop early has made fewer pair arrivals, so its partner's bounded wait
+    // gives up and both skip the record
+    float* red_e = red + (pair_phase & 1) * 2 * kM;
+    red_e[half * kM + r] = ok ? l : -1.f;
     mbar_arrive(bar(pair_bar));
-    bool pair_ok = mbar_wait_bounded(bar(pair_bar), 0, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+    bool pair_ok = mbar_wait_bounded(bar(pair_bar), pair_phase & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+    ++pair_phase;
     pair_ok = __all_sync(0xffffffffu, pair_ok);
-    const float l0 = pair_ok ? red[r] : -1.f, l1 = pair_ok ? red[kM + r] : -1.f;
+    const float l0 = pair_ok ? red_e[r] : -1.f, l1 = pair_ok ? red_e[kM + r] : -1.f;
     ok = __all_sync(0xffffffffu, l0 >= 0.f && l1 >= 0.f);
     if (ok) {
       tc_fence_after();
@@ -433,10 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (rec >= 0 && half == 0)
         p.rec_lse[(int64_t)rec * p.n_q + h] = lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
       if (p.fused_merge) {
-        // both halves' parts of the record are stored before the row's ticket moves (phase 1)
+        // both halves' parts of the record are stored before the row's ticket moves
         __threadfence();
         mbar_arrive(bar(pair_bar));
-        bool stored = mbar_wait_bounded(bar(pair_bar), 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+        bool stored = mbar_wait_bounded(bar(pair_bar), pair_phase & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
+        ++pair_phase;
         stored = __all_sync(0xffffffffu, stored);
         if (half == 0 && stored) {
           const bool last_arrival = rec >= 0 && arrive_row(p, b, h);
