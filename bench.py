@@ -50,8 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--backend", choices=["auto", "dense", "cascade"], default="auto")
     ap.add_argument("--serial", action="store_true",
                     help="run the prefix and suffix kernels one after the other on the caller's stream")
-    ap.add_argument("--prefix-share", type=float, default=1.0,
-                    help="share of the SMs the prefix work list is sized for when running concurrently")
+    ap.add_argument("--prefix-share", type=float, default=0.0,
+                    help="share of the SMs the prefix work list is sized for when running concurrently "
+                         "(0: the library's automatic share)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="rough bound on the CPU-baseline sample's run time")
@@ -346,16 +347,18 @@ def run_granikv(args):
         batch = gb.Batch(slab_ids, seq, cache.req_to_slot, cache.cap)
         ctx.dispatch(batch, plan)
         nbytes = algorithmic_bytes(spec, slab_ids, seq, 2)
+        # events bracket the step's L back-to-back decode-attention calls (not each call, so
+        # that nothing sits between two calls' kernels on the stream)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
         for layer in range(L):
-            if record:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
             ctx.decode_attention(layer, qs[layer], batch, plan, outs[layer], lses[layer], ws, ws_bytes, stream)
-            if record:
-                e1.record(stream)
-                ev_pairs.append((e0, e1))
-                timed_bytes.append(nbytes)
+        if record:
+            e1.record(stream)
+            ev_pairs.append((e0, e1))
+            timed_bytes.append(nbytes)
         return batch
 
     for _ in range(args.warmup):
@@ -382,7 +385,7 @@ def run_granikv(args):
     t_local = t_start.elapsed_time(t_end) / 1000.0
     t_max = max_over_ranks(t_local, world, dev)
     value = world * B * L * args.steps / t_max
-    call_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    call_ms = [a.elapsed_time(b) / L for a, b in ev_pairs]
     avg_call_s = statistics.mean(call_ms) / 1000.0
     avg_bytes = statistics.mean(timed_bytes)
 

@@ -181,8 +181,11 @@ granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan
 /* Prefix/suffix concurrency of the tensor-core path: when on (the default), the suffix kernel
  * runs on a library-owned stream forked from and joined back into the caller's stream, next to
  * the prefix kernel.  prefix_sm_share in (0, 1) splits the SMs: the prefix work list is sized
- * for that share and the suffix for the rest; 1 (the default) sizes both for all SMs, and the
- * suffix fills SMs as the prefix frees them.  Takes effect at the next granikv_dispatch. */
+ * for that share and the suffix gets the SMs the prefix CTAs leave; 0 (the default) picks the
+ * share from the step's estimated prefix and suffix work; 1 sizes both for all SMs, and the
+ * suffix fills SMs as the prefix frees them.  When off, the prefix, suffix and merge kernels
+ * run one after another on the caller's stream.  GRANIKV_ERR_INVALID for a share outside
+ * [0, 1].  Takes effect at the next granikv_dispatch. */
 granikv_status granikv_set_concurrency(granikv_ctx* ctx, int32_t on, float prefix_sm_share);
 
 /* Merge strategy of the tensor-core path ("2 Related Work": partial states merged by

@@ -311,7 +311,7 @@ class Context:
         _check(self._lib.granikv_workspace_size(self.handle, plan.handle, C.byref(n)), "granikv_workspace_size")
         return n.value
 
-    def set_concurrency(self, on: bool, prefix_sm_share: float = 0.5):
+    def set_concurrency(self, on: bool, prefix_sm_share: float = 0.0):
         _check(self._lib.granikv_set_concurrency(self.handle, 1 if on else 0, prefix_sm_share),
                "granikv_set_concurrency")
 

@@ -23,8 +23,11 @@ namespace {
 constexpr int32_t kDefaultMaxSlabs = 1024;
 constexpr int32_t kDefaultMaxBatch = 4096;
 // Dense/cascade crossover on GB300 for the Llama-3.1-8B shape, re-fitted from the L_p x B
-// sweep (the pages' A100 value is 1024 and they state other GPUs need a re-fit).
-constexpr int32_t kDefaultMsat = 1024;
+// sweep of msat_fit.py (the pages' A100 value is 1024 and they state other GPUs need a re-fit).
+// With the tcgen05 dense kernel the fit lands on the sweep's smallest M_eff (4): the dense
+// backend is at least as fast as the cascade one almost everywhere on this GPU, and far faster
+// from M_eff = 128 on.
+constexpr int32_t kDefaultMsat = 4;
 
 struct Extent {
   int64_t off, len;
@@ -64,7 +67,7 @@ struct granikv_ctx {
   cudaStream_t aux = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int32_t concurrent = 1;
-  float prefix_share = 1.0f;
+  float prefix_share = 0.0f;  // 0: automatic
   int32_t fused_merge = 0;  // merge by the last producer instead of a merge kernel
   // tickets of the last call (zeroed again after a device check failure)
   void* last_tickets = nullptr;
@@ -555,8 +558,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     if (groups[i].impl == kImplGeneric) fast_all = false;
   const bool concurrent = fast_all && c->concurrent && G > 0 && T_all > 0;
   const bool split_sms = concurrent && c->prefix_share < 0.999f;
-  const int32_t prefix_sms = split_sms ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
-  const int32_t suffix_sms = split_sms ? std::max(1, c->num_sms - prefix_sms) : c->num_sms;
+  const bool auto_share = split_sms && c->prefix_share <= 0.f;
+  const int32_t prefix_sms =
+      split_sms && !auto_share ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
+  int32_t suffix_sms = c->num_sms;  // set after the prefix pieces when the SMs are split
 
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
   //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
@@ -585,6 +590,36 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       if (ctas_for(mid) <= target) hi = mid;
       else lo = mid + 1;
     }
+    bool auto_found = false;
+    if (auto_share) {
+      // Automatic split: the piece length whose prefix time (one wave: the longest piece) and
+      // suffix time (its work spread over the SMs the prefix CTAs leave) are most nearly equal,
+      // i.e. the smallest max of the two.  Costs measured on GB300: a prefix CTA 5 us plus, per
+      // 128-query-row block and token, 0.01 us (dense) or 0.02 us (cascade); the suffix 1.40
+      // SM-us per 16 COLD tokens of one group of up to 8 KV heads.
+      double w_s = 0.0;
+      const int64_t head_groups = (n_kv + 7) / 8;
+      for (int32_t b = 0; b < B; ++b) w_s += 1.40 * (double)head_groups * (double)((bt->seq_len[b] + 15) / 16);
+      double best = 1e300;
+      for (int64_t n = 1; n <= max_tiles; ++n) {
+        const int64_t cand = (max_tiles + n - 1) / n;
+        if (n > 1 && cand == (max_tiles + n - 2) / (n - 1)) continue;  // same length as n - 1
+        const int64_t ctas = ctas_for(cand);
+        if (ctas >= c->num_sms) break;  // one wave, and at least one SM for the suffix
+        double t_p = 0.0;
+        for (int32_t i = 0; i < G; ++i) {
+          const int64_t tile = tile_tokens_for(groups[i].impl);
+          const double per_token = groups[i].impl == kImplDenseTc ? 0.01 : 0.02;
+          t_p = std::max(t_p, 5.0 + per_token * (double)std::min<int64_t>(cand * tile, groups[i].L_p));
+        }
+        const double t = std::max(t_p, w_s / (double)(c->num_sms - ctas));
+        if (t < best) {
+          best = t;
+          lo = cand;
+          auto_found = true;
+        }
+      }
+    }
     for (int32_t i = 0; i < G; ++i) {
       DevGroup& dg = groups[i];
       const int64_t tile = tile_tokens_for(dg.impl);
@@ -597,6 +632,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       dg.n_long = (int32_t)(t - base * n_splits);
       dg.pad[0] = dg.pad[1] = dg.pad[2] = 0;
     }
+    // the tensor-core prefix kernels hold one SM per CTA; the suffix gets every other SM (an
+    // automatic split that found no piece length leaving the suffix an SM shares them all)
+    if (split_sms && (!auto_share || auto_found))
+      suffix_sms = (int32_t)std::max<int64_t>(1, (int64_t)c->num_sms - ctas_for(lo));
   }
   for (int32_t i = 0; i < G; ++i) {
     const DevGroup& dg = groups[i];
@@ -609,19 +648,22 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     gi.n_splits = dg.n_splits;
     gi.slot_offset = dg.slab_off;
   }
-  // 4. suffix: cut the concatenation of all requests' COLD tokens into one equal run per
-  //    token-CTA (stream-K); each request segment inside a run is one work item and record
+  // 4. suffix: cut the concatenation of all requests' COLD tokens, in 16-token tiles counted
+  //    per request (a request's last tile may be partial), into one equal run of tiles per
+  //    token-CTA (stream-K); each request segment inside a run is one work item and record.
+  //    Cuts fall on tile boundaries of the request, so a CTA's time follows its tile count.
+  constexpr int64_t kSTile = 16;
   int64_t T = 0;
-  for (int32_t b = 0; b < B; ++b) T += bt->seq_len[b];
+  for (int32_t b = 0; b < B; ++b) T += (bt->seq_len[b] + kSTile - 1) / kSTile;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
   int32_t n_scta = 0;
-  int64_t quota = 1;
+  int64_t quota = 1;  // tiles per token-CTA
   if (T > 0) {
     // one wave over the suffix's SMs, unless a CTA would then stream more tokens than it can
     // stage slot ids for
-    n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + 15) / 16);
-    n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens - 1) / kSuffixMaxCtaTokens);
+    n_scta = (int32_t)std::min<int64_t>(suffix_sms, T);
+    n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens / kSTile - 1) / (kSuffixMaxCtaTokens / kSTile));
     quota = (T + n_scta - 1) / n_scta;
   }
 
@@ -646,12 +688,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     const int32_t L = bt->seq_len[b];
     r.seq_len = L;
     int32_t k = 0;
-    for (int64_t t = 0; t < L;) {
-      const int64_t take = std::min<int64_t>(L - t, quota - used);
+    const int64_t n_t = (L + kSTile - 1) / kSTile;
+    for (int64_t t = 0; t < n_t;) {
+      const int64_t take = std::min<int64_t>(n_t - t, quota - used);
       DevSuffixItem it;
       it.b = b;
-      it.t0 = (int32_t)t;
-      it.t1 = (int32_t)(t + take);
+      it.t0 = (int32_t)(t * kSTile);
+      it.t1 = (int32_t)std::min<int64_t>((t + take) * kSTile, L);
       it.rec = (int32_t)(rec + r.n_prefix + k);
       sitems.push_back(it);
       ++k;
@@ -782,7 +825,7 @@ granikv_status granikv_workspace_size(granikv_ctx* c, const granikv_plan* p, siz
 }
 
 granikv_status granikv_set_concurrency(granikv_ctx* c, int32_t on, float share) {
-  if (!c || !(share > 0.f && share <= 1.f)) return GRANIKV_ERR_INVALID;
+  if (!c || !(share >= 0.f && share <= 1.f)) return GRANIKV_ERR_INVALID;
   c->concurrent = on ? 1 : 0;
   c->prefix_share = share;
   return GRANIKV_OK;
@@ -885,12 +928,14 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   c->last_tickets_bytes = tickets_bytes;
 
   cudaError_t e = cudaSuccess;
-  auto launch_suffix = [&](cudaStream_t st) -> cudaError_t {
+  auto launch_suffix = [&](cudaStream_t st, bool pdl) -> cudaError_t {
     if (p->n_sitems <= 0) return cudaSuccess;
     c->n_kernels += 1;
-    return p->suffix_impl == kImplSuffixMma ? launch_suffix_mma(a, a.scta_begin, p->n_scta, st)
+    return p->suffix_impl == kImplSuffixMma ? launch_suffix_mma(a, a.scta_begin, p->n_scta, st, pdl)
                                             : launch_suffix_generic(c->cfg.dtype, a, st);
   };
+  // programmatic dependent launch only between kernels of this call on one stream, and for the
+  // first prefix kernel (whose stream predecessor is whatever the caller enqueued last)
   auto launch_prefix = [&](cudaStream_t st) -> cudaError_t {
     cudaError_t r = cudaSuccess;
     if (p->pitem_count[kImplGeneric] > 0) {
@@ -903,8 +948,9 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     }
     if (r == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
       if (!c->has_tmaps) return cudaErrorNotSupported;
+      const bool first = p->pitem_count[kImplGeneric] == 0 && p->pitem_count[kImplCascadeMma] == 0;
       r = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
-                          c->tmap_v[layer], st);
+                          c->tmap_v[layer], st, first);
       c->n_kernels += 1;
     }
     return r;
@@ -915,18 +961,21 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     e = cudaEventRecord(c->ev_fork, s);
     if (e == cudaSuccess) e = launch_prefix(s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c->aux, c->ev_fork, 0);
-    if (e == cudaSuccess) e = launch_suffix(c->aux);
+    if (e == cudaSuccess) e = launch_suffix(c->aux, false);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_join, c->aux);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_join, 0);
     if (e == cudaSuccess && !p->fused) {
-      e = launch_merge(c->cfg.dtype, a, s);
+      e = launch_merge(c->cfg.dtype, a, s, false);
       c->n_kernels += 1;
     }
   } else {
     e = launch_prefix(s);
-    if (e == cudaSuccess) e = launch_suffix(s);
+    // the suffix kernel follows a prefix kernel of this call, the merge the suffix kernel
+    const bool after_prefix = p->n_pitems > 0 && p->pitem_count[kImplDenseTc] > 0;
+    if (e == cudaSuccess) e = launch_suffix(s, after_prefix && p->suffix_impl == kImplSuffixMma);
     if (e == cudaSuccess && !p->fused) {
-      e = launch_merge(c->cfg.dtype, a, s);
+      const bool after_suffix = p->n_sitems > 0 && p->suffix_impl == kImplSuffixMma;
+      e = launch_merge(c->cfg.dtype, a, s, after_suffix);
       c->n_kernels += 1;
     }
   }

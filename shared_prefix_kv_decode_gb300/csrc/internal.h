@@ -20,6 +20,8 @@ enum DevErr : int32_t {
   kDevTableOverflow = 2,  // a token table row would pass cap
   kDevBadSlab = 3,        // a slab range outside [0, n_hot)
   kDevBadRecord = 4,      // a partial-state record index outside the workspace
+  kDevSmemAlign = 5,      // a kernel's dynamic shared memory was not aligned as its layout needs
+  kDevTimeout = 6,        // a bounded mbarrier wait expired (the CTA drained and gave up)
 };
 
 // Kernel implementations a prefix group or the suffix pass can run on.
@@ -109,6 +111,8 @@ struct AttnParams {
 };
 
 // ---- launchers (kernels_*.cu) ------------------------------------------------------------
+// `pdl`: launch as a programmatic dependent of the previous kernel in the stream (see
+// launch_util.cuh); only for a kernel whose stream predecessor is a kernel of this library.
 cudaError_t launch_cold_alloc(const int32_t* excl /*[B+1]*/, int32_t B, const int32_t* ring,
                               int64_t n_cold, int64_t head, int32_t* req_to_slot,
                               int32_t* suffix_len, int32_t cap, int32_t* slots_out,
@@ -124,11 +128,12 @@ cudaError_t launch_cold_append(int32_t dtype, const void* k_new, const void* v_n
 cudaError_t launch_prefix_generic(int32_t dtype, const AttnParams& p, int32_t first_item,
                                   int32_t n_items, cudaStream_t s);
 cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream_t s);
-cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s);
-cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int32_t n_cta, cudaStream_t s);
+cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int32_t n_cta, cudaStream_t s,
+                              bool pdl);
 cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
-                            const CUtensorMap& tmv, cudaStream_t s);
+                            const CUtensorMap& tmv, cudaStream_t s, bool pdl);
 
 constexpr int kNumImpl = 4;
 

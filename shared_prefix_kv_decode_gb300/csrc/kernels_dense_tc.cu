@@ -9,7 +9,9 @@
 // (request, head-in-group) pairs of KV head j, so M = 128 query rows share every K/V tile.
 // Per 128-token tile i:
 //     S(i) = Q K(i)^T   (M=128, N=128, K=128: 8 tcgen05.mma from shared memory, fp32 in TMEM)
-//     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps; bf16, written back over S(i) in TMEM)
+//     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps; bf16, written back over S(i) in TMEM;
+//            three quarters of the exponentials on MUFU, one quarter as a polynomial on the FMA
+//            pipe, so the two units share the load)
 //     O   += P(i) V(i)  (M=128, N=128, K=128: 8 tcgen05.mma with A = P(i) read from TMEM)
 // Every MMA is 128x128x16, so one issuing thread keeps the tensor core fed.
 // Roles:
@@ -21,7 +23,10 @@
 //  * warps 8 and 9, TMA loads (two 64-dim halves per tile, 128-byte swizzle), each in a warp of
 //    its own: warp 8 fills a 2-slot K ring whose slots free up as soon as S(i) completes, warp 9
 //    a 3-slot V ring freed by PV(i).
-//  * warp 10, the MMAs: PV(i), then S(i+2) (three S/P buffers in TMEM).
+//  * warp 10, the MMAs, issued as their inputs become ready: S(j) up to three tiles ahead of
+//    the PV products (three S/P buffers in TMEM), PV(i) once the softmax has written P(i).
+// The K producer initialises the barriers and issues the first K and V tiles before the Q
+// gather, so their HBM latency overlaps it.
 // The running max is only moved (and O rescaled in TMEM) when it grows by more than 2^8; the
 // final normalisation uses the same max, so the result is the exact softmax.  Every mbarrier
 // wait is bounded in time; on expiry the CTA raises an abort flag, latches an error, drains what
@@ -29,6 +34,7 @@
 #include <cuda.h>
 
 #include "internal.h"
+#include "launch_util.cuh"
 #include "merge_util.cuh"
 #include "mma_util.cuh"
 #include "tc_util.cuh"
@@ -44,7 +50,6 @@ constexpr int kHalfCols = kN / 2;             // S columns per softmax thread
 constexpr int kKSlots = 2;                    // slots of the K ring
 constexpr int kVSlots = 3;                    // slots of the V ring
 constexpr int kSBufs = 3;                     // S/P buffers in TMEM
-constexpr int kAhead = kSBufs - 1;            // S(i + kAhead) is issued right after PV(i)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kWarpTmaK = 8, kWarpTmaV = 9, kWarpMma = 10;
@@ -65,7 +70,6 @@ constexpr uint32_t kColO = 384;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;     // log2 of the largest growth tolerated in P
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int32_t kDevTimeout = 6;
 
 enum : int {
   kBarKFull = 0,                            // [kKSlots] TMA -> MMA (K)
@@ -111,7 +115,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (t1 - t0 + kN - 1) / kN;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
 
-  if (tid == 0) {
+  // The K producer thread initialises the barriers and issues the first K and V tiles at once,
+  // so their HBM latency overlaps the Q gather below; its loop later starts after them.
+  const int k_pre = min(n_tiles, kKSlots), v_pre = min(n_tiles, kVSlots);
+  auto issue_tile = [&](bool is_k, int i) {
+    const CUtensorMap* tm = is_k ? &tmk : &tmv;
+    const int slots = is_k ? kKSlots : kVSlots;
+    const int full = (is_k ? kBarKFull : kBarVFull) + i % slots;
+    const uint32_t dst = (is_k ? sK : sV) + (i % slots) * kTile;
+    const int32_t z = (int32_t)(gr.slab_off + t0 + i * kN);
+    mbar_arrive_expect_tx(bar(full), kTile);
+    tma_load_3d(dst, tm, 0, j, z, bar(full));
+    tma_load_3d(dst + kHalf, tm, 64, j, z, bar(full));
+  };
+  if (warp == kWarpTmaK && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1u;
       if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxThreads;
@@ -121,15 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = slab_ok ? 0 : 1;
     if (!slab_ok) atomicCAS(p.err, 0, (int32_t)kDevBadSlab);
     mbar_fence_init();
+    fence_proxy_async_smem();
+    grid_dep_wait();  // the slab may have been written by the work before this kernel
+    if (slab_ok) {
+      for (int i = 0; i < k_pre; ++i) issue_tile(true, i);
+      for (int i = 0; i < v_pre; ++i) issue_tile(false, i);
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpTmaK && lane == 0) {
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
-  }
+  // q and the records are touched only after the previous kernel in the stream has completed
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   // Q rows of this block -> shared memory, K-major with 128-byte swizzle: row r, 16-byte
   // chunk c lives in 64-dim block c/8 at r*128 + ((c%8) ^ (r%8))*16; rows past the group are 0
   const int32_t rbase = it.row_block * kM;
@@ -155,24 +179,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTmaK || warp == kWarpTmaV) {
     // ---------------- TMA producers: warp 8 the K ring, warp 9 the V ring ----------------
-    if (lane == 0 && !*abort_flag) {
-      const bool is_k = warp == kWarpTmaK;
-      const CUtensorMap* tm = is_k ? &tmk : &tmv;
-      const uint32_t ring = is_k ? sK : sV;
-      const int full = is_k ? kBarKFull : kBarVFull;
-      const int empty = is_k ? kBarKEmpty : kBarVEmpty;
-      const int slots = is_k ? kKSlots : kVSlots;
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+    const bool is_k = warp == kWarpTmaK;
+    const int full = is_k ? kBarKFull : kBarVFull;
+    const int empty = is_k ? kBarKEmpty : kBarVEmpty;
+    const int slots = is_k ? kKSlots : kVSlots;
+    // the first `slots` tiles were issued before the block-wide barrier (when the slab is valid)
+    int issued = slab_ok ? (is_k ? k_pre : v_pre) : 0;
+    if (lane == 0) {
+      for (int i = issued; i < n_tiles && !*abort_flag; ++i) {
         const int st = i % slots;
-        if (i >= slots && !mbar_wait_bounded(bar(empty + st), ((i / slots) - 1) & 1, abort_flag, p.err,
-                                             kDevTimeout, kWaitLimitNs))
+        if (!mbar_wait_bounded(bar(empty + st), ((i / slots) - 1) & 1, abort_flag, p.err, kDevTimeout,
+                               kWaitLimitNs))
           break;
-        const uint32_t dst = ring + st * kTile;
-        const int32_t z = (int32_t)(gr.slab_off + t0 + i * kN);
-        mbar_arrive_expect_tx(bar(full + st), kTile);
-        tma_load_3d(dst, tm, 0, j, z, bar(full + st));
-        tma_load_3d(dst + kHalf, tm, 64, j, z, bar(full + st));
+        issue_tile(is_k, i);
         issued = i + 1;
       }
       // never leave with a copy in flight: wait for every issued tile to land
@@ -200,51 +219,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kHalf apart (leading offset), 8-token groups 1024 bytes apart (stride)
       const uint64_t dv0 = smem_desc_sw128(sV, kHalf, 1024);
       int committed = 0;
-      auto issue_s = [&](int i) -> bool {
-        const int st = i % kKSlots;
-        if (!mbar_wait_bounded(bar(kBarKFull + st), (i / kKSlots) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t dS = tmem + (uint32_t)((i % kSBufs) * kN);
-        const uint64_t dk = dk0 + (uint64_t)((st * kTile) >> 4);
+      // Event-driven issue (non-blocking barrier tests): PV(i) as soon as P(i) and V(i) are
+      // ready, S(j) as soon as K(j) has landed and its TMEM buffer is free.  S(j) overwrites S(j-3)/P(j-3), so it may go in once
+      // PV(j-3), the last reader of P(j-3), has been issued (tcgen05 MMAs of one thread execute
+      // in order; the softmax finished with S(j-3) before it produced P(j-3)).  Polling both
+      // conditions keeps the issuing thread from sitting on one while the other is ready.
+      int next_s = 0, next_pv = 0;
+      uint64_t t_last = globaltimer_ns();
+      while (next_pv < n_tiles) {
+        bool progressed = false;
+        if (next_pv < next_s) {
+          const int i = next_pv;
+          const int st = i % kVSlots;
+          const int sb = i % kSBufs;
+          if (mbar_test_wait(bar(kBarPFull + sb), (i / kSBufs) & 1) &&
+              mbar_test_wait(bar(kBarVFull + st), (i / kVSlots) & 1)) {
+            tc_fence_after();
+            const uint32_t pa = tmem + (uint32_t)(sb * kN);  // P(i): 64 columns, two tokens per column
+            const uint64_t dv = dv0 + (uint64_t)((st * kTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = dq0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t b = dk + (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
-          umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kN / 16; ++ks)
+              umma_f16_ts(tmem + kColO, pa + (uint32_t)(ks * 8), dv + (uint64_t)((ks * 2048) >> 4), idO,
+                          (i > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(bar(kBarVEmpty + st));
+            umma_commit(bar(kBarPvDone + sb));
+            committed += 2;
+            ++next_pv;
+            progressed = true;
+          }
         }
-        umma_commit(bar(kBarSFull + i % kSBufs));
-        umma_commit(bar(kBarKEmpty + st));
-        committed += 2;
-        return true;
-      };
-      // PV(i) then S(i+kAhead): S(i+kAhead) overwrites the TMEM buffer of S(i-1)/P(i-1); the
-      // softmax finished with S(i-1) before it produced P(i-1) (waited for one iteration
-      // earlier), and PV(i-1), which reads P(i-1), was issued before it, and tcgen05 MMAs of
-      // one thread execute in order.
-      bool ok = true;
-      for (int i = 0; ok && i < kAhead && i < n_tiles; ++i) ok = issue_s(i);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % kVSlots;
-        const int sb = i % kSBufs;
-        if (!mbar_wait_bounded(bar(kBarPFull + sb), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
-                               kWaitLimitNs) ||
-            !mbar_wait_bounded(bar(kBarVFull + st), (i / kVSlots) & 1, abort_flag, p.err, kDevTimeout,
-                               kWaitLimitNs)) {
-          ok = false;
+        if (next_s < n_tiles && next_s < next_pv + kSBufs) {
+          const int i = next_s;
+          const int st = i % kKSlots;
+          if (mbar_test_wait(bar(kBarKFull + st), (i / kKSlots) & 1)) {
+            tc_fence_after();
+            const uint32_t dS = tmem + (uint32_t)((i % kSBufs) * kN);
+            const uint64_t dk = dk0 + (uint64_t)((st * kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t a = dq0 + (uint64_t)(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+              const uint64_t b = dk + (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4);
+              umma_f16(dS, a, b, idS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(kBarSFull + i % kSBufs));
+            umma_commit(bar(kBarKEmpty + st));
+            committed += 2;
+            ++next_s;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+        } else if (*abort_flag) {
+          break;
+        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicCAS(p.err, 0, (int32_t)kDevTimeout);
           break;
         }
-        tc_fence_after();
-        const uint32_t pa = tmem + (uint32_t)(sb * kN);  // P(i): 64 columns, two tokens per column
-        const uint64_t dv = dv0 + (uint64_t)((st * kTile) >> 4);
-#pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks)
-          umma_f16_ts(tmem + kColO, pa + (uint32_t)(ks * 8), dv + (uint64_t)((ks * 2048) >> 4), idO,
-                      (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(bar(kBarVEmpty + st));
-        umma_commit(bar(kBarPvDone + sb));
-        committed += 2;
-        if (i + kAhead < n_tiles && !issue_s(i + kAhead)) ok = false;
       }
       // drain: every tcgen05 op this thread issued completes before the CTA frees TMEM
       if (committed > 0) {
@@ -266,6 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)((quad * 32) << 16);
     const int pair_bar = kBarPair + quad;           // mbarrier of the two warps sharing rows
     const float scale = p.scale_log2;
+    // this row's request, head and record, looked up now so the loads finish during the tiles
+    const int32_t row = rbase + r;
+    int32_t b = -1, h = 0, rec = -1;
+    if (row < rows) {
+      b = p.group_req[gr.req_begin + row / g];
+      h = j * g + row % g;
+      rec = p.reqs[b].rec_base + it.split;
+    }
     float m_used = -INFINITY;  // running max in scaled (base-2) units, identical in both halves
     float l = 0.f;             // this half's share of the row sum
     int pair_phase = 0;
@@ -348,8 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float a = ex2_approx(fmaf(s[2 * k], scale, nm));
-        const float b = ex2_approx(fmaf(s[2 * k + 1], scale, nm));
+        const float xa = fmaf(s[2 * k], scale, nm), xb = fmaf(s[2 * k + 1], scale, nm);
+        float a, b;
+        if ((k & 3) == 3) {  // a quarter of the exponentials on the FMA pipe, the rest on MUFU
+          a = ex2_poly3(xa);
+          b = ex2_poly3(xb);
+        } else {
+          a = ex2_approx(xa);
+          b = ex2_approx(xb);
+        }
         ps[k & 3] += a + b;
         pk[k] = pack_bf16(a, b);
       }
@@ -395,16 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float lt = l0 + l1;
-      const int32_t row = rbase + r;
-      int32_t b = -1, h = 0, rec = -1;
-      if (row < rows) {
-        b = p.group_req[gr.req_begin + row / g];
-        h = j * g + row % g;
-        rec = p.reqs[b].rec_base + it.split;
-        if (rec < 0 || rec >= p.n_records) {
-          if (half == 0) atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
-          rec = -1;
-        }
+      if (row < rows && (rec < 0 || rec >= p.n_records)) {
+        if (half == 0) atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
+        rec = -1;
       }
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       float* dst = rec >= 0 ? p.rec_o + ((int64_t)rec * p.n_q + h) * kD + half * 64 : nullptr;
@@ -450,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
-                            const CUtensorMap& tmv, cudaStream_t s) {
+                            const CUtensorMap& tmv, cudaStream_t s, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   static bool attr_done = false;
   if (!attr_done) {
@@ -458,8 +498,7 @@ cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_i
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  dense_tc_kernel<<<n_items, kThreads, kSmemBytes, s>>>(p, first_item, tmk, tmv);
-  return cudaGetLastError();
+  return launch_kernel(dense_tc_kernel, dim3(n_items), dim3(kThreads), kSmemBytes, s, pdl, p, first_item, tmk, tmv);
 }
 
 }  // namespace granikv

@@ -9,6 +9,7 @@
 //
 // These kernels serve the fp32 path and every shape the tensor-core kernels do not cover.
 #include "internal.h"
+#include "launch_util.cuh"
 
 #include <cuda_bf16.h>
 
@@ -279,6 +280,8 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
 constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(256) merge_bf16_d128_kernel(AttnParams p) {
+  grid_dep_wait();  // the records are complete once the kernels before this one are
+  grid_dep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // b * n_q + h
   if (row >= (int64_t)p.B * p.n_q) return;
@@ -352,11 +355,16 @@ cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
   }
 }
 
-cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s, bool pdl) {
   if (dtype == 1 && p.d == 128) {
+    static bool attr_done = false;
+    if (!attr_done) {
+      cudaError_t e = prefer_max_shared(merge_bf16_d128_kernel);
+      if (e != cudaSuccess) return e;
+      attr_done = true;
+    }
     const int64_t rows = (int64_t)p.B * p.n_q;
-    merge_bf16_d128_kernel<<<(int)((rows + 7) / 8), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(merge_bf16_d128_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, pdl, p);
   }
   return dtype == 1 ? launch_merge_t<__nv_bfloat16>(p, s) : launch_merge_t<float>(p, s);
 }

@@ -37,6 +37,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same (try_wait may suspend the thread for a while when the phase is
+// not complete; a thread that polls several barriers uses this instead).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns false) when another
 // role has raised the CTA's abort flag, or after `limit_ns`, in which case it raises the flag
 // and latches `code` in the device error word.  No wait in these kernels is unbounded.
@@ -165,10 +177,30 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// 2^x on the special-function unit (MUFU)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA and integer pipes, for x <= 126 (x below -126 is clamped there, giving a
+// value below 2^-126, i.e. zero for the sums it enters).  Range reduction 2^x = 2^j * 2^f with
+// j = rint(x): adding 1.5 * 2^23 rounds x to an integer that then sits in the low mantissa
+// bits of the sum, and shifting those bits left by 23 adds j to the exponent field of 2^f
+// (the exponent-field construction of Schraudolph, "A fast, compact approximation of the
+// exponential function", Neural Computation 11(4), 1999).  2^f on [-1/2, 1/2] is a cubic
+// minimax fit in relative error (max 7.5e-5 in f32 arithmetic; exp2_poly_fit.py derives the
+// coefficients by linear programming).
+__device__ __forceinline__ float ex2_poly3(float x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  x = fmaxf(x, -126.0f);
+  const float t = __fadd_rn(x, kRound);
+  const float f = __fsub_rn(x, __fsub_rn(t, kRound));
+  float q = fmaf(0.05517224967479706f, f, 0.24261115491390228f);
+  q = fmaf(q, f, 0.6932608485221863f);
+  q = fmaf(q, f, 0.9999281167984009f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
 }
 
 }  // namespace granikv

@@ -7,9 +7,9 @@ measure M_sat = 1024 on A100 and say other GPUs need a re-fit ("Limitations").
 This sweeps the Llama-3.1-8B attention shape (32/8/128, bf16) over
 L_p in {512, 2048, 8192, 16384, 32768} x B in {1, 8, 32, 128, 256, 512} with 256 COLD tokens
 per request, timing decode attention with the backend forced to DENSE, forced to CASCADE, and
-dispatched (AUTO).  The L2 is flushed before every timed call.  M_sat is the smallest grid
-M_eff at which dense is no slower than cascade for every L_p >= 2048, at that M_eff and at
-every larger one.
+dispatched (AUTO).  The L2 is flushed before every timed call.  M_sat is the grid threshold
+whose dispatch loses the least time against the faster backend of each cell (summed log
+slowdown over the table).
 
   python -m shared_prefix_kv_decode_gb300.msat_fit [--reps 20] [--json out.json]
 """
@@ -70,17 +70,22 @@ def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch):
 
 
 def fit_msat(rows, g=4):
-    """Smallest grid M_eff such that dense <= cascade for every L_p >= 2048 at that M_eff and all
-    larger grid M_eff; None if dense never wins that way."""
+    """The threshold that fits the measured table best: among the grid's M_eff values (and one
+    past the largest, i.e. cascade everywhere), the M_sat whose dispatch (dense at M_eff >= M_sat,
+    cascade below) has the smallest summed log slowdown against the faster backend of each cell.
+    Ties go to the larger M_sat.  A single noisy cell thus moves the threshold only when it
+    outweighs the cells on the other side."""
     meffs = sorted({r["B"] * g for r in rows})
-    ok = {}
-    for me in meffs:
-        cells = [r for r in rows if r["B"] * g == me and r["L_p"] >= 2048]
-        ok[me] = all(r["dense_us"] <= r["cascade_us"] for r in cells)
-    for i, me in enumerate(meffs):
-        if all(ok[m] for m in meffs[i:]):
-            return me
-    return None
+    cands = meffs + [2 * meffs[-1]]
+
+    def regret(m_sat):
+        tot = 0.0
+        for r in rows:
+            t = r["dense_us"] if r["B"] * g >= m_sat else r["cascade_us"]
+            tot += math.log(t / min(r["dense_us"], r["cascade_us"]))
+        return tot
+
+    return min(cands, key=lambda m: (round(regret(m), 12), -m))
 
 
 def main(argv=None):

@@ -188,11 +188,12 @@ def test_backends_agree(cuda_ok):
 
 @pytest.mark.parametrize("backend", ["dense", "cascade"])
 @pytest.mark.parametrize("setting", [(False, 0.5, False), (True, 0.3, False), (True, 1.0, False),
-                                     (False, 0.5, True), (True, 0.3, True), (True, 0.5, True),
-                                     (True, 1.0, True)])
+                                     (True, 0.0, False), (False, 0.5, True), (True, 0.3, True),
+                                     (True, 0.5, True), (True, 1.0, True), (True, 0.0, True)])
 def test_concurrency_and_merge_settings(cuda_ok, backend, setting):
-    """The suffix kernel on its own stream next to the prefix kernel (several SM shares) or
-    serial, with the merge kernel or the last-producer merge: every setting matches the oracle
+    """The suffix kernel on its own stream next to the prefix kernel (several SM shares, 0 for
+    the automatic one) or serial, with the merge kernel or the last-producer merge: every
+    setting matches the oracle
     and repeats bit for bit (records are merged in record order, whoever merges them)."""
     wl = W.medium_shared(2, q_scale=1.0)
     lw = _load(wl)

@@ -202,3 +202,28 @@ def test_dispatch_host_time_under_budget(granikv_lib):
         lib.granikv_dispatch(ctx.handle, C.byref(batch.c), plan.handle)
     per = (time.perf_counter() - t) / n
     assert per < 200e-6
+
+
+def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
+    """The prefix work list is sized for the prefix's share of the SMs (152 on a host-only
+    context): all SMs when serial or at share 1, fewer pieces at share 0.5, and the automatic
+    share (0) in between for a step whose prefix work outweighs its suffix work."""
+    ctx = _host_ctx(n_slots=200000)
+    sid, _ = ctx.hot_alloc(16384)
+    slabs, seq = [sid] * 64, [300] * 64
+
+    def splits(on, share):
+        ctx.set_concurrency(on, share)
+        return _dispatch_groups(ctx, slabs, seq)[0]["n_splits"]
+
+    n_serial = splits(False, 0.0)
+    n_full = splits(True, 1.0)
+    n_half = splits(True, 0.5)
+    n_auto = splits(True, 0.0)
+    # 8 KV heads x 2 row blocks per piece: 9 pieces fill 144 of 152 SMs, 4 fill 64 of 76
+    assert n_serial == n_full == 9
+    assert n_half == 4
+    assert n_half < n_auto < n_full
+    for bad in (-0.1, 1.5, float("nan")):
+        with pytest.raises(gb.GranikvError):
+            ctx.set_concurrency(True, bad)

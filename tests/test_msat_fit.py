@@ -1,15 +1,15 @@
-"""The M_sat re-fit rule on hand-made timing tables (no GPU): the smallest grid M_eff at which
-dense is no slower than cascade for every L_p >= 2048, at that M_eff and all larger ones
-("3 GraniKV" per-step dispatch; "Limitations": the threshold is hardware-specific)."""
+"""The M_sat re-fit rule on hand-made timing tables (no GPU): the grid threshold whose dispatch
+(dense at M_eff >= M_sat) loses the least time against the faster backend of each cell ("3
+GraniKV" per-step dispatch; "Limitations": the threshold is hardware-specific)."""
 
 from shared_prefix_kv_decode_gb300.msat_fit import fit_msat
 
 
-def _rows(win):
+def _rows(win, slow=2.0):
     rows = []
     for L_p in (512, 2048, 8192):
         for B in (1, 8, 32, 128, 256):
-            d, c = (1.0, 2.0) if win(L_p, B) else (2.0, 1.0)
+            d, c = (1.0, slow) if win(L_p, B) else (slow, 1.0)
             rows.append({"L_p": L_p, "B": B, "dense_us": d, "cascade_us": c})
     return rows
 
@@ -18,15 +18,22 @@ def test_crossover_at_first_winning_meff():
     assert fit_msat(_rows(lambda L, B: B >= 32)) == 128
 
 
-def test_short_prefixes_do_not_count():
-    # dense loses at L_p = 512 for every B but wins above 2048 from B = 8 on
+def test_majority_of_cells_decides():
+    # dense loses at L_p = 512 for every B but wins above 2048 from B = 8 on: the threshold
+    # B = 8 (M_eff 32) gives up four short-prefix cells and keeps eight long-prefix ones
     assert fit_msat(_rows(lambda L, B: L >= 2048 and B >= 8)) == 32
 
 
-def test_a_loss_above_moves_the_threshold_up():
-    # dense wins at B = 32 but loses again at B = 128 (one L_p), so only B >= 256 qualifies
-    assert fit_msat(_rows(lambda L, B: (B >= 32 and not (B == 128 and L == 8192)))) == 1024
+def test_one_loss_above_does_not_move_the_threshold():
+    # dense wins from B = 32 on except one cell (B = 128, L_p = 8192)
+    assert fit_msat(_rows(lambda L, B: (B >= 32 and not (B == 128 and L == 8192)))) == 128
 
 
-def test_never_wins():
-    assert fit_msat(_rows(lambda L, B: False)) is None
+def test_many_losses_above_move_it():
+    # dense loses at B = 32 and 128 for every L_p, wins only at B = 256
+    assert fit_msat(_rows(lambda L, B: B >= 256 or B == 8)) == 1024
+
+
+def test_always_and_never():
+    assert fit_msat(_rows(lambda L, B: True)) == 4
+    assert fit_msat(_rows(lambda L, B: False)) > 4 * 256
