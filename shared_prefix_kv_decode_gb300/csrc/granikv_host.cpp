@@ -658,13 +658,14 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
   int32_t n_scta = 0;
-  int64_t quota = 1;  // tiles per token-CTA
+  int64_t q_base = 1, q_extra = 0;  // token-CTA k streams q_base tiles, plus one if k < q_extra
   if (T > 0) {
     // one wave over the suffix's SMs, unless a CTA would then stream more tokens than it can
     // stage slot ids for
     n_scta = (int32_t)std::min<int64_t>(suffix_sms, T);
     n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens / kSTile - 1) / (kSuffixMaxCtaTokens / kSTile));
-    quota = (T + n_scta - 1) / n_scta;
+    q_base = T / n_scta;
+    q_extra = T % n_scta;
   }
 
   // 5. records and work items
@@ -690,6 +691,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     int32_t k = 0;
     const int64_t n_t = (L + kSTile - 1) / kSTile;
     for (int64_t t = 0; t < n_t;) {
+      const int64_t quota = q_base + (cta < q_extra ? 1 : 0);
       const int64_t take = std::min<int64_t>(n_t - t, quota - used);
       DevSuffixItem it;
       it.b = b;
@@ -955,7 +957,20 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     }
     return r;
   };
-  if (p->concurrent) {
+  const bool one_launch = p->concurrent && c->has_tmaps && p->n_pitems > 0 &&
+                          p->pitem_count[kImplDenseTc] == p->n_pitems && p->suffix_impl == kImplSuffixMma &&
+                          p->n_sitems > 0;
+  if (one_launch) {
+    // the dense prefix items and the suffix token-CTAs side by side in one grid, then the
+    // merge: both chained to their stream predecessor by programmatic dependent launch
+    e = launch_prefix_suffix_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
+                                c->tmap_v[layer], a.scta_begin, p->n_scta, s, true);
+    c->n_kernels += 1;
+    if (e == cudaSuccess && !p->fused) {
+      e = launch_merge(c->cfg.dtype, a, s, true);
+      c->n_kernels += 1;
+    }
+  } else if (p->concurrent) {
     // fork: the suffix kernel runs on the auxiliary stream next to the prefix kernel (enqueued
     // first, so the longer prefix work starts first); join before anything else on the stream
     e = cudaEventRecord(c->ev_fork, s);

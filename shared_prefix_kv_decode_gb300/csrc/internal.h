@@ -134,6 +134,11 @@ cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int
 cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, cudaStream_t s, bool pdl);
+// One launch for both: CTAs [0, n_dense) run dense prefix items first_item.., the rest the
+// suffix token-CTAs (n_scta per KV-head group of eight).
+cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_item, int32_t n_dense, const CUtensorMap& tmk,
+                                    const CUtensorMap& tmv, const int32_t* cta_begin, int32_t n_scta, cudaStream_t s,
+                                    bool pdl);
 
 constexpr int kNumImpl = 4;
 

@@ -177,6 +177,38 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---- packed f32x2 arithmetic (sm_100 family): two floats in one 64-bit register ----------
+
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// three-input maximum (sm_100 family)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x on the special-function unit (MUFU)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -184,7 +216,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA and integer pipes, for x <= 126 (x below -126 is clamped there, giving a
+// 2^x for two packed floats on the FMA and integer pipes, for x <= 126 (x below -126 is clamped there, giving a
 // value below 2^-126, i.e. zero for the sums it enters).  Range reduction 2^x = 2^j * 2^f with
 // j = rint(x): adding 1.5 * 2^23 rounds x to an integer that then sits in the low mantissa
 // bits of the sum, and shifting those bits left by 23 adds j to the exponent field of 2^f
@@ -192,6 +224,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // exponential function", Neural Computation 11(4), 1999).  2^f on [-1/2, 1/2] is a cubic
 // minimax fit in relative error (max 7.5e-5 in f32 arithmetic; exp2_poly_fit.py derives the
 // coefficients by linear programming).
+__device__ __forceinline__ uint64_t ex2_poly3_x2(uint64_t x2) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  float xa, xb;
+  f2_unpack(x2, xa, xb);
+  const uint64_t x = f2_pack(fmaxf(xa, -126.0f), fmaxf(xb, -126.0f));
+  const uint64_t t = f2_add(x, f2_pack(kRound, kRound));
+  const uint64_t f = f2_sub(x, f2_sub(t, f2_pack(kRound, kRound)));
+  uint64_t q = f2_fma(f2_pack(0.05517224967479706f, 0.05517224967479706f), f,
+                      f2_pack(0.24261115491390228f, 0.24261115491390228f));
+  q = f2_fma(q, f, f2_pack(0.6932608485221863f, 0.6932608485221863f));
+  q = f2_fma(q, f, f2_pack(0.9999281167984009f, 0.9999281167984009f));
+  float qa, qb, ta, tb;
+  f2_unpack(q, qa, qb);
+  f2_unpack(t, ta, tb);
+  return f2_pack(__int_as_float(__float_as_int(qa) + (__float_as_int(ta) << 23)),
+                 __int_as_float(__float_as_int(qb) + (__float_as_int(tb) << 23)));
+}
+
+// the same for one float
 __device__ __forceinline__ float ex2_poly3(float x) {
   constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
   x = fmaxf(x, -126.0f);

@@ -24,6 +24,14 @@ def header_coefficients():
     return [nums[2], nums[1], nums[0], c3]
 
 
+def test_packed_variant_uses_the_same_coefficients():
+    src = open(HDR).read()
+    body = src[src.index("uint64_t ex2_poly3_x2(uint64_t x2)"):]
+    body = body[:body.index("return")]
+    got = sorted(set(float(v) for v in re.findall(r"([0-9]\.[0-9]{6,})f", body)))
+    assert got == sorted(header_coefficients()), got
+
+
 def test_header_matches_fit():
     pytest.importorskip("scipy")
     coef, err = E.fit(3)
