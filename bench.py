@@ -320,12 +320,24 @@ def run_granikv(args):
     ctx.set_checks(True)
     ctx.set_concurrency(not args.serial, args.prefix_share)
     stream = torch.cuda.current_stream(dev)
-    qs = [lw.q] + [(torch.randn((B, spec.n_q, spec.d), generator=gen, device=dev) / math.sqrt(spec.d)
-                    ).to(torch.bfloat16) for _ in range(L - 1)]
-    knew = [torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
-    vnew = [torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
-    outs = [torch.empty((B, spec.n_q, spec.d), dtype=torch.bfloat16, device=dev) for _ in range(L)]
-    lses = [torch.empty((B, spec.n_q), dtype=torch.float32, device=dev) for _ in range(L)]
+    # A step's inputs (q, new K, new V of every layer) live in one device buffer and its outputs
+    # (o, lse of every layer) in another, so the end-to-end run moves each direction with one
+    # copy per step; the per-layer tensors are views into them.
+    n_qe, n_kve = B * spec.n_q * spec.d, B * spec.n_kv * spec.d
+    in_dev = torch.empty((L, n_qe + 2 * n_kve), dtype=torch.bfloat16, device=dev)
+    qs = [in_dev[layer, :n_qe].view(B, spec.n_q, spec.d) for layer in range(L)]
+    knew = [in_dev[layer, n_qe:n_qe + n_kve].view(B, spec.n_kv, spec.d) for layer in range(L)]
+    vnew = [in_dev[layer, n_qe + n_kve:].view(B, spec.n_kv, spec.d) for layer in range(L)]
+    qs[0].copy_(lw.q)
+    for layer in range(1, L):
+        qs[layer].copy_((torch.randn((B, spec.n_q, spec.d), generator=gen, device=dev) / math.sqrt(spec.d)))
+    for layer in range(L):
+        knew[layer].copy_(torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev))
+        vnew[layer].copy_(torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev))
+    o_bytes, l_bytes = B * spec.n_q * spec.d * 2, B * spec.n_q * 4
+    out_dev = torch.empty((L, o_bytes + l_bytes), dtype=torch.uint8, device=dev)
+    outs = [out_dev[layer, :o_bytes].view(torch.bfloat16).view(B, spec.n_q, spec.d) for layer in range(L)]
+    lses = [out_dev[layer, o_bytes:].view(torch.float32).view(B, spec.n_q) for layer in range(L)]
     slots = torch.empty((B,), dtype=torch.int32, device=dev)
     plan = ctx.plan()
     slab_ids = lw.slab_ids
@@ -391,23 +403,15 @@ def run_granikv(args):
 
     # end to end through the C ABI with host buffers: pinned host inputs copied in and the
     # step's outputs read back inside the timed region, every step
-    q_h = [x.cpu().pin_memory() for x in qs]
-    k_h = [x.cpu().pin_memory() for x in knew]
-    v_h = [x.cpu().pin_memory() for x in vnew]
-    o_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
-    l_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in lses]
-    h2d = sum(x.numel() * x.element_size() for x in q_h + k_h + v_h)
-    d2h = sum(x.numel() * x.element_size() for x in o_h + l_h)
+    in_host = in_dev.cpu().pin_memory()
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    h2d = in_host.numel() * in_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for layer in range(L):
-            qs[layer].copy_(q_h[layer], non_blocking=True)
-            knew[layer].copy_(k_h[layer], non_blocking=True)
-            vnew[layer].copy_(v_h[layer], non_blocking=True)
+        in_dev.copy_(in_host, non_blocking=True)
         step(False)
-        for layer in range(L):
-            o_h[layer].copy_(outs[layer], non_blocking=True)
-            l_h[layer].copy_(lses[layer], non_blocking=True)
+        out_host.copy_(out_dev, non_blocking=True)
 
     barrier(world)
     torch.cuda.synchronize()

@@ -10,6 +10,7 @@
 // These kernels serve the fp32 path and every shape the tensor-core kernels do not cover.
 #include "internal.h"
 #include "launch_util.cuh"
+#include "tc_util.cuh"
 
 #include <cuda_bf16.h>
 
@@ -274,20 +275,23 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
 }
 
 // bf16, head_dim 128: one warp per (request, head), lane owns 4 elements; one pass over the
-// records with a running log-sum-exp, up to sixteen records' loads in flight at a time (a
-// typical row has a dozen records, so it is merged in one memory round trip).  Records are read
-// with streaming loads (they are not read again).
-constexpr int kMergeBatch = 16;
+// records with a running log-sum-exp, up to eight records' loads in flight at a time (a row of
+// the automatic split has five to nine records, so it is merged in one or two memory round
+// trips).  Records are read with streaming loads (they are not read again).  At most 64
+// registers per thread, so four CTAs fit on an SM next to nothing and one or two next to a
+// still-running decode CTA: with programmatic dependent launch the whole grid is resident
+// before the records are complete.
+constexpr int kMergeBatch = 8;
 
-__global__ void __launch_bounds__(256) merge_bf16_d128_kernel(AttnParams p) {
-  grid_dep_wait();  // the records are complete once the kernels before this one are
-  grid_dep_launch_dependents();
+__global__ void __launch_bounds__(256, 4) merge_bf16_d128_kernel(AttnParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // b * n_q + h
   if (row >= (int64_t)p.B * p.n_q) return;
   const int32_t b = (int32_t)(row / p.n_q);
   const int32_t h = (int32_t)(row % p.n_q);
-  const DevReq r = p.reqs[b];
+  const DevReq r = p.reqs[b];  // the plan: written before the kernels of the call
+  grid_dep_wait();             // the records are complete once the kernels before this one are
+  grid_dep_launch_dependents();
   const float* lse_rec = p.rec_lse + (int64_t)r.rec_base * p.n_q + h;
   const float4* orec = reinterpret_cast<const float4*>(p.rec_o + ((int64_t)r.rec_base * p.n_q + h) * 128) + lane;
   const int64_t lstride = p.n_q;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(256) merge_bf16_d128_kernel(AttnParams p) {
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, l[u]);
     if (mb == -INFINITY) continue;
-    const float a = exp2f((m - mb) * kLog2e);  // 0 while m is still -inf
+    const float a = ex2_approx((m - mb) * kLog2e);  // 0 while m is still -inf
     den *= a;
     acc.x *= a;
     acc.y *= a;
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(256) merge_bf16_d128_kernel(AttnParams p) {
     acc.w *= a;
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const float w = exp2f((l[u] - mb) * kLog2e);  // 0 for absent records
+      const float w = ex2_approx((l[u] - mb) * kLog2e);  // 0 for absent records
       den += w;
       acc.x += w * x[u].x;
       acc.y += w * x[u].y;
