@@ -87,7 +87,8 @@ enum : int {
   kBarPvDone = kBarPFull + kSBufs,          // [kSBufs] PV(i) done -> softmax
   kBarDrain = kBarPvDone + kSBufs,          // all MMAs done -> teardown
   kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter (64 arrivals)
-  kNumBars = kBarPair + 4
+  kBarQFull = kBarPair + 4,                 // Q tile loaded by TMA -> MMA
+  kNumBars = kBarQFull + 1
 };
 static_assert(8 * kNumBars + 16 <= kBarArea, "barrier area");
 
@@ -95,7 +96,7 @@ static_assert(8 * kNumBars + 16 <= kBarArea, "barrier area");
 // Prefix work item `item` (one CTA) on `smem_raw` (at least kSmemBytes), run by kThreads
 // threads.  tmk/tmv: the layer's K and V tensor maps, kernel parameters (__grid_constant__).
 __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item, const CUtensorMap* tmk,
-                                              const CUtensorMap* tmv, unsigned char* smem_raw) {
+                                              const CUtensorMap* tmv, const CUtensorMap* tmq, unsigned char* smem_raw) {
   // 1024-byte alignment for the 128-byte-swizzle atoms
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base = (raw_u + 1023u) & ~1023u;
@@ -119,6 +120,10 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   piece_range(gr, it.split, t0, t1);
   const int n_tiles = (t1 - t0 + kN - 1) / kN;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
+  // Q by TMA when the group's requests are consecutive in the batch: the row block is then a
+  // (64 dims, g heads, 128/g requests) box of q [B, n_q, 128]; otherwise the threads gather it
+  const bool q_tma = p.q_tma != 0 && gr.q_b0 >= 0;
+  const int32_t rbase = it.row_block * kM;
 
   // The K producer thread initialises the barriers and issues the first K and V tiles at once,
   // so their HBM latency overlaps the Q gather below; its loop later starts after them.
@@ -136,10 +141,11 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   if (warp == kWarpTmaK && lane == 0) {
     tma_prefetch_desc(tmk);
     tma_prefetch_desc(tmv);
+    if (q_tma) tma_prefetch_desc(tmq);
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1u;
       if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxThreads;
-      if (i >= kBarPair) count = 64u;
+      if (i >= kBarPair && i < kBarPair + 4) count = 64u;
       mbar_init(bar(i), count);
     }
     *abort_flag = slab_ok ? 0 : 1;
@@ -148,6 +154,12 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     fence_proxy_async_smem();
     grid_dep_wait();  // the slab may have been written by the work before this kernel
     if (slab_ok) {
+      if (q_tma) {
+        const int32_t z = gr.q_b0 + rbase / g;
+        mbar_arrive_expect_tx(bar(kBarQFull), kQBytes);
+        tma_load_3d(sQ, tmq, 0, j * g, z, bar(kBarQFull));
+        tma_load_3d(sQ + kM * 128, tmq, 64, j * g, z, bar(kBarQFull));
+      }
       for (int i = 0; i < k_pre; ++i) issue_tile(true, i);
       for (int i = 0; i < v_pre; ++i) issue_tile(false, i);
     }
@@ -160,9 +172,9 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   grid_dep_wait();
   grid_dep_launch_dependents();
   // Q rows of this block -> shared memory, K-major with 128-byte swizzle: row r, 16-byte
-  // chunk c lives in 64-dim block c/8 at r*128 + ((c%8) ^ (r%8))*16; rows past the group are 0
-  const int32_t rbase = it.row_block * kM;
-  for (int idx = tid; idx < kM * 16; idx += kThreads) {
+  // chunk c lives in 64-dim block c/8 at r*128 + ((c%8) ^ (r%8))*16 (the layout the TMA box
+  // load produces); rows past the group are 0
+  for (int idx = q_tma ? kM * 16 : tid; idx < kM * 16; idx += kThreads) {
     const int r = idx >> 4;
     const int c = idx & 15;
     const int32_t row = rbase + r;
@@ -199,7 +211,16 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         issue_tile(is_k, i);
         issued = i + 1;
       }
-      // never leave with a copy in flight: wait for every issued tile to land
+      // never leave with a copy in flight: wait for every issued tile (and Q) to land
+      if (is_k && q_tma && slab_ok) {
+        const uint64_t t_start = globaltimer_ns();
+        while (!mbar_try_wait(bar(kBarQFull), 0)) {
+          if (globaltimer_ns() - t_start > kWaitLimitNs) {
+            atomicCAS(p.err, 0, kDevTimeout);
+            break;
+          }
+        }
+      }
       for (int i = max(0, issued - slots); i < issued; ++i) {
         const int st = i % slots;
         const uint64_t t_start = globaltimer_ns();
@@ -230,6 +251,9 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       // in order; the softmax finished with S(j-3) before it produced P(j-3)).  Polling both
       // conditions keeps the issuing thread from sitting on one while the other is ready.
       int next_s = 0, next_pv = 0;
+      if (q_tma && !mbar_wait_bounded(bar(kBarQFull), 0, abort_flag, p.err, kDevTimeout, kWaitLimitNs))
+        next_pv = n_tiles;  // gave up (abort raised): issue nothing
+      tc_fence_after();
       uint64_t t_last = globaltimer_ns();
       while (next_pv < n_tiles) {
         bool progressed = false;

@@ -162,6 +162,21 @@ bool encode_pool_map(CUtensorMap* m, void* base, int64_t n_slots, int32_t n_kv) 
   return r == CUDA_SUCCESS;
 }
 
+// q [B, n_q, 128] bf16 as a 3-D tensor (dim, head, request) with (64, g, 128/g) boxes: one box
+// is a dense row block's q rows of one 64-dim half, in the layout the operand descriptors expect.
+bool encode_q_map(CUtensorMap* m, const void* q, int32_t B, int32_t n_q, int32_t g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || ((uintptr_t)q % 16) != 0 || g < 1 || kDenseRows % g != 0) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)n_q, (cuuint64_t)B};
+  cuuint64_t strides[2] = {256, (cuuint64_t)n_q * 256};
+  cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(kDenseRows / g)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int32_t rows_per_cta_for(int32_t impl) {
   switch (impl) {
     case kImplDenseTc: return kDenseRows;
@@ -630,7 +645,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       dg.tile = (int32_t)tile;
       dg.split_len = (int32_t)(base * tile);
       dg.n_long = (int32_t)(t - base * n_splits);
-      dg.pad[0] = dg.pad[1] = dg.pad[2] = 0;
+      dg.q_b0 = -1;
+      dg.pad[0] = dg.pad[1] = 0;
     }
     // the tensor-core prefix kernels hold one SM per CTA; the suffix gets every other SM (an
     // automatic split that found no piece length leaving the suffix an SM shares them all)
@@ -674,6 +690,15 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     std::vector<int32_t> fill(begin.begin(), begin.end() - 1);
     for (int32_t b = 0; b < B; ++b)
       if (req_group[b] >= 0) group_req[fill[req_group[b]]++] = b;
+  }
+  // dense groups whose requests are consecutive in the batch load their q rows by TMA boxes
+  for (int32_t i = 0; i < G; ++i) {
+    DevGroup& dg = groups[i];
+    if (dg.impl != kImplDenseTc || kDenseRows % g != 0) continue;
+    bool contiguous = true;
+    for (int32_t k = 1; k < dg.n_req && contiguous; ++k)
+      contiguous = group_req[dg.req_begin + k] == group_req[dg.req_begin] + k;
+    if (contiguous && dg.n_req > 0) dg.q_b0 = group_req[dg.req_begin];
   }
   std::vector<DevReq> reqs(B);
   std::vector<DevSuffixItem> sitems;
@@ -926,6 +951,10 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.checks = c->checks;
   a.tickets = tickets;
   a.fused_merge = p->fused ? 1 : 0;
+  CUtensorMap tmq{};
+  a.q_tma = 0;
+  if (p->pitem_count[kImplDenseTc] > 0 && c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128)
+    a.q_tma = encode_q_map(&tmq, q, bt->B, c->cfg.n_q, c->g) ? 1 : 0;
   c->last_tickets = tickets;
   c->last_tickets_bytes = tickets_bytes;
 
@@ -952,7 +981,7 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
       if (!c->has_tmaps) return cudaErrorNotSupported;
       const bool first = p->pitem_count[kImplGeneric] == 0 && p->pitem_count[kImplCascadeMma] == 0;
       r = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
-                          c->tmap_v[layer], st, first);
+                          c->tmap_v[layer], tmq, st, first);
       c->n_kernels += 1;
     }
     return r;
@@ -964,7 +993,7 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     // the dense prefix items and the suffix token-CTAs side by side in one grid, then the
     // merge: both chained to their stream predecessor by programmatic dependent launch
     e = launch_prefix_suffix_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
-                                c->tmap_v[layer], a.scta_begin, p->n_scta, s, true);
+                                c->tmap_v[layer], tmq, a.scta_begin, p->n_scta, s, true);
     c->n_kernels += 1;
     if (e == cudaSuccess && !p->fused) {
       e = launch_merge(c->cfg.dtype, a, s, true);

@@ -53,7 +53,8 @@ struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int32_t row_blocks;    // ceil(n_req * g / rows_per_cta)
   int32_t n_long;        // the first n_long pieces are one tile longer than split_len
   int32_t tile;          // token granularity of the pieces
-  int32_t pad[3];
+  int32_t q_b0;          // dense: the group's requests are q_b0, q_b0+1, ... (q rows by TMA), else -1
+  int32_t pad[2];
 };
 static_assert(sizeof(DevGroup) == 64, "DevGroup layout");
 
@@ -108,6 +109,7 @@ struct AttnParams {
   int32_t checks;
   int32_t* tickets;       // [B, n_q] arrivals per row (fused merge), zero between calls
   int32_t fused_merge;    // 1: the last producer of a row merges it (no merge kernel)
+  int32_t q_tma;          // 1: the q tensor map passed to the dense kernel is valid
 };
 
 // ---- launchers (kernels_*.cu) ------------------------------------------------------------
@@ -133,12 +135,12 @@ cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int
                               bool pdl);
 cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
-                            const CUtensorMap& tmv, cudaStream_t s, bool pdl);
+                            const CUtensorMap& tmv, const CUtensorMap& tmq, cudaStream_t s, bool pdl);
 // One launch for both: CTAs [0, n_dense) run dense prefix items first_item.., the rest the
 // suffix token-CTAs (n_scta per KV-head group of eight).
 cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_item, int32_t n_dense, const CUtensorMap& tmk,
-                                    const CUtensorMap& tmv, const int32_t* cta_begin, int32_t n_scta, cudaStream_t s,
-                                    bool pdl);
+                                    const CUtensorMap& tmv, const CUtensorMap& tmq, const int32_t* cta_begin,
+                                    int32_t n_scta, cudaStream_t s, bool pdl);
 
 constexpr int kNumImpl = 4;
 
