@@ -35,7 +35,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn query-tokens/s at L_p=16K on 1 GB300; % HBM / tensor roofline"
 UNIT = "q-tok/s"
-WORKLOAD = "llama8b_single_prefix_16k"
+WORKLOAD = "llama8b_single_prefix_16k"  # the headline configuration
+# Other full-size configurations the bench can run (``--workload``); the headline line is the
+# default one.
+WORKLOADS = {  # name -> suffix description
+    "llama8b_single_prefix_16k": (None, "log-normal median 300, sigma 1, clipped [32, 2048]"),
+    "hetero_multi_prefix_k8": (None, "8 prefixes L_p ~ U[2048, 16384], 8-32 requests each, log-normal suffixes"),
+    "qwen_tp1_16k": (None, "suffix U[64, 1024]"),
+}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -54,6 +61,8 @@ def parse_args(argv=None):
                     help="share of the SMs the prefix work list is sized for when running concurrently "
                          "(0: the library's automatic share)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=WORKLOAD,
+                    help="full-size configuration to time (default: the headline one)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="rough bound on the CPU-baseline sample's run time")
     return ap.parse_args(argv)
@@ -86,6 +95,13 @@ def barrier(world: int):
 
 
 # ---- accounting -----------------------------------------------------------------------------
+
+def workload_fn(name):
+    import workloads as W
+    return {"llama8b_single_prefix_16k": W.llama8b_single_prefix_16k,
+            "hetero_multi_prefix_k8": W.hetero_multi_prefix_k8,
+            "qwen_tp1_16k": W.qwen_tp1_16k}[name]
+
 
 def algorithmic_bytes(spec, slab_ids, seq_lens, esize: int) -> int:
     """Bytes one decode-attention call must move at minimum: each HOT prefix's K and V once,
@@ -254,7 +270,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import workloads as W
-    wl = W.llama8b_single_prefix_16k(seed=0)
+    wl = workload_fn(args.workload)(seed=0)
     per_step = 2
     B = wl.spec.B
     for i in range(args.warmup):
@@ -268,7 +284,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1000.0 * t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": WORKLOAD, "n_q": 32, "n_kv": 8, "head_dim": 128, "L_p": 16384,
+            "config": {"workload": args.workload, "n_q": wl.spec.n_q, "n_kv": wl.spec.n_kv,
+                       "head_dim": wl.spec.d, "L_p": wl.spec.prefix_lens[0],
                        "B": B, "sample_per_step": f"{per_step} requests, one layer"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                              "sample": f"{per_step} requests per step of {wl.spec.name}, one layer"},
@@ -301,7 +318,7 @@ def run_granikv(args):
     L = args.layers
     steps_total = args.warmup + args.steps
     e2e_steps = max(3, min(args.steps, 10))
-    wl = W.llama8b_single_prefix_16k(seed=rank)
+    wl = workload_fn(args.workload)(seed=rank)
     spec = wl.spec
     B = spec.B
     extra = steps_total + e2e_steps + 8
@@ -436,7 +453,7 @@ def run_granikv(args):
     achieved = avg_bytes / avg_call_s / 1e9
     groups = plan.groups()
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": profiled_traffic("decode_attention_" + WORKLOAD),
+                "frac": achieved / hbm, "traffic": profiled_traffic("decode_attention_" + args.workload),
                 "kernel": "granikv_decode_attention launches (prefix + suffix + merge)",
                 "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": avg_bytes,
@@ -446,9 +463,9 @@ def run_granikv(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n_q": spec.n_q, "n_kv": spec.n_kv, "head_dim": spec.d,
-                   "L_p": spec.prefix_lens[0], "B": B,
-                   "suffix": "log-normal median 300, sigma 1, clipped [32, 2048]",
+        "config": {"workload": args.workload, "n_q": spec.n_q, "n_kv": spec.n_kv, "head_dim": spec.d,
+                   "L_p": spec.prefix_lens[0] if len(spec.prefix_lens) == 1 else list(spec.prefix_lens), "B": B,
+                   "suffix": WORKLOADS[args.workload][1],
                    "layers_per_step": L, "backend": args.backend,
                    "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],

@@ -571,7 +571,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   bool fast_all = fast_suffix_pre || T_all == 0;
   for (int32_t i = 0; i < G; ++i)
     if (groups[i].impl == kImplGeneric) fast_all = false;
-  const bool concurrent = fast_all && c->concurrent && G > 0 && T_all > 0;
+  bool concurrent = fast_all && c->concurrent && G > 0 && T_all > 0;
   const bool split_sms = concurrent && c->prefix_share < 0.999f;
   const bool auto_share = split_sms && c->prefix_share <= 0.f;
   const int32_t prefix_sms =
@@ -612,27 +612,46 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       // i.e. the smallest max of the two.  Costs measured on GB300: a prefix CTA 5 us plus, per
       // 128-query-row block and token, 0.01 us (dense) or 0.02 us (cascade); the suffix 1.40
       // SM-us per 16 COLD tokens of one group of up to 8 KV heads.
-      double w_s = 0.0;
+      // The split is also weighed against running the two one after another on all SMs, with
+      // the suffix then bound by the bandwidth HBM gives its random 2 KB row reads (about
+      // 5.8 TB/s measured), and the step's bytes bounding either way at about 5.9 TB/s.
+      double w_s = 0.0, suffix_bytes = 0.0, prefix_bytes = 0.0;
       const int64_t head_groups = (n_kv + 7) / 8;
-      for (int32_t b = 0; b < B; ++b) w_s += 1.40 * (double)head_groups * (double)((bt->seq_len[b] + 15) / 16);
-      double best = 1e300;
-      for (int64_t n = 1; n <= max_tiles; ++n) {
-        const int64_t cand = (max_tiles + n - 1) / n;
-        if (n > 1 && cand == (max_tiles + n - 2) / (n - 1)) continue;  // same length as n - 1
-        const int64_t ctas = ctas_for(cand);
-        if (ctas >= c->num_sms) break;  // one wave, and at least one SM for the suffix
+      for (int32_t b = 0; b < B; ++b) {
+        w_s += 1.40 * (double)head_groups * (double)((bt->seq_len[b] + 15) / 16);
+        suffix_bytes += 4.0 * n_kv * c->cfg.head_dim * (double)bt->seq_len[b];
+      }
+      for (int32_t i = 0; i < G; ++i) prefix_bytes += 4.0 * n_kv * c->cfg.head_dim * (double)groups[i].L_p;
+      auto prefix_time = [&](int64_t cand) {
         double t_p = 0.0;
         for (int32_t i = 0; i < G; ++i) {
           const int64_t tile = tile_tokens_for(groups[i].impl);
           const double per_token = groups[i].impl == kImplDenseTc ? 0.01 : 0.02;
           t_p = std::max(t_p, 5.0 + per_token * (double)std::min<int64_t>(cand * tile, groups[i].L_p));
         }
-        const double t = std::max(t_p, w_s / (double)(c->num_sms - ctas));
+        return t_p;
+      };
+      const double t_bytes = (prefix_bytes + suffix_bytes) / 5.9e6;  // us at 5.9 TB/s
+      double best = 1e300;
+      const int64_t lo_serial = lo;
+      for (int64_t n = 1; n <= max_tiles; ++n) {
+        const int64_t cand = (max_tiles + n - 1) / n;
+        if (n > 1 && cand == (max_tiles + n - 2) / (n - 1)) continue;  // same length as n - 1
+        const int64_t ctas = ctas_for(cand);
+        if (ctas >= c->num_sms) break;  // one wave, and at least one SM for the suffix
+        const double t = std::max({prefix_time(cand), w_s / (double)(c->num_sms - ctas), t_bytes});
         if (t < best) {
           best = t;
           lo = cand;
           auto_found = true;
         }
+      }
+      const double t_serial =
+          prefix_time(lo_serial) + std::max(w_s / (double)c->num_sms, suffix_bytes / 5.8e6);
+      if (auto_found && t_serial < best) {
+        lo = lo_serial;
+        auto_found = false;
+        concurrent = false;
       }
     }
     for (int32_t i = 0; i < G; ++i) {
