@@ -340,21 +340,30 @@ def run_granikv(args):
     # A step's inputs (q, new K, new V of every layer) live in one device buffer and its outputs
     # (o, lse of every layer) in another, so the end-to-end run moves each direction with one
     # copy per step; the per-layer tensors are views into them.
+    # Two such buffer sets: the end-to-end leg copies step k+1's inputs in (and step k's outputs
+    # out) on a copy stream while step k computes.
     n_qe, n_kve = B * spec.n_q * spec.d, B * spec.n_kv * spec.d
-    in_dev = torch.empty((L, n_qe + 2 * n_kve), dtype=torch.bfloat16, device=dev)
-    qs = [in_dev[layer, :n_qe].view(B, spec.n_q, spec.d) for layer in range(L)]
-    knew = [in_dev[layer, n_qe:n_qe + n_kve].view(B, spec.n_kv, spec.d) for layer in range(L)]
-    vnew = [in_dev[layer, n_qe + n_kve:].view(B, spec.n_kv, spec.d) for layer in range(L)]
+    o_bytes, l_bytes = B * spec.n_q * spec.d * 2, B * spec.n_q * 4
+
+    def buffer_set():
+        in_dev = torch.empty((L, n_qe + 2 * n_kve), dtype=torch.bfloat16, device=dev)
+        out_dev = torch.empty((L, o_bytes + l_bytes), dtype=torch.uint8, device=dev)
+        return {"in": in_dev, "out": out_dev,
+                "q": [in_dev[layer, :n_qe].view(B, spec.n_q, spec.d) for layer in range(L)],
+                "k": [in_dev[layer, n_qe:n_qe + n_kve].view(B, spec.n_kv, spec.d) for layer in range(L)],
+                "v": [in_dev[layer, n_qe + n_kve:].view(B, spec.n_kv, spec.d) for layer in range(L)],
+                "o": [out_dev[layer, :o_bytes].view(torch.bfloat16).view(B, spec.n_q, spec.d) for layer in range(L)],
+                "lse": [out_dev[layer, o_bytes:].view(torch.float32).view(B, spec.n_q) for layer in range(L)]}
+
+    bufs = [buffer_set(), buffer_set()]
+    qs, knew, vnew = bufs[0]["q"], bufs[0]["k"], bufs[0]["v"]
     qs[0].copy_(lw.q)
     for layer in range(1, L):
         qs[layer].copy_((torch.randn((B, spec.n_q, spec.d), generator=gen, device=dev) / math.sqrt(spec.d)))
     for layer in range(L):
         knew[layer].copy_(torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev))
         vnew[layer].copy_(torch.randn((B, spec.n_kv, spec.d), generator=gen, device=dev))
-    o_bytes, l_bytes = B * spec.n_q * spec.d * 2, B * spec.n_q * 4
-    out_dev = torch.empty((L, o_bytes + l_bytes), dtype=torch.uint8, device=dev)
-    outs = [out_dev[layer, :o_bytes].view(torch.bfloat16).view(B, spec.n_q, spec.d) for layer in range(L)]
-    lses = [out_dev[layer, o_bytes:].view(torch.float32).view(B, spec.n_q) for layer in range(L)]
+    bufs[1]["in"].copy_(bufs[0]["in"])
     slots = torch.empty((B,), dtype=torch.int32, device=dev)
     plan = ctx.plan()
     slab_ids = lw.slab_ids
@@ -367,12 +376,13 @@ def run_granikv(args):
     ev_pairs = []
     timed_bytes = []
 
-    def step(record):
+    def step(record, bs=0):
+        bset = bufs[bs]
         ctx.cold_alloc(ones, cache.req_to_slot, cache.suffix_len, cache.cap, slots, stream)
         for i in range(B):
             seq[i] += 1
         for layer in range(L):
-            ctx.cold_append(layer, knew[layer], vnew[layer], slots, B, stream)
+            ctx.cold_append(layer, bset["k"][layer], bset["v"][layer], slots, B, stream)
         batch = gb.Batch(slab_ids, seq, cache.req_to_slot, cache.cap)
         ctx.dispatch(batch, plan)
         nbytes = algorithmic_bytes(spec, slab_ids, seq, 2)
@@ -383,7 +393,8 @@ def run_granikv(args):
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         for layer in range(L):
-            ctx.decode_attention(layer, qs[layer], batch, plan, outs[layer], lses[layer], ws, ws_bytes, stream)
+            ctx.decode_attention(layer, bset["q"][layer], batch, plan, bset["o"][layer], bset["lse"][layer], ws,
+                                 ws_bytes, stream)
         if record:
             e1.record(stream)
             ev_pairs.append((e0, e1))
@@ -418,25 +429,44 @@ def run_granikv(args):
     avg_call_s = statistics.mean(call_ms) / 1000.0
     avg_bytes = statistics.mean(timed_bytes)
 
-    # end to end through the C ABI with host buffers: pinned host inputs copied in and the
-    # step's outputs read back inside the timed region, every step
-    in_host = in_dev.cpu().pin_memory()
-    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    # end to end through the C ABI with host buffers: every step's inputs are copied in from
+    # pinned host memory and its outputs read back inside the timed region; the copies run on a
+    # copy stream, step k+1's inputs and step k's outputs while step k computes (two buffer sets)
+    in_host = bufs[0]["in"].cpu().pin_memory()
+    out_host = torch.empty(bufs[0]["out"].shape, dtype=bufs[0]["out"].dtype).pin_memory()
     h2d = in_host.numel() * in_host.element_size()
     d2h = out_host.numel() * out_host.element_size()
-
-    def e2e_step():
-        in_dev.copy_(in_host, non_blocking=True)
-        step(False)
-        out_host.copy_(out_dev, non_blocking=True)
+    copy_stream = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_out = [torch.cuda.Event(), torch.cuda.Event()]
 
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    copy_stream.wait_event(e0)
+    with torch.cuda.stream(copy_stream):
+        bufs[0]["in"].copy_(in_host, non_blocking=True)
+    ev_in[0].record(copy_stream)
+    for k in range(e2e_steps):
+        bs = k % 2
+        stream.wait_event(ev_in[bs])
+        if k >= 2:
+            stream.wait_event(ev_out[bs])  # step k-2's outputs have left this set
+        step(False, bs)
+        ev_done[bs].record(stream)
+        with torch.cuda.stream(copy_stream):
+            if k + 1 < e2e_steps:
+                if k >= 1:
+                    copy_stream.wait_event(ev_done[1 - bs])  # step k-1 finished with that set
+                bufs[1 - bs]["in"].copy_(in_host, non_blocking=True)
+                ev_in[1 - bs].record(copy_stream)
+            copy_stream.wait_event(ev_done[bs])
+            out_host.copy_(bufs[bs]["out"], non_blocking=True)
+            ev_out[bs].record(copy_stream)
+    stream.wait_stream(copy_stream)
     e1.record(stream)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1000.0, world, dev)
