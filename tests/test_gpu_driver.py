@@ -1,0 +1,44 @@
+"""Multi-step decode with arrivals and completions between steps ("3 GraniKV": the dispatcher
+decides per realized batch; "B.4 Per-Step Dispatch Trace"): after several steps of churn the
+library's attention for every active request equals the oracle's, computed from the host copies
+of the request's logical K/V (its prefix, prompt and decoded tokens), not from the pools."""
+
+import numpy as np
+import pytest
+
+from oracle import attention as OA
+
+pytestmark = pytest.mark.gpu
+
+
+def test_driver_churn_matches_oracle(cuda_ok):
+    from shared_prefix_kv_decode_gb300.decode_driver import DecodeDriver
+
+    n_q, n_kv, d = 32, 8, 128
+    drv = DecodeDriver(prefix_lens=[700, 1500], n_layers=1, n_q=n_q, n_kv=n_kv, head_dim=d, max_batch=64,
+                       cap=512, n_slots=40000, seed=3, keep_logical=True)
+    sched = np.random.default_rng(7)
+    for i in range(20):
+        drv.arrive(i % 2, int(sched.integers(1, 200)))
+    for step in range(12):
+        for b in sorted([b for b in range(drv.B) if sched.random() < 0.1], reverse=True):
+            drv.complete(b)
+        for _ in range(int(sched.integers(0, 3))):
+            drv.arrive(int(sched.integers(2)), int(sched.integers(1, 200)))
+        drv.step()
+    trace = drv.finish_trace()
+    assert len(trace) == 12 and all(t["B"] > 0 and 1 <= len(t["groups"]) <= 2 for t in trace)
+    assert all(t["gpu_us"] > 0 and t["dispatch_us"] > 0 for t in trace)
+    o, lse = drv.last_out
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    q = drv.last_q[0]
+    scale = OA.softmax_scale(d)
+    for b in range(drv.B):
+        K, V = drv.logical_kv(b, 0)
+        for h in range(n_q):
+            j = OA.kv_head(h, n_q, n_kv)
+            o_ref, lse_ref = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
+                                       V[:, j].astype(np.float64), scale)
+            assert np.max(np.abs(o[b, h] - o_ref)) <= 1e-2, (b, h)
+            assert abs(lse[b, h] - lse_ref) <= 1e-3, (b, h)
