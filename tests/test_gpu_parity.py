@@ -312,3 +312,32 @@ def test_hot_layout_equals_paged_equivalent_layout(cuda_ok, backend):
     assert_close(o_h.float().cpu().numpy().astype(np.float64), l_h.cpu().numpy().astype(np.float64),
                  o_p.float().cpu().numpy().astype(np.float64), l_p.cpu().numpy().astype(np.float64),
                  "bf16", f"hot vs paged {backend}")
+
+
+@pytest.mark.parametrize("shape", [(32, 16), (8, 8), (64, 8), (16, 2)])
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_head_shapes(cuda_ok, shape, backend):
+    """GQA shapes besides the configurations': more than eight KV heads (two head groups in the
+    suffix kernel), one query head per KV head (g = 1), g = 8, and two KV heads; bf16, d = 128,
+    the small mixed batch (ragged prefixes, a prefix-only and a prefix-less request)."""
+    n_q, n_kv = shape
+    wl = W.small_mixed(4, dtype="bf16", n_q=n_q, n_kv=n_kv, q_scale=1.0)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"heads {shape} {backend}")
+
+
+@pytest.mark.parametrize("backend", BACKENDS)
+@pytest.mark.parametrize("lens", [(100, 5), (128, 0), (1, 1), (129, 16)])
+def test_single_request(cuda_ok, backend, lens):
+    """B = 1: a prefix shorter than, equal to and one token past a 128-token tile, with a short
+    or empty suffix (and a one-token prefix with a one-token suffix)."""
+    L_p, L_s = lens
+    spec = W.WorkloadSpec(name="single", dtype="bf16", n_q=32, n_kv=8, d=128, prefix_lens=[L_p],
+                          req_prefix=[0], suffix_lens=[L_s], q_scale=1.0, n_slots=4096)
+    wl = W.Workload(spec, 11)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"single {lens} {backend}")
