@@ -240,6 +240,13 @@ granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int32_t layer, 
  * GRANIKV_ERR_DEVICE_CHECK (no trap, no assert).  Default 1 for alloc/append, which are cheap;
  * the attention kernels check when on. */
 granikv_status granikv_set_checks(granikv_ctx* ctx, int32_t on);
+/* Test hook for the failure path (no counterpart in the paper): when on, the next
+ * granikv_decode_attention call's first suffix token-CTA withholds the copies of its first
+ * tile, so that CTA's consumers' bounded wait (2 s) expires.  The CTA then raises its abort
+ * flag, waits for the copies it did issue, and exits; the call latches
+ * GRANIKV_ERR_DEVICE_CHECK (reported by granikv_sync_status), and the context stays usable for
+ * the next call.  Applies to one call of the bf16 tensor-core suffix path; 0 cancels it. */
+granikv_status granikv_inject_stall(granikv_ctx* ctx, int32_t on);
 /* Synchronise the stream and report (and clear) the device error word. */
 granikv_status granikv_sync_status(granikv_ctx* ctx, granikv_stream_t stream);
 /* Kernels (and host-to-device plan or offset copies) this context has enqueued since it was

@@ -111,6 +111,7 @@ _SIGNATURES = [
     ("granikv_decode_attention_static", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
                                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("granikv_set_checks", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_inject_stall", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_sync_status", C.c_int32, [C.c_void_p, C.c_void_p]),
     ("granikv_launch_count", C.c_int32, [C.c_void_p, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
 ]
@@ -347,6 +348,11 @@ class Context:
     # checks
     def set_checks(self, on: bool):
         _check(self._lib.granikv_set_checks(self.handle, 1 if on else 0), "granikv_set_checks")
+
+    def inject_stall(self, on: bool = True):
+        """Test hook: the next decode call's first suffix token-CTA withholds its first tile (see
+        granikv_inject_stall in include/granikv.h)."""
+        _check(self._lib.granikv_inject_stall(self.handle, 1 if on else 0), "granikv_inject_stall")
 
     def sync_status(self, stream=None):
         _check(self._lib.granikv_sync_status(self.handle, _stream(stream)), "granikv_sync_status")

@@ -68,6 +68,7 @@ struct granikv_ctx {
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int32_t concurrent = 1;
   float prefix_share = 0.0f;  // 0: automatic
+  int32_t inject_stall = 0;   // test hook for the next decode call
   int32_t fused_merge = 0;  // merge by the last producer instead of a merge kernel
   // tickets of the last call (zeroed again after a device check failure)
   void* last_tickets = nullptr;
@@ -970,6 +971,8 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.checks = c->checks;
   a.tickets = tickets;
   a.fused_merge = p->fused ? 1 : 0;
+  a.inject_stall = c->inject_stall;
+  c->inject_stall = 0;
   CUtensorMap tmq{};
   a.q_tma = 0;
   if (p->pitem_count[kImplDenseTc] > 0 && c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128)
@@ -1051,6 +1054,12 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
 granikv_status granikv_set_checks(granikv_ctx* c, int32_t on) {
   if (!c) return GRANIKV_ERR_INVALID;
   c->checks = on ? 1 : 0;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_inject_stall(granikv_ctx* c, int32_t on) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  c->inject_stall = on ? 1 : 0;
   return GRANIKV_OK;
 }
 

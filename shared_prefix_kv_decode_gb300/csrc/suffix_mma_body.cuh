@@ -133,6 +133,8 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     int n = 0;      // tiles issued
     int pos = 0;    // position of the current segment's first token in sslot
     bool stop = false;
+    // test hook: token-CTA 0 of group 0 withholds its first tile
+    const bool skip0 = p.inject_stall != 0 && cta == 0 && group == 0;
     for (int sg = 0; sg < n_seg && !stop; ++sg) {
       const DevSuffixItem seg = segs[sg];
       for (int t = seg.t0; t < seg.t1; t += kTile, ++n) {
@@ -152,6 +154,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
           else
             latch_err(p.err, kDevBadSlot);
         }
+        if (skip0 && n == 0) continue;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(st), 2u * kTile * gbytes);
         __syncwarp();
         const uint32_t dst = sbase + st * kStageBytes + (is_v ? kTileBytes : 0) + r * kRowStride;
@@ -161,7 +164,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     }
     // never leave with a copy in flight: wait for the last issued tiles to land
     if (lane == 0) {
-      for (int i = max(0, n - kStages); i < n; ++i) {
+      for (int i = max(skip0 ? 1 : 0, n - kStages); i < n; ++i) {
         const uint64_t t_start = globaltimer_ns();
         while (!mbar_try_wait(full_bar(i % kStages), (i / kStages) & 1)) {
           if (globaltimer_ns() - t_start > kWaitLimitNs) {
