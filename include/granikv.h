@@ -163,6 +163,59 @@ granikv_status granikv_cold_append(granikv_ctx* ctx, int32_t layer, const void* 
                                    const void* v_new, const int32_t* slots, int32_t N,
                                    granikv_stream_t stream);
 
+/* ---- prefix index ("2 Related Work", prefix-aware serving: a radix tree over token-id
+ * sequences with reference-counted nodes; card page: one HOT slab per radix-tree prefix node;
+ * "B.10 Cross-pool admission and promotion policy": HOT first, COLD fallback, no demotion).
+ * Host only, no device access; the HOT slabs come from the context's HOT pool.
+ *
+ * A prefix is used whole: a request reuses the deepest admitted prefix whose full token
+ * sequence starts its own, and attends over all of it (L_p = its length).  Nested prefixes each
+ * own a slab of their full length.  Prefix handles are never reused.  The LRU clock advances
+ * on insert, on a match that takes a reference, on acquire and on release. -------------- */
+
+typedef struct granikv_index granikv_index;
+
+typedef struct granikv_prefix_info {
+  int32_t prefix_id;   /* handle (>= 0), or -1 when a match found nothing                */
+  int32_t length;      /* L_p, tokens                                                     */
+  int32_t slab_id;     /* HOT slab, or -1 when the prefix was placed in COLD              */
+  int32_t refcount;    /* requests holding the prefix                                     */
+  int64_t slot_offset; /* first HOT slot of the slab, or -1                               */
+} granikv_prefix_info;
+
+/* An empty index over ctx's HOT pool.  ctx must outlive the index.  Destroying the index
+ * returns the slabs of its HOT prefixes to the pool (a COLD prefix's slots are the caller's). */
+granikv_status granikv_index_create(granikv_ctx* ctx, granikv_index** out);
+granikv_status granikv_index_destroy(granikv_index* idx);
+/* Deepest admitted prefix of tokens (host [n]); out->prefix_id = -1 when none.  acquire = 1
+ * takes a reference on the prefix found. */
+granikv_status granikv_index_match(granikv_index* idx, const int32_t* tokens, int32_t n,
+                                   int32_t acquire, granikv_prefix_info* out);
+/* Admit tokens (host [n], n >= 1) as a prefix with refcount 0.  If exactly this sequence is
+ * already admitted, that prefix is returned and nothing else changes.  Otherwise HOT first: a
+ * first-fit slab of n slots.  If none is free, unreferenced HOT prefixes are evicted, least
+ * recently used first, until the slab fits -- but only if evicting all of them would make it
+ * fit; else nothing is evicted and the prefix is placed in COLD (slab_id = -1: the caller
+ * stores its K/V in COLD slots).  Referenced prefixes never move or leave HOT.
+ *   evicted: host [max_evicted] or NULL; receives the handles evicted, n_evicted their number
+ *            (may be NULL).  GRANIKV_ERR_INVALID, with nothing changed, if evicted is given and
+ *            more than max_evicted would go. */
+granikv_status granikv_index_insert(granikv_index* idx, const int32_t* tokens, int32_t n,
+                                    granikv_prefix_info* out, int32_t* evicted,
+                                    int32_t max_evicted, int32_t* n_evicted);
+/* Take or drop one reference.  GRANIKV_ERR_INVALID for an unknown handle, or a release of a
+ * prefix nobody holds. */
+granikv_status granikv_index_acquire(granikv_index* idx, int32_t prefix_id);
+granikv_status granikv_index_release(granikv_index* idx, int32_t prefix_id);
+/* Remove an unreferenced prefix; a HOT one's slab returns to the pool.  GRANIKV_ERR_INVALID for
+ * an unknown or referenced handle. */
+granikv_status granikv_index_remove(granikv_index* idx, int32_t prefix_id);
+granikv_status granikv_index_info(granikv_index* idx, int32_t prefix_id, granikv_prefix_info* out);
+/* Live prefixes, how many of them are in HOT, and tree nodes (root not counted: a node marks
+ * where an admitted prefix ends or where two of them diverge). */
+granikv_status granikv_index_stats(granikv_index* idx, int32_t* n_prefixes, int32_t* n_hot,
+                                   int32_t* n_nodes);
+
 /* ---- per-step dispatch ("3 GraniKV", per-step dispatch; "B.4 Per-Step Dispatch Trace";
  * "B.8": class-local dense batching).  Host only, no device access. ------------------------ */
 

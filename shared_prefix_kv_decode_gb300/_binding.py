@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes as C
 import os
+import weakref
 from typing import Optional, Sequence
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -75,6 +76,14 @@ class GroupInfo(C.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class PrefixInfo(C.Structure):
+    _fields_ = [("prefix_id", C.c_int32), ("length", C.c_int32), ("slab_id", C.c_int32),
+                ("refcount", C.c_int32), ("slot_offset", C.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
 _lib = None
 
 # (name, restype, argtypes) of every exported symbol
@@ -94,6 +103,18 @@ _SIGNATURES = [
     ("granikv_cold_free_count", C.c_int32, [C.c_void_p, C.POINTER(C.c_int64)]),
     ("granikv_cold_append", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_int32, C.c_void_p]),
+    ("granikv_index_create", C.c_int32, [C.c_void_p, C.POINTER(C.c_void_p)]),
+    ("granikv_index_destroy", C.c_int32, [C.c_void_p]),
+    ("granikv_index_match", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32), C.c_int32, C.c_int32,
+                                        C.POINTER(PrefixInfo)]),
+    ("granikv_index_insert", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32), C.c_int32, C.POINTER(PrefixInfo),
+                                         C.POINTER(C.c_int32), C.c_int32, C.POINTER(C.c_int32)]),
+    ("granikv_index_acquire", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_index_release", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_index_remove", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_index_info", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(PrefixInfo)]),
+    ("granikv_index_stats", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32),
+                                        C.POINTER(C.c_int32)]),
     ("granikv_plan_create", C.c_int32, [C.c_void_p, C.POINTER(C.c_void_p)]),
     ("granikv_plan_destroy", C.c_int32, [C.c_void_p]),
     ("granikv_dispatch", C.c_int32, [C.c_void_p, C.POINTER(_Batch), C.c_void_p]),
@@ -224,6 +245,74 @@ class Plan:
             pass
 
 
+class Index:
+    """A prefix index (granikv_index) over a context's HOT pool.  Methods follow the C entry
+    points' names; prefixes are given as sequences of token ids."""
+
+    def __init__(self, ctx: "Context"):
+        self._ctx = ctx
+        self._lib = ctx._lib
+        h = C.c_void_p()
+        _check(self._lib.granikv_index_create(ctx.handle, C.byref(h)), "granikv_index_create")
+        self.handle = h
+        ctx._indexes.append(weakref.ref(self))
+
+    @staticmethod
+    def _tokens(tokens: Sequence[int]):
+        arr = _i32_array(tokens) if len(tokens) else (C.c_int32 * 1)()
+        return arr, C.cast(arr, C.POINTER(C.c_int32)), len(tokens)
+
+    def match(self, tokens: Sequence[int], acquire: bool = False) -> dict:
+        arr, ptr, n = self._tokens(tokens)
+        out = PrefixInfo()
+        _check(self._lib.granikv_index_match(self.handle, ptr, n, 1 if acquire else 0, C.byref(out)),
+               "granikv_index_match")
+        return out.as_dict()
+
+    def insert(self, tokens: Sequence[int], max_evicted: int = 1024):
+        """Admit a prefix; returns (info dict, list of evicted prefix handles)."""
+        arr, ptr, n = self._tokens(tokens)
+        out = PrefixInfo()
+        ev = (C.c_int32 * max(1, max_evicted))()
+        n_ev = C.c_int32()
+        _check(self._lib.granikv_index_insert(self.handle, ptr, n, C.byref(out),
+                                              C.cast(ev, C.POINTER(C.c_int32)), max_evicted,
+                                              C.byref(n_ev)), "granikv_index_insert")
+        return out.as_dict(), [ev[i] for i in range(n_ev.value)]
+
+    def acquire(self, prefix_id: int):
+        _check(self._lib.granikv_index_acquire(self.handle, prefix_id), "granikv_index_acquire")
+
+    def release(self, prefix_id: int):
+        _check(self._lib.granikv_index_release(self.handle, prefix_id), "granikv_index_release")
+
+    def remove(self, prefix_id: int):
+        _check(self._lib.granikv_index_remove(self.handle, prefix_id), "granikv_index_remove")
+
+    def info(self, prefix_id: int) -> dict:
+        out = PrefixInfo()
+        _check(self._lib.granikv_index_info(self.handle, prefix_id, C.byref(out)), "granikv_index_info")
+        return out.as_dict()
+
+    def stats(self):
+        """(live prefixes, HOT prefixes, tree nodes)"""
+        a, b, c = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(self._lib.granikv_index_stats(self.handle, C.byref(a), C.byref(b), C.byref(c)),
+               "granikv_index_stats")
+        return a.value, b.value, c.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self._lib.granikv_index_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Context:
     """A libgranikv context (granikv_ctx).  Methods follow the C entry points' names."""
 
@@ -244,9 +333,17 @@ class Context:
         _check(self._lib.granikv_create(C.byref(cfg), C.byref(h)), "granikv_create")
         self.handle = h
         self.n_q, self.n_kv, self.head_dim, self.dtype = n_q, n_kv, head_dim, dtype
+        self._indexes = []
+
+    def index(self) -> Index:
+        return Index(self)
 
     def close(self):
         if getattr(self, "handle", None):
+            for ref in getattr(self, "_indexes", []):
+                x = ref()
+                if x is not None:
+                    x.close()  # an index returns its slabs to this context's HOT pool
             self._lib.granikv_destroy(self.handle)
             self.handle = None
 

@@ -8,7 +8,7 @@ decoded tokens; "B.10 Cross-pool admission and promotion policy": HOT first, COL
 
 from __future__ import annotations
 
-from typing import List, Optional, Sequence
+from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
@@ -43,6 +43,10 @@ class GraniKVCache:
         self.suffix_len = torch.zeros((max_batch,), dtype=torch.int32, device=self.device)
         self.seq_len_host = [0] * max_batch
         self._ws: Optional[torch.Tensor] = None
+        self._index: Optional[gb.Index] = None
+        self.cached: Dict[int, dict] = {}                      # prefixes written by admit()
+        self.cold_prefix_slots: Dict[int, torch.Tensor] = {}  # COLD-placed prefix -> its slots
+        self.row_prefix: List[Optional[Tuple[int, int]]] = [None] * max_batch  # (handle, shared COLD len)
 
     @property
     def n_hot(self) -> int:
@@ -65,6 +69,102 @@ class GraniKVCache:
             v = v_layers[layer].contiguous()
             self.ctx.hot_fill(layer, sid, k, v, s)
         return sid
+
+    # prefix lifecycle ("2 Related Work": a reference-counted radix index over token ids;
+    # "B.10": HOT first, COLD fallback, no demotion) ---------------------------------------
+    @property
+    def index(self) -> gb.Index:
+        if self._index is None:
+            self._index = self.ctx.index()
+        return self._index
+
+    def admit(self, tokens: Sequence[int], k_layers: Sequence[torch.Tensor], v_layers: Sequence[torch.Tensor]):
+        """Cache a prefix given by its token ids and its K/V per layer ([L_p, n_kv, d] each).
+        HOT first (a slab filled by device copies); if the index places it in COLD, its K/V go
+        once into COLD slots that the prefix owns and that its requests share.  Returns
+        (prefix info, evicted handles); an already-cached prefix is not written again."""
+        info, evicted = self.index.insert(tokens)
+        for pid in evicted:  # only unreferenced HOT prefixes are evicted; their slabs are free
+            self.cached.pop(pid, None)
+        pid, L_p = info["prefix_id"], info["length"]
+        if pid in self.cached:
+            return info, evicted
+        s = self.stream()
+        if info["slab_id"] >= 0:
+            for layer in range(self.n_layers):
+                self.ctx.hot_fill(layer, info["slab_id"], k_layers[layer].contiguous(),
+                                  v_layers[layer].contiguous(), s)
+        else:
+            table = torch.empty((1, L_p), dtype=torch.int32, device=self.device)
+            count = torch.zeros((1,), dtype=torch.int32, device=self.device)
+            slots = torch.empty((L_p,), dtype=torch.int32, device=self.device)
+            self.ctx.cold_alloc([L_p], table, count, L_p, slots, s)
+            for layer in range(self.n_layers):
+                self.ctx.cold_append(layer, k_layers[layer].contiguous(), v_layers[layer].contiguous(),
+                                     slots, L_p, s)
+            self.cold_prefix_slots[pid] = slots
+        self.cached[pid] = info
+        return info, evicted
+
+    def attach(self, b: int, tokens: Sequence[int]):
+        """Start request row b from its prompt's token ids: the longest cached prefix it starts
+        with is matched and referenced.  A HOT prefix is read through its slab; a COLD one's
+        slots head the row's token table.  Returns (slab id or -1, prefix tokens reused); the
+        caller then appends the remaining prompt tokens with append()."""
+        if self.row_prefix[b] is not None or self.seq_len_host[b]:
+            raise RuntimeError(f"row {b} is in use")
+        info = self.index.match(tokens, acquire=True)
+        pid = info["prefix_id"]
+        if pid < 0:
+            self.row_prefix[b] = None
+            return -1, 0
+        if info["slab_id"] >= 0:
+            self.row_prefix[b] = (pid, 0)
+            return info["slab_id"], info["length"]
+        L_p = info["length"]
+        if L_p > self.cap:
+            self.index.release(pid)
+            raise ValueError("a COLD prefix longer than the token table")
+        self.req_to_slot[b, :L_p].copy_(self.cold_prefix_slots[pid])
+        self.suffix_len[b].fill_(L_p)
+        self.seq_len_host[b] = L_p
+        self.row_prefix[b] = (pid, L_p)
+        return -1, L_p
+
+    def detach(self, b: int):
+        """Request row b is finished: its own COLD slots return to the free ring and its prefix
+        reference is dropped (the prefix stays cached until evicted or removed)."""
+        shared = 0
+        if self.row_prefix[b] is not None:
+            pid, shared = self.row_prefix[b]
+            self.index.release(pid)
+        own = self.seq_len_host[b] - shared
+        if own > 0:
+            self.ctx.cold_free(self.req_to_slot[b, shared:self.seq_len_host[b]].clone(), own, self.stream())
+        self.row_prefix[b] = None
+        self.seq_len_host[b] = 0
+        self.suffix_len[b].zero_()
+
+    def remove_prefix(self, pid: int):
+        """Drop an unreferenced cached prefix: a HOT slab returns to the pool, a COLD prefix's
+        slots to the free ring."""
+        self.index.remove(pid)
+        self.cached.pop(pid, None)
+        slots = self.cold_prefix_slots.pop(pid, None)
+        if slots is not None:
+            self.ctx.cold_free(slots, slots.numel(), self.stream())
+
+    def move_row(self, src: int, dst: int):
+        """Move request row src (token table, lengths, prefix reference) into the free row dst."""
+        if src == dst:
+            return
+        self.req_to_slot[dst].copy_(self.req_to_slot[src])
+        self.suffix_len[dst].copy_(self.suffix_len[src])
+        self.seq_len_host[dst] = self.seq_len_host[src]
+        self.row_prefix[dst] = self.row_prefix[src]
+        self.seq_len_host[src] = 0
+        self.row_prefix[src] = None
+        self.suffix_len[src].zero_()
 
     # COLD tokens --------------------------------------------------------------------------
     def append(self, n_new: Sequence[int], k_layers: Sequence[torch.Tensor], v_layers: Sequence[torch.Tensor],

@@ -1103,4 +1103,29 @@ void granikv_internal_plan_forget_upload(granikv_plan* p) {
   if (p) p->uploaded_ws = nullptr;
 }
 
+void granikv_internal_hot_if_released(const granikv_ctx* c, const int32_t* slabs, int32_t n,
+                                      int64_t* largest_free, int32_t* free_ids) {
+  std::vector<Extent> ext = c->free_ext;
+  int32_t ids = 0;
+  for (const Slab& s : c->slabs) ids += s.live ? 0 : 1;
+  for (int32_t i = 0; i < n; ++i) {
+    const Slab& s = c->slabs[slabs[i]];
+    ext.push_back({s.off, s.len});
+    ids += 1;
+  }
+  std::sort(ext.begin(), ext.end(), [](const Extent& a, const Extent& b) { return a.off < b.off; });
+  int64_t best = 0, run_off = -1, run_len = 0;
+  for (const Extent& e : ext) {
+    if (run_off >= 0 && run_off + run_len == e.off) {
+      run_len += e.len;
+    } else {
+      run_off = e.off;
+      run_len = e.len;
+    }
+    best = std::max(best, run_len);
+  }
+  *largest_free = best;
+  *free_ids = ids;
+}
+
 }  // namespace granikv

@@ -154,5 +154,9 @@ namespace granikv {
 // Host-side helpers shared between the library's translation units (not part of the C ABI).
 int32_t granikv_internal_device(const granikv_ctx* ctx, int* device);        // a granikv_status
 void granikv_internal_plan_forget_upload(granikv_plan* plan);
+// HOT pool as it would be if the live slabs slabs[0..n) were released as well (nothing is
+// changed): the largest free extent, and the number of unused slab ids.
+void granikv_internal_hot_if_released(const granikv_ctx* ctx, const int32_t* slabs, int32_t n,
+                                      int64_t* largest_free, int32_t* free_ids);
 
 }  // namespace granikv
