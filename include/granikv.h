@@ -287,6 +287,28 @@ granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int32_t layer, 
                                                const granikv_batch* batch, granikv_plan* plan,
                                                void* o, float* lse, granikv_stream_t stream);
 
+/* ---- prefill of a HOT slab ("2 Related Work", prefix-aware serving: a cached prefix skips
+ * prefill for its matched tokens, so a prefix is prefilled once, when it is admitted; card
+ * page: the HOT slab stores the prefix's K_p contiguously, which batched prefix kernels assume
+ * and paged engines do not provide). ---------------------------------------------------- */
+
+/* Causal self-attention of a HOT prefix's own L_p tokens over its slab, in one layer: query
+ * token t (t < L_p) attends slab keys [0, t], with the softmax scale 1/sqrt(head_dim) and KV
+ * head h / (n_q/n_kv) for query head h, as decode attention.
+ *   k_new, v_new: device [L_p, n_kv, head_dim] or both NULL; when given they are first copied
+ *                 into the slab (the prefill writes the contiguous K_p/V_p), stream-ordered
+ *   q:   device [L_p, n_q, head_dim];  o: device [L_p, n_q, head_dim] (context dtype)
+ *   lse: device [L_p, n_q] fp32, natural log
+ *   ws:  device workspace of granikv_prefill_workspace_size(L_p) bytes, 256-byte aligned
+ * L_p is the slab's length.  Runs on the tensor-core dense kernel (one CTA per 128 query rows and
+ * KV head, keys up to the rows' diagonal) and the merge kernel.  GRANIKV_ERR_UNSUPPORTED unless
+ * the dtype is bf16, head_dim is 128 and n_q/n_kv divides 128. */
+granikv_status granikv_prefill_attention(granikv_ctx* ctx, int32_t layer, int32_t slab_id,
+                                         const void* k_new, const void* v_new, const void* q, void* o,
+                                         float* lse, void* workspace, size_t ws_bytes,
+                                         granikv_stream_t stream);
+granikv_status granikv_prefill_workspace_size(granikv_ctx* ctx, int32_t L_p, size_t* bytes);
+
 /* ---- checks -------------------------------------------------------------------------- */
 
 /* 1: kernels bounds-check slot ids, slab ranges and table rows, skip bad accesses and latch

@@ -19,7 +19,9 @@ shows up as a value error.
 
 An empty key sequence gives the empty partial (o = 0, lse = -inf); merging with it is the
 identity.  Parity of every function here is pinned by tests/test_oracle_pins.py (brute force,
-closed forms, merge invariants, permutation invariance, planted needles).
+closed forms, merge invariants, permutation invariance, planted needles; for causal_prefill,
+PyTorch's causal scaled-dot-product attention, the one-key closed form of the first token and
+the direction of the mask).
 """
 
 from __future__ import annotations
@@ -145,3 +147,26 @@ def prefix_suffix_partials(wl, b: int, h: int):
         pp = (np.zeros(s.d), -math.inf)
     ss = attend(q, wl.suffix_k(b)[:, j, :], wl.suffix_v(b)[:, j, :], scale)
     return pp, ss
+
+
+def causal_prefill(q: np.ndarray, K: np.ndarray, V: np.ndarray, tokens: Optional[List[int]] = None,
+                   heads: Optional[List[int]] = None):
+    """Causal self-attention of a prefix's own tokens, the step that fills a HOT slab
+    ("2 Related Work", prefix-aware serving: a prefix is prefilled once, then reused): query
+    token t attends keys 0..t of the prefix.
+
+    q: [L, n_q, d]; K, V: [L, n_kv, d].  Returns (o [len(tokens), len(heads), d],
+    lse [len(tokens), len(heads)]) in float64 for the requested tokens and heads (all by
+    default), each one attend() over the first t+1 keys of its KV head."""
+    L, n_q, d = q.shape
+    n_kv = K.shape[1]
+    tokens = list(range(L)) if tokens is None else list(tokens)
+    heads = list(range(n_q)) if heads is None else list(heads)
+    scale = softmax_scale(d)
+    o = np.zeros((len(tokens), len(heads), d), dtype=np.float64)
+    lse = np.zeros((len(tokens), len(heads)), dtype=np.float64)
+    for a, t in enumerate(tokens):
+        for c, h in enumerate(heads):
+            j = kv_head(h, n_q, n_kv)
+            o[a, c], lse[a, c] = attend(q[t, h], K[:t + 1, j], V[:t + 1, j], scale)
+    return o, lse

@@ -131,6 +131,10 @@ _SIGNATURES = [
                                              C.c_size_t, C.c_void_p]),
     ("granikv_decode_attention_static", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
                                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    ("granikv_prefill_attention", C.c_int32, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
+                                              C.c_void_p]),
+    ("granikv_prefill_workspace_size", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(C.c_size_t)]),
     ("granikv_set_checks", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_inject_stall", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_sync_status", C.c_int32, [C.c_void_p, C.c_void_p]),
@@ -441,6 +445,19 @@ class Context:
         _check(self._lib.granikv_decode_attention_static(self.handle, layer, _ptr(q), C.byref(batch.c),
                                                          plan.handle, _ptr(o), _ptr(lse), _stream(stream)),
                "granikv_decode_attention_static")
+
+    # prefill of a HOT slab
+    def prefill_workspace_size(self, L_p: int) -> int:
+        n = C.c_size_t()
+        _check(self._lib.granikv_prefill_workspace_size(self.handle, L_p, C.byref(n)),
+               "granikv_prefill_workspace_size")
+        return n.value
+
+    def prefill_attention(self, layer: int, slab_id: int, k_new, v_new, q, o, lse, workspace, ws_bytes: int,
+                          stream=None):
+        _check(self._lib.granikv_prefill_attention(self.handle, layer, slab_id, _ptr(k_new), _ptr(v_new), _ptr(q),
+                                                   _ptr(o), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
+               "granikv_prefill_attention")
 
     # checks
     def set_checks(self, on: bool):

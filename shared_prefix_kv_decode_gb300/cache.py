@@ -210,3 +210,23 @@ class GraniKVCache:
         ws = self.workspace(plan)
         self.ctx.decode_attention(layer, q, batch, plan, o, lse, ws, ws.numel(), self.stream())
         return o, lse
+
+    def prefill(self, layer: int, slab_id: int, q: torch.Tensor, k: Optional[torch.Tensor] = None,
+                v: Optional[torch.Tensor] = None, o: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None):
+        """Causal prefill of a HOT prefix in one layer: its K/V ([L_p, n_kv, d], if given) are
+        written into the slab, then each of its L_p query tokens (q [L_p, n_q, d]) attends the
+        slab up to itself.  Returns (o [L_p, n_q, d], lse [L_p, n_q])."""
+        L_p = q.shape[0]
+        if o is None:
+            o = torch.empty((L_p, self.n_q, self.head_dim), dtype=self.tdtype, device=self.device)
+        if lse is None:
+            lse = torch.empty((L_p, self.n_q), dtype=torch.float32, device=self.device)
+        n = self.ctx.prefill_workspace_size(L_p)
+        if self._ws is None or self._ws.numel() < n:
+            self._ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.device)
+        kk = k.contiguous() if k is not None else None
+        vv = v.contiguous() if v is not None else None
+        self.ctx.prefill_attention(layer, slab_id, kk, vv, q.contiguous(), o, lse, self._ws, self._ws.numel(),
+                                   self.stream())
+        return o, lse

@@ -14,6 +14,9 @@
 //            on the FMA pipe and the rest on MUFU, so the two units share the load)
 //     O   += P(i) V(i)  (M=128, N=128, K=128: 8 tcgen05.mma with A = P(i) read from TMEM)
 // Every MMA is 128x128x16, so one issuing thread keeps the tensor core fed.
+// The same CTA runs the causal prefill of a slab (a group flagged causal): its "requests" are the
+// slab's own tokens, row r is token r/g, the CTA reads keys only up to its block's last token,
+// and each row masks the keys after its own token in the diagonal tile.
 // Roles:
 //  * warps 0-7, softmax and epilogue: warp w serves TMEM lanes 32*(w%4).. (row r = lane r) and
 //    column half w/4 of each tile.  The two warps of a row quarter swap their half-row maxima
@@ -118,7 +121,11 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   const int32_t rows = gr.n_req * g;
   int32_t t0, t1;
   piece_range(gr, it.split, t0, t1);
-  const int n_tiles = (t1 - t0 + kN - 1) / kN;
+  // causal prefill: row r is token r/g of the slab and sees keys [0, r/g], so the block's last
+  // token ends the keys this CTA reads (g divides 128, so a block's tokens lie in one tile)
+  const bool causal = gr.causal != 0;
+  if (causal) t1 = min(t1, (it.row_block * kM + kM) / g);
+  const int n_tiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
   // Q by TMA when the group's requests are consecutive in the batch: the row block is then a
   // (64 dims, g heads, 128/g requests) box of q [B, n_q, 128]; otherwise the threads gather it
@@ -335,6 +342,8 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       h = j * g + row % g;
       rec = p.reqs[b].rec_base + it.split;
     }
+    // keys this row may see end at row_end (slab coordinates): its own token + 1 when causal
+    const int32_t row_end = (causal && row < rows) ? min(t1, row / g + 1) : t1;
     float m_used = -INFINITY;  // running max in scaled (base-2) units, identical in both halves
     float l = 0.f;             // this half's share of the row sum
     int pair_phase = 0;
@@ -345,7 +354,8 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
       if (!ok) break;
       tc_fence_after();
-      const int valid = min(kN, t1 - t0 - i * kN);
+      const int valid = min(kN, t1 - t0 - i * kN);               // tokens of the tile in range
+      const int valid_row = min(valid, row_end - t0 - i * kN);    // of those, keys this row sees
       const uint32_t ts = tmem + lane_off + (uint32_t)(sb * kN + half * kHalfCols);
       float s[kHalfCols];
       {
@@ -359,9 +369,9 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
           s[32 + k] = __uint_as_float(u[1][k]);
         }
       }
-      if (valid < kN) {
+      if (valid_row < kN) {
 #pragma unroll
-        for (int k = 0; k < kHalfCols; ++k) s[k] = half * kHalfCols + k < valid ? s[k] : -INFINITY;
+        for (int k = 0; k < kHalfCols; ++k) s[k] = half * kHalfCols + k < valid_row ? s[k] : -INFINITY;
       }
       // half-row max (scale > 0 commutes with max), swapped with the other half
       float mx;

@@ -73,6 +73,7 @@ struct granikv_ctx {
   // tickets of the last call (zeroed again after a device check failure)
   void* last_tickets = nullptr;
   size_t last_tickets_bytes = 0;
+  std::vector<unsigned char> prefill_blob;  // host image of the last prefill call's plan
   // TMA descriptors of each layer's K and V pools (dense backend), valid when has_tmaps
   std::vector<CUtensorMap> tmap_k, tmap_v;
   bool has_tmaps = false;
@@ -666,7 +667,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       dg.split_len = (int32_t)(base * tile);
       dg.n_long = (int32_t)(t - base * n_splits);
       dg.q_b0 = -1;
-      dg.pad[0] = dg.pad[1] = 0;
+      dg.causal = 0;
+      dg.pad = 0;
     }
     // the tensor-core prefix kernels hold one SM per CTA; the suffix gets every other SM (an
     // automatic split that found no piece length leaving the suffix an SM shares them all)
@@ -1046,6 +1048,133 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
     }
   }
   if (e == cudaErrorNotSupported) return GRANIKV_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+// ---- prefill of a HOT slab ------------------------------------------------------------------
+
+namespace {
+// Workspace of a prefill over L_p tokens: the plan image (one causal group whose requests are
+// the slab's tokens, one record per token) followed by the records.
+struct PrefillLayout {
+  size_t off_group_req, off_req, off_pitems, off_rec, off_lse, total;
+  int32_t row_blocks;
+};
+PrefillLayout prefill_layout(const granikv_ctx* c, int32_t L_p) {
+  PrefillLayout l{};
+  const int64_t rows = (int64_t)L_p * c->g;
+  l.row_blocks = (int32_t)((rows + kDenseRows - 1) / kDenseRows);
+  size_t off = align_up(sizeof(DevGroup), 16);
+  l.off_group_req = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)L_p, 16);
+  l.off_req = off;
+  off = align_up(off + sizeof(DevReq) * (size_t)L_p, 16);
+  l.off_pitems = off;
+  off = align_up(off + sizeof(DevPrefixItem) * (size_t)l.row_blocks * c->cfg.n_kv, 256);
+  l.off_rec = off;
+  off = align_up(off + sizeof(float) * (size_t)L_p * c->cfg.n_q * c->cfg.head_dim, 256);
+  l.off_lse = off;
+  off = align_up(off + sizeof(float) * (size_t)L_p * c->cfg.n_q, 256);
+  l.total = off;
+  return l;
+}
+}  // namespace
+
+granikv_status granikv_prefill_workspace_size(granikv_ctx* c, int32_t L_p, size_t* bytes) {
+  if (!c || !bytes || L_p <= 0) return GRANIKV_ERR_INVALID;
+  *bytes = prefill_layout(c, L_p).total;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_prefill_attention(granikv_ctx* c, int32_t layer, int32_t sid, const void* k_new,
+                                         const void* v_new, const void* q, void* o, float* lse, void* ws,
+                                         size_t ws_bytes, granikv_stream_t stream) {
+  if (!c || !q || !o || !lse || !ws) return GRANIKV_ERR_INVALID;
+  if (layer < 0 || layer >= c->cfg.n_layers) return GRANIKV_ERR_INVALID;
+  if (sid < 0 || sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live) return GRANIKV_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return GRANIKV_ERR_INVALID;
+  if ((uintptr_t)ws % 256) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  if (c->cfg.dtype != GRANIKV_DTYPE_BF16 || c->cfg.head_dim != 128 || kDenseRows % c->g != 0 || !c->has_tmaps)
+    return GRANIKV_ERR_UNSUPPORTED;
+  const int32_t L_p = c->slabs[sid].len;
+  const PrefillLayout lay = prefill_layout(c, L_p);
+  if (ws_bytes < lay.total) return GRANIKV_ERR_INVALID;
+  if (k_new) {
+    granikv_status st = granikv_hot_fill(c, layer, sid, k_new, v_new, stream);
+    if (st != GRANIKV_OK) return st;
+  }
+  DeviceGuard dg(c->cfg.device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int32_t n_kv = c->cfg.n_kv, n_q = c->cfg.n_q;
+
+  // plan image: one group (the slab), request b = token b, one record per token; the CTAs of
+  // the longest rows (the last row blocks, which read the most keys) first
+  DevGroup gr{};
+  gr.slab_off = c->slabs[sid].off;
+  gr.L_p = L_p;
+  gr.n_req = L_p;
+  gr.req_begin = 0;
+  gr.n_splits = 1;
+  gr.tile = kDenseTile;
+  gr.split_len = (L_p + kDenseTile - 1) / kDenseTile * kDenseTile;
+  gr.n_long = 0;
+  gr.backend = GRANIKV_BACKEND_DENSE;
+  gr.impl = kImplDenseTc;
+  gr.rows_per_cta = kDenseRows;
+  gr.row_blocks = lay.row_blocks;
+  gr.q_b0 = 0;
+  gr.causal = 1;
+  std::vector<unsigned char>& blob = c->prefill_blob;
+  blob.assign(lay.off_rec, 0);
+  std::memcpy(blob.data(), &gr, sizeof(DevGroup));
+  int32_t* greq = reinterpret_cast<int32_t*>(blob.data() + lay.off_group_req);
+  DevReq* reqs = reinterpret_cast<DevReq*>(blob.data() + lay.off_req);
+  for (int32_t b = 0; b < L_p; ++b) {
+    greq[b] = b;
+    reqs[b] = DevReq{b, 1, 1, 0};
+  }
+  DevPrefixItem* items = reinterpret_cast<DevPrefixItem*>(blob.data() + lay.off_pitems);
+  int32_t n_items = 0;
+  for (int32_t rb = lay.row_blocks - 1; rb >= 0; --rb)
+    for (int32_t j = 0; j < n_kv; ++j) items[n_items++] = DevPrefixItem{0, j, rb, 0};
+  unsigned char* wsb = static_cast<unsigned char*>(ws);
+  cudaError_t e = cudaMemcpyAsync(wsb, blob.data(), blob.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  c->n_copies += 1;
+
+  AttnParams a{};
+  a.q = q;
+  a.o = o;
+  a.lse = lse;
+  a.kpool = c->kpool[layer];
+  a.vpool = c->vpool[layer];
+  a.n_slots = c->cfg.n_slots;
+  a.n_hot = c->n_hot;
+  a.B = L_p;
+  a.n_q = n_q;
+  a.n_kv = n_kv;
+  a.d = c->cfg.head_dim;
+  a.g = c->g;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  a.groups = (const DevGroup*)wsb;
+  a.group_req = (const int32_t*)(wsb + lay.off_group_req);
+  a.reqs = (const DevReq*)(wsb + lay.off_req);
+  a.pitems = (const DevPrefixItem*)(wsb + lay.off_pitems);
+  a.n_pitems = n_items;
+  a.rec_o = (float*)(wsb + lay.off_rec);
+  a.rec_lse = (float*)(wsb + lay.off_lse);
+  a.n_records = L_p;
+  a.err = c->d_err;
+  a.checks = c->checks;
+  CUtensorMap tmq{};
+  a.q_tma = encode_q_map(&tmq, q, L_p, n_q, c->g) ? 1 : 0;
+  e = launch_dense_tc(a, 0, n_items, c->tmap_k[layer], c->tmap_v[layer], tmq, s, true);
+  c->n_kernels += 1;
+  if (e == cudaSuccess) {
+    e = launch_merge(c->cfg.dtype, a, s, true);
+    c->n_kernels += 1;
+  }
   return cuda_status(e);
 }
 

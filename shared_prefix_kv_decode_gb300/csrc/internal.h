@@ -54,7 +54,9 @@ struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int32_t n_long;        // the first n_long pieces are one tile longer than split_len
   int32_t tile;          // token granularity of the pieces
   int32_t q_b0;          // dense: the group's requests are q_b0, q_b0+1, ... (q rows by TMA), else -1
-  int32_t pad[2];
+  int32_t causal;        // dense prefill of the slab's own tokens: request b of the group is token b
+                         // of the slab and attends keys [0, b] (0 for decode groups)
+  int32_t pad;
 };
 static_assert(sizeof(DevGroup) == 64, "DevGroup layout");
 

@@ -244,9 +244,62 @@ def pin_needles():
             assert np.max(np.abs(o[h] - V[pos, j])) <= 0.05, (b, h)
 
 
+# ------------------------------------------------------------------------------------------
+# causal prefill of a prefix (the step that fills a HOT slab)
+
+def _prefill_case(L, n_q, n_kv, d, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((L, n_q, d))
+    K = rng.standard_normal((L, n_kv, d))
+    V = rng.standard_normal((L, n_kv, d))
+    return q, K, V
+
+
+def pin_prefill_torch_sdpa():
+    # PyTorch's own causal scaled-dot-product attention in float64, KV heads repeated for GQA
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for (L, n_q, n_kv, d) in [(37, 8, 2, 16), (64, 4, 4, 8), (9, 6, 1, 32)]:
+        q, K, V = _prefill_case(L, n_q, n_kv, d, L)
+        o, _ = A.causal_prefill(q, K, V)
+        g = n_q // n_kv
+        tq = torch.from_numpy(q).permute(1, 0, 2)                              # [n_q, L, d]
+        tk = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(g, dim=0)  # [n_q, L, d]
+        tv = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(g, dim=0)
+        ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True).permute(1, 0, 2).numpy()
+        assert np.max(np.abs(o - ref)) < 1e-12
+
+
+def pin_prefill_first_token():
+    # a single key: the output is that key's value row, the lse its scaled score
+    q, K, V = _prefill_case(20, 8, 2, 16, 3)
+    o, lse = A.causal_prefill(q, K, V, tokens=[0])
+    for h in range(8):
+        j = h // 4
+        assert np.array_equal(o[0, h], V[0, j])
+        assert abs(lse[0, h] - float(q[0, h] @ K[0, j]) / 4.0) < 1e-12
+
+
+def pin_prefill_mask_direction():
+    # token t does not see tokens after it, and does see the ones before it
+    q, K, V = _prefill_case(30, 4, 2, 8, 5)
+    o, lse = A.causal_prefill(q, K, V)
+    K2, V2 = K.copy(), V.copy()
+    K2[20:] += 3.0
+    V2[20:] -= 2.0
+    o2, lse2 = A.causal_prefill(q, K2, V2)
+    assert np.array_equal(o[:20], o2[:20]) and np.array_equal(lse[:20], lse2[:20])
+    assert np.all(np.abs(o[20:] - o2[20:]).max(axis=(1, 2)) > 1e-3)
+    V3 = V.copy()
+    V3[0] += 1.0
+    o3, _ = A.causal_prefill(q, K, V3)
+    assert np.all(np.abs(o3 - o).max(axis=(1, 2)) > 1e-6)
+
+
 PINS = [pin_bruteforce_mpmath, pin_torch_softmax, pin_closed_forms, pin_uniform_q_zero,
         pin_gqa_mapping, pin_concat_prefix_suffix, pin_merge_invariant,
-        pin_prefix_suffix_decomposition, pin_permutation_invariance, pin_needles]
+        pin_prefix_suffix_decomposition, pin_permutation_invariance, pin_needles,
+        pin_prefill_torch_sdpa, pin_prefill_first_token, pin_prefill_mask_direction]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
