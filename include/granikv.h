@@ -133,7 +133,8 @@ granikv_status granikv_hot_info(granikv_ctx* ctx, int32_t slab_id, int64_t* slot
 /* Number of HOT slots, and the largest free extent. */
 granikv_status granikv_hot_stats(granikv_ctx* ctx, int64_t* n_hot, int64_t* largest_free);
 /* Copy a prefix's K/V ([L_p, n_kv, head_dim], device, contiguous) into a slab of one layer.
- * Stream-ordered device-to-device copies; the prefill that produces K/V is outside the path. */
+ * Stream-ordered device-to-device copies (granikv_prefill_attention does the same copy and then
+ * the prefix's causal attention; the projection that produces K/V is outside the library). */
 granikv_status granikv_hot_fill(granikv_ctx* ctx, int32_t layer, int32_t slab_id,
                                 const void* k, const void* v, granikv_stream_t stream);
 
@@ -300,9 +301,9 @@ granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int32_t layer, 
  *   q:   device [L_p, n_q, head_dim];  o: device [L_p, n_q, head_dim] (context dtype)
  *   lse: device [L_p, n_q] fp32, natural log
  *   ws:  device workspace of granikv_prefill_workspace_size(L_p) bytes, 256-byte aligned
- * L_p is the slab's length.  Runs on the tensor-core dense kernel (one CTA per 128 query rows and
- * KV head, keys up to the rows' diagonal) and the merge kernel.  GRANIKV_ERR_UNSUPPORTED unless
- * the dtype is bf16, head_dim is 128 and n_q/n_kv divides 128. */
+ * L_p is the slab's length.  Runs on the tensor-core dense kernel alone (one CTA per 128 query
+ * rows and KV head, keys up to the rows' diagonal, o and lse written directly).
+ * GRANIKV_ERR_UNSUPPORTED unless the dtype is bf16, head_dim is 128 and n_q/n_kv divides 128. */
 granikv_status granikv_prefill_attention(granikv_ctx* ctx, int32_t layer, int32_t slab_id,
                                          const void* k_new, const void* v_new, const void* q, void* o,
                                          float* lse, void* workspace, size_t ws_bytes,

@@ -493,7 +493,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     if (ok) {
       tc_fence_after();
       const float lt = l0 + l1;
-      if (row < rows && (rec < 0 || rec >= p.n_records)) {
+      if (!causal && row < rows && (rec < 0 || rec >= p.n_records)) {
         if (half == 0) atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
         rec = -1;
       }
@@ -517,8 +517,16 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
                           __uint_as_float(u[c][k + 2]) * inv, __uint_as_float(u[c][k + 3]) * inv);
         }
       if (half == 0) {
-        reinterpret_cast<int64_t*>(smem + kOffV)[r] = rec >= 0 ? ((int64_t)rec * p.n_q + h) * kD : -1;
-        if (rec >= 0) p.rec_lse[(int64_t)rec * p.n_q + h] = lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+        const float lse_row = lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+        if (causal) {
+          // a prefill row has exactly one record: the final o (bf16) and lse go out directly
+          const int64_t orow = (int64_t)b * p.n_q + h;
+          reinterpret_cast<int64_t*>(smem + kOffV)[r] = row < rows ? orow * kD : -1;
+          if (row < rows) p.lse[orow] = lse_row;
+        } else {
+          reinterpret_cast<int64_t*>(smem + kOffV)[r] = rec >= 0 ? ((int64_t)rec * p.n_q + h) * kD : -1;
+          if (rec >= 0) p.rec_lse[(int64_t)rec * p.n_q + h] = lse_row;
+        }
       }
     }
     // both halves of the quarter's 32 rows are staged (both warps of a pair agree on `ok`)
@@ -533,11 +541,16 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       for (int i = 0; i < 16; ++i) {
         const int rr = quad * 32 + half * 16 + i;
         const int64_t d = sdst[rr];
-        if (d >= 0)
-          *reinterpret_cast<float4*>(p.rec_o + d + lane * 4) =
-              *reinterpret_cast<const float4*>(stage + rr * 512 + ((lane ^ (rr & 31)) << 4));
+        if (d < 0) continue;
+        const float4 x = *reinterpret_cast<const float4*>(stage + rr * 512 + ((lane ^ (rr & 31)) << 4));
+        if (causal) {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + d + lane * 4) =
+              make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+        } else {
+          *reinterpret_cast<float4*>(p.rec_o + d + lane * 4) = x;
+        }
       }
-      if (p.fused_merge) {
+      if (p.fused_merge && !causal) {
         // the row's record is complete (both warps stored their rows) before its ticket moves
         __threadfence();
         mbar_arrive(bar(pair_bar));

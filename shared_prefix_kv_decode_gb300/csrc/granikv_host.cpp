@@ -1054,10 +1054,11 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
 // ---- prefill of a HOT slab ------------------------------------------------------------------
 
 namespace {
-// Workspace of a prefill over L_p tokens: the plan image (one causal group whose requests are
-// the slab's tokens, one record per token) followed by the records.
+// Workspace of a prefill over L_p tokens: the plan image only (one causal group whose requests
+// are the slab's tokens; each query row has one partial state, which the dense kernel writes
+// out as the final o and lse, so there are no records and no merge).
 struct PrefillLayout {
-  size_t off_group_req, off_req, off_pitems, off_rec, off_lse, total;
+  size_t off_group_req, off_req, off_pitems, total;
   int32_t row_blocks;
 };
 PrefillLayout prefill_layout(const granikv_ctx* c, int32_t L_p) {
@@ -1071,10 +1072,6 @@ PrefillLayout prefill_layout(const granikv_ctx* c, int32_t L_p) {
   off = align_up(off + sizeof(DevReq) * (size_t)L_p, 16);
   l.off_pitems = off;
   off = align_up(off + sizeof(DevPrefixItem) * (size_t)l.row_blocks * c->cfg.n_kv, 256);
-  l.off_rec = off;
-  off = align_up(off + sizeof(float) * (size_t)L_p * c->cfg.n_q * c->cfg.head_dim, 256);
-  l.off_lse = off;
-  off = align_up(off + sizeof(float) * (size_t)L_p * c->cfg.n_q, 256);
   l.total = off;
   return l;
 }
@@ -1126,7 +1123,7 @@ granikv_status granikv_prefill_attention(granikv_ctx* c, int32_t layer, int32_t 
   gr.q_b0 = 0;
   gr.causal = 1;
   std::vector<unsigned char>& blob = c->prefill_blob;
-  blob.assign(lay.off_rec, 0);
+  blob.assign(lay.total, 0);
   std::memcpy(blob.data(), &gr, sizeof(DevGroup));
   int32_t* greq = reinterpret_cast<int32_t*>(blob.data() + lay.off_group_req);
   DevReq* reqs = reinterpret_cast<DevReq*>(blob.data() + lay.off_req);
@@ -1162,19 +1159,13 @@ granikv_status granikv_prefill_attention(granikv_ctx* c, int32_t layer, int32_t 
   a.reqs = (const DevReq*)(wsb + lay.off_req);
   a.pitems = (const DevPrefixItem*)(wsb + lay.off_pitems);
   a.n_pitems = n_items;
-  a.rec_o = (float*)(wsb + lay.off_rec);
-  a.rec_lse = (float*)(wsb + lay.off_lse);
-  a.n_records = L_p;
+  a.n_records = 0;
   a.err = c->d_err;
   a.checks = c->checks;
   CUtensorMap tmq{};
   a.q_tma = encode_q_map(&tmq, q, L_p, n_q, c->g) ? 1 : 0;
   e = launch_dense_tc(a, 0, n_items, c->tmap_k[layer], c->tmap_v[layer], tmq, s, true);
   c->n_kernels += 1;
-  if (e == cudaSuccess) {
-    e = launch_merge(c->cfg.dtype, a, s, true);
-    c->n_kernels += 1;
-  }
   return cuda_status(e);
 }
 
