@@ -84,13 +84,19 @@ typedef struct granikv_config {
 
 /* One decode step's batch.  Request b attends over its HOT prefix slab (if slab_id[b] >= 0)
  * followed by the seq_len[b] tokens listed in req_to_slot[b, 0:seq_len[b]].  A prefix that is
- * not in HOT is simply the head of that list (the paged fallback). */
+ * not in HOT is simply the head of that list (the paged fallback).
+ * seq_len_dev (optional) lets one plan serve several decode steps, as a CUDA graph replayed
+ * step after step needs: the plan is made for seq_len (the lengths the requests may reach, e.g.
+ * the current ones plus a headroom), and each attention call reads the lengths the requests
+ * have now from seq_len_dev (device [B], e.g. the suffix_len array granikv_cold_alloc keeps) and
+ * attends over req_to_slot[b, 0:min(seq_len[b], seq_len_dev[b])]. */
 typedef struct granikv_batch {
   int32_t B;
   const int32_t* slab_id;     /* host [B]: HOT slab of request b, or -1                   */
   const int32_t* seq_len;     /* host [B]: tokens of request b in its COLD token table     */
   const int32_t* req_to_slot; /* device [B, cap] int32: COLD slot of each token, row-major */
   int32_t cap;                /* row stride of req_to_slot                                 */
+  const int32_t* seq_len_dev; /* device [B] int32 or NULL: the tokens that exist now       */
 } granikv_batch;
 
 typedef struct granikv_group_info {
@@ -158,6 +164,18 @@ granikv_status granikv_cold_free(granikv_ctx* ctx, const int32_t* slots, int32_t
                                  granikv_stream_t stream);
 /* Free COLD slots (host mirror of the ring's fill). */
 granikv_status granikv_cold_free_count(granikv_ctx* ctx, int64_t* n_free);
+/* granikv_cold_alloc with n_new[b] = n for every request b < B (decode steps: n = 1), safe to
+ * capture in a CUDA graph and replay: the kernel reads the ring position from device memory,
+ * checks there that n*B slots are free (otherwise it pops nothing and latches
+ * GRANIKV_ERR_DEVICE_CHECK, reported by granikv_sync_status) and moves it; slots_out (device
+ * [n*B], may be NULL) receives the slots in request order.  The host's copy of the ring
+ * position is advanced as if the call ran once, so after capturing or replaying graphs that
+ * contain it, call granikv_cold_sync before the next granikv_cold_alloc or granikv_cold_free. */
+granikv_status granikv_cold_alloc_uniform(granikv_ctx* ctx, int32_t n, int32_t B, int32_t* req_to_slot,
+                                          int32_t* suffix_len, int32_t cap, int32_t* slots_out,
+                                          granikv_stream_t stream);
+/* Synchronise the stream and take the host's copy of the COLD ring position from the device. */
+granikv_status granikv_cold_sync(granikv_ctx* ctx, granikv_stream_t stream);
 /* Scatter N new tokens' K/V ([N, n_kv, head_dim] each, device) into one layer's pools at
  * slots[i] (device [N]).  A slot outside [n_hot, n_slots) is a device check failure. */
 granikv_status granikv_cold_append(granikv_ctx* ctx, int32_t layer, const void* k_new,

@@ -64,7 +64,8 @@ class _Config(C.Structure):
 
 class _Batch(C.Structure):
     _fields_ = [("B", C.c_int32), ("slab_id", C.POINTER(C.c_int32)),
-                ("seq_len", C.POINTER(C.c_int32)), ("req_to_slot", C.c_void_p), ("cap", C.c_int32)]
+                ("seq_len", C.POINTER(C.c_int32)), ("req_to_slot", C.c_void_p), ("cap", C.c_int32),
+                ("seq_len_dev", C.c_void_p)]
 
 
 class GroupInfo(C.Structure):
@@ -101,6 +102,9 @@ _SIGNATURES = [
                                        C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p]),
     ("granikv_cold_free", C.c_int32, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p]),
     ("granikv_cold_free_count", C.c_int32, [C.c_void_p, C.POINTER(C.c_int64)]),
+    ("granikv_cold_alloc_uniform", C.c_int32, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                               C.c_int32, C.c_void_p, C.c_void_p]),
+    ("granikv_cold_sync", C.c_int32, [C.c_void_p, C.c_void_p]),
     ("granikv_cold_append", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
                                         C.c_int32, C.c_void_p]),
     ("granikv_index_create", C.c_int32, [C.c_void_p, C.POINTER(C.c_void_p)]),
@@ -205,14 +209,16 @@ def _i32_array(values: Sequence[int]):
 class Batch:
     """Host-side batch descriptor (granikv_batch); keeps its host arrays alive."""
 
-    def __init__(self, slab_id: Sequence[int], seq_len: Sequence[int], req_to_slot, cap: int):
+    def __init__(self, slab_id: Sequence[int], seq_len: Sequence[int], req_to_slot, cap: int, seq_len_dev=None):
         if len(slab_id) != len(seq_len):
             raise ValueError("slab_id and seq_len differ in length")
         self._slab = _i32_array(slab_id)
         self._len = _i32_array(seq_len)
-        self._table = req_to_slot  # keep the tensor alive
+        self._table = req_to_slot  # keep the tensors alive
+        self._live = seq_len_dev
         self.c = _Batch(len(slab_id), C.cast(self._slab, C.POINTER(C.c_int32)),
-                        C.cast(self._len, C.POINTER(C.c_int32)), _ptr(req_to_slot) or 0, int(cap))
+                        C.cast(self._len, C.POINTER(C.c_int32)), _ptr(req_to_slot) or 0, int(cap),
+                        _ptr(seq_len_dev))
 
     @property
     def B(self) -> int:
@@ -389,6 +395,13 @@ class Context:
 
     def cold_free(self, slots, n: int, stream=None):
         _check(self._lib.granikv_cold_free(self.handle, _ptr(slots), n, _stream(stream)), "granikv_cold_free")
+
+    def cold_alloc_uniform(self, n: int, B: int, req_to_slot, suffix_len, cap: int, slots_out=None, stream=None):
+        _check(self._lib.granikv_cold_alloc_uniform(self.handle, n, B, _ptr(req_to_slot), _ptr(suffix_len), cap,
+                                                    _ptr(slots_out), _stream(stream)), "granikv_cold_alloc_uniform")
+
+    def cold_sync(self, stream=None):
+        _check(self._lib.granikv_cold_sync(self.handle, _stream(stream)), "granikv_cold_sync")
 
     def cold_free_count(self) -> int:
         n = C.c_int64()

@@ -54,6 +54,7 @@ struct granikv_ctx {
   int32_t* d_ring = nullptr;
   int32_t* d_err = nullptr;
   int32_t* d_stage = nullptr;  // [max_batch + 1] exclusive offsets for cold_alloc
+  int64_t* d_ring_pos = nullptr;  // {head, tail} of the COLD ring on the device (absolute counts)
   int32_t num_sms = 152;
   int32_t cc_major = 0, cc_minor = 0;
   // dispatch state
@@ -287,9 +288,14 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
     if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_ring, sizeof(int32_t) * c->n_cold);
     if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_err, sizeof(int32_t) * 4);
     if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_stage, sizeof(int32_t) * (c->cfg.max_batch + 1));
+    if (e == cudaSuccess) e = cudaMalloc((void**)&c->d_ring_pos, sizeof(int64_t) * 2);
     if (e == cudaSuccess)
       e = cudaMemcpy(c->d_ring, init.data(), sizeof(int32_t) * c->n_cold, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(int32_t) * 4);
+    if (e == cudaSuccess) {
+      const int64_t pos[2] = {c->head, c->tail};
+      e = cudaMemcpy(c->d_ring_pos, pos, sizeof(pos), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming);
@@ -308,6 +314,8 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
       if (c->d_ring) cudaFree(c->d_ring);
       if (c->d_err) cudaFree(c->d_err);
       if (c->d_stage) cudaFree(c->d_stage);
+    if (c->d_ring_pos) cudaFree(c->d_ring_pos);
+      if (c->d_ring_pos) cudaFree(c->d_ring_pos);
       if (c->ev_fork) cudaEventDestroy(c->ev_fork);
       if (c->ev_join) cudaEventDestroy(c->ev_join);
       if (c->aux) cudaStreamDestroy(c->aux);
@@ -445,7 +453,7 @@ granikv_status granikv_cold_alloc(granikv_ctx* c, const int32_t* n_new, int32_t 
                                   cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = launch_cold_alloc(c->d_stage, B, c->d_ring, c->n_cold, c->head, req_to_slot, suffix_len,
-                          cap, slots_out, c->d_err, s);
+                          cap, slots_out, c->d_ring_pos, c->d_err, s);
   if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
   c->n_copies += 1;
   c->n_kernels += 1;
@@ -461,10 +469,39 @@ granikv_status granikv_cold_free(granikv_ctx* c, const int32_t* slots, int32_t n
   if (n == 0) return GRANIKV_OK;
   DeviceGuard dg(c->cfg.device);
   cudaError_t e = launch_cold_free(slots, n, c->d_ring, c->n_cold, c->tail, c->n_hot,
-                                   c->cfg.n_slots, c->checks, c->d_err, (cudaStream_t)stream);
+                                   c->cfg.n_slots, c->checks, c->d_ring_pos, c->d_err, (cudaStream_t)stream);
   if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
   c->n_kernels += 1;
   c->tail += n;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_cold_alloc_uniform(granikv_ctx* c, int32_t n, int32_t B, int32_t* req_to_slot,
+                                          int32_t* suffix_len, int32_t cap, int32_t* slots_out,
+                                          granikv_stream_t stream) {
+  if (!c || n < 0 || B <= 0 || !req_to_slot || !suffix_len || cap <= 0 || n > cap) return GRANIKV_ERR_INVALID;
+  if (B > c->cfg.max_batch) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  if (n == 0) return GRANIKV_OK;
+  DeviceGuard dg(c->cfg.device);
+  cudaError_t e = launch_cold_alloc_uniform(n, B, c->d_ring, c->n_cold, req_to_slot, suffix_len, cap, slots_out,
+                                            c->d_ring_pos, c->d_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  c->n_kernels += 1;
+  c->head += (int64_t)n * B;  // as if it ran once; granikv_cold_sync reads the device's count
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_cold_sync(granikv_ctx* c, granikv_stream_t stream) {
+  if (!c) return GRANIKV_ERR_INVALID;
+  if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
+  DeviceGuard dg(c->cfg.device);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  int64_t pos[2] = {0, 0};
+  if (e == cudaSuccess) e = cudaMemcpy(pos, c->d_ring_pos, sizeof(pos), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
+  c->head = pos[0];
+  c->tail = pos[1];
   return GRANIKV_OK;
 }
 
@@ -975,6 +1012,7 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.fused_merge = p->fused ? 1 : 0;
   a.inject_stall = c->inject_stall;
   c->inject_stall = 0;
+  a.live_len = bt->seq_len_dev;
   CUtensorMap tmq{};
   a.q_tma = 0;
   if (p->pitem_count[kImplDenseTc] > 0 && c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128)

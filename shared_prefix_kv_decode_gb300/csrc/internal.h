@@ -22,6 +22,7 @@ enum DevErr : int32_t {
   kDevBadRecord = 4,      // a partial-state record index outside the workspace
   kDevSmemAlign = 5,      // a kernel's dynamic shared memory was not aligned as its layout needs
   kDevTimeout = 6,        // a bounded mbarrier wait expired (the CTA drained and gave up)
+  kDevColdEmpty = 7,      // a device-side COLD allocation found fewer free slots than asked
 };
 
 // Kernel implementations a prefix group or the suffix pass can run on.
@@ -113,18 +114,24 @@ struct AttnParams {
   int32_t fused_merge;    // 1: the last producer of a row merges it (no merge kernel)
   int32_t q_tma;          // 1: the q tensor map passed to the dense kernel is valid
   int32_t inject_stall;   // test hook: suffix token-CTA 0 withholds its first tile (see header)
+  const int32_t* live_len;  // [B] device token counts that end each request's suffix segments early
+                            // (the plan may cover more tokens than exist yet); NULL: the plan's
 };
 
 // ---- launchers (kernels_*.cu) ------------------------------------------------------------
 // `pdl`: launch as a programmatic dependent of the previous kernel in the stream (see
 // launch_util.cuh); only for a kernel whose stream predecessor is a kernel of this library.
-cudaError_t launch_cold_alloc(const int32_t* excl /*[B+1]*/, int32_t B, const int32_t* ring,
-                              int64_t n_cold, int64_t head, int32_t* req_to_slot,
-                              int32_t* suffix_len, int32_t cap, int32_t* slots_out,
-                              int32_t* err, cudaStream_t s);
+cudaError_t launch_cold_alloc(const int32_t* excl /*[B+1]*/, int32_t B, const int32_t* ring, int64_t n_cold,
+                              int64_t head, int32_t* req_to_slot, int32_t* suffix_len, int32_t cap,
+                              int32_t* slots_out, int64_t* ring_pos, int32_t* err, cudaStream_t s);
+// n slots for each of requests 0..B-1, the ring position read from and written back to
+// ring_pos[0..1] (head, tail) on the device, the free count checked there (one block).
+cudaError_t launch_cold_alloc_uniform(int32_t n, int32_t B, const int32_t* ring, int64_t n_cold, int32_t* req_to_slot,
+                                      int32_t* suffix_len, int32_t cap, int32_t* slots_out, int64_t* ring_pos,
+                                      int32_t* err, cudaStream_t s);
 cudaError_t launch_cold_free(const int32_t* slots, int32_t n, int32_t* ring, int64_t n_cold,
                              int64_t tail, int64_t n_hot, int64_t n_slots, int32_t checks,
-                             int32_t* err, cudaStream_t s);
+                             int64_t* ring_pos, int32_t* err, cudaStream_t s);
 cudaError_t launch_cold_append(int32_t dtype, const void* k_new, const void* v_new,
                                const int32_t* slots, int32_t N, void* kpool, void* vpool,
                                int64_t row_elems, int64_t n_hot, int64_t n_slots,

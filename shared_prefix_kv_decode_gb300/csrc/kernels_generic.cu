@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(256) prefix_generic_kernel(AttnParams p, int32
 // slot req_to_slot[b, t].  Warps take the query heads in turn.
 template <typename T, int VPL>
 __global__ void __launch_bounds__(256) suffix_generic_kernel(AttnParams p) {
-  const DevSuffixItem it = p.sitems[blockIdx.x];
+  DevSuffixItem it = p.sitems[blockIdx.x];
+  if (p.live_len) it.t1 = max(it.t0, min(it.t1, p.live_len[it.b]));  // tokens that exist now
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t tok_stride = (int64_t)p.n_kv * p.d;
   const int32_t* table = p.req_to_slot + (int64_t)it.b * p.cap;

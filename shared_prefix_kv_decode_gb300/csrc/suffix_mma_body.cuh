@@ -100,13 +100,25 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
   DevSuffixItem* sseg = reinterpret_cast<DevSuffixItem*>(smem + kOffSegs);
   const int n_seg = seg_end - seg_begin;
   for (int k = threadIdx.x; k < min(n_seg, kSegSmem); k += blockDim.x) sseg[k] = p.sitems[seg_begin + k];
-  const DevSuffixItem* segs = n_seg <= kSegSmem ? sseg : p.sitems + seg_begin;
-  // the token tables, pools and q are read only after the previous kernel in the stream completed
+  // the token tables, lengths, pools and q are read only after the previous kernel in the
+  // stream completed
   grid_dep_wait();
   grid_dep_launch_dependents();
+  // a plan made for more tokens than exist yet: each segment ends at its request's live length
+  auto clamp = [&](DevSuffixItem sgi) {
+    if (p.live_len) sgi.t1 = max(sgi.t0, min(sgi.t1, p.live_len[sgi.b]));
+    return sgi;
+  };
+  if (p.live_len) {
+    __syncthreads();  // the staged descriptors are complete
+    for (int k = threadIdx.x; k < min(n_seg, kSegSmem); k += blockDim.x) sseg[k] = clamp(sseg[k]);
+    __syncthreads();
+  }
+  auto seg_at = [&](int k) { return k < kSegSmem ? sseg[k] : clamp(p.sitems[seg_begin + k]); };
   int n_tok = 0;
   for (int sg = seg_begin; sg < seg_end; ++sg) {
-    const DevSuffixItem seg = p.sitems[sg];
+    // from global memory: the staged copies are not complete before the barrier below
+    const DevSuffixItem seg = clamp(p.sitems[sg]);
     const int len = seg.t1 - seg.t0;
     const int32_t* row = p.req_to_slot + (int64_t)seg.b * p.cap + seg.t0;
     for (int k = threadIdx.x; k < len && n_tok + k < kSuffixMaxCtaTokens; k += blockDim.x) sslot[n_tok + k] = row[k];
@@ -136,7 +148,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     // test hook: token-CTA 0 of group 0 withholds its first tile
     const bool skip0 = p.inject_stall != 0 && cta == 0 && group == 0;
     for (int sg = 0; sg < n_seg && !stop; ++sg) {
-      const DevSuffixItem seg = segs[sg];
+      const DevSuffixItem seg = seg_at(sg);
       for (int t = seg.t0; t < seg.t1; t += kTile, ++n) {
         const int st = n % kStages;
         // every lane polls; the warp goes on only if all of them saw the phase complete
@@ -190,7 +202,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     const int nn = lane >> 2;
     if (sg < n_seg && nn < g) {
       const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)segs[sg].b * p.n_q + j * g + nn) * kD);
+          static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)seg_at(sg).b * p.n_q + j * g + nn) * kD);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         qn[kk][0] = qrow[kk * 8 + (lane & 3)];
@@ -205,7 +217,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
   const uint32_t head_off = (uint32_t)warp * kRowBytes;
   int tile = 0;  // tiles consumed so far
   for (int sg = 0; sg < n_seg; ++sg) {
-    const DevSuffixItem seg = segs[sg];
+    const DevSuffixItem seg = seg_at(sg);
     uint32_t qf[8][2];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {

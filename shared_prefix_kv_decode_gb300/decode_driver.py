@@ -14,9 +14,17 @@ return the request's COLD slots (granikv_cold_free) and move the last request's 
 its row, so the active requests always occupy table rows 0..B-1.
 
 The per-step trace holds B, the groups (M_eff, backend, pieces), the host time of the dispatch
-call and the GPU time of the step's attention calls.
+call, the host time to issue the whole step and the GPU time of the step's attention calls.
 
-  python -m shared_prefix_kv_decode_gb300.decode_driver [--steps 64] [--layers 2] [--seed 0]
+Graph mode (B.5 "Per-Step Dispatch Overhead"; SURVEY's CUDA-graph capture of the step): the
+step's slot allocation (granikv_cold_alloc_uniform), K/V scatter and attention calls of every
+layer are captured once in a CUDA graph and replayed step after step.  The plan is made for the
+requests' lengths plus a headroom and the kernels read the lengths that exist from the device
+(granikv_batch.seq_len_dev), so one capture serves until the batch changes or a request would
+outgrow its planned length; then the step runs eagerly once (which also uploads the new plan)
+and is captured again.
+
+  python -m shared_prefix_kv_decode_gb300.decode_driver [--steps 64] [--layers 2] [--seed 0] [--graph]
 """
 
 from __future__ import annotations
@@ -44,7 +52,8 @@ class DecodeDriver:
 
     def __init__(self, *, prefix_lens: Sequence[int], n_layers: int = 1, n_q: int = 32, n_kv: int = 8,
                  head_dim: int = 128, max_batch: int = 256, cap: int = 4096, n_slots: int = 1 << 17,
-                 seed: int = 0, keep_logical: bool = False, device: int = 0):
+                 seed: int = 0, keep_logical: bool = False, device: int = 0, graph: bool = False,
+                 headroom: int = 16):
         self.n_layers, self.n_q, self.n_kv, self.d = n_layers, n_q, n_kv, head_dim
         self.rng = np.random.default_rng(seed)
         self.keep = keep_logical
@@ -69,6 +78,20 @@ class DecodeDriver:
         self._events = []
         self.last_q: Optional[List[np.ndarray]] = None
         self.last_out = None
+        # graph mode: fixed device buffers the captured step reads and writes
+        self.graph_mode, self.headroom = graph, headroom
+        self._graph = None
+        self._graph_key = None
+        self._planned: List[int] = []
+        self._cold_dirty = False  # graph work moved the ring position on the device only
+        if graph:
+            dt, dev = torch.bfloat16, self.dev
+            self._q_buf = [torch.zeros((max_batch, n_q, head_dim), dtype=dt, device=dev) for _ in range(n_layers)]
+            self._k_buf = [torch.zeros((max_batch, n_kv, head_dim), dtype=dt, device=dev) for _ in range(n_layers)]
+            self._v_buf = [torch.zeros((max_batch, n_kv, head_dim), dtype=dt, device=dev) for _ in range(n_layers)]
+            self._o_buf = [torch.zeros((max_batch, n_q, head_dim), dtype=dt, device=dev) for _ in range(n_layers)]
+            self._lse_buf = [torch.zeros((max_batch, n_q), dtype=torch.float32, device=dev) for _ in range(n_layers)]
+            self._slots_buf = torch.zeros((max_batch,), dtype=torch.int32, device=dev)
 
     # ---- helpers -------------------------------------------------------------------------
     def _draw(self, shape, scale: float = 1.0) -> np.ndarray:
@@ -83,12 +106,19 @@ class DecodeDriver:
     def B(self) -> int:
         return len(self.rows)
 
-    def _append(self, n_new: List[int]):
-        """n_new[b] new tokens for active request b, K/V drawn here, in every layer."""
-        N = int(sum(n_new))
+    def _sync_cold(self):
+        """Bring the host's copy of the COLD ring position up to date after graph work."""
+        if self._cold_dirty:
+            self.ctx.cold_sync(self.cache.stream())
+            self._cold_dirty = False
+
+    def _draw_new(self, N: int):
+        """K/V of N new tokens in every layer: host copies (float32) and device tensors."""
         ks = [self._draw((N, self.n_kv, self.d)) for _ in range(self.n_layers)]
         vs = [self._draw((N, self.n_kv, self.d)) for _ in range(self.n_layers)]
-        self.cache.append(n_new, [self._dev(x) for x in ks], [self._dev(x) for x in vs])
+        return ks, vs, [self._dev(x) for x in ks], [self._dev(x) for x in vs]
+
+    def _keep_new(self, n_new: List[int], ks, vs):
         if self.keep:
             off = 0
             for b, n in enumerate(n_new):
@@ -97,6 +127,13 @@ class DecodeDriver:
                     r["k"][layer].append(ks[layer][off:off + n])
                     r["v"][layer].append(vs[layer][off:off + n])
                 off += n
+
+    def _append(self, n_new: List[int]):
+        """n_new[b] new tokens for active request b, K/V drawn here, in every layer."""
+        self._sync_cold()
+        ks, vs, kd, vd = self._draw_new(int(sum(n_new)))
+        self.cache.append(n_new, kd, vd)
+        self._keep_new(n_new, ks, vs)
 
     # ---- arrivals and completions --------------------------------------------------------
     def arrive(self, prefix: int, prompt_len: int):
@@ -114,6 +151,7 @@ class DecodeDriver:
     def complete(self, b: int):
         """Request in row b finishes: its COLD slots go back to the free list, and the last row's
         request moves into row b."""
+        self._sync_cold()
         s = self.cache.stream()
         L = self.rows[b]["len"]
         if L:
@@ -131,36 +169,107 @@ class DecodeDriver:
 
     # ---- one decode step -----------------------------------------------------------------
     def step(self):
+        """One decode step of every active request: one new token each (slot, K/V in every
+        layer), then attention in every layer."""
         B = self.B
         if B == 0:
             return None
-        self._append([1] * B)
         for r in self.rows:
             r["len"] += 1
         slab_ids = [self.slabs[r["prefix"]] for r in self.rows]
-        batch = self.cache.batch(slab_ids, [r["len"] for r in self.rows])
-        t0 = time.perf_counter()
-        self.ctx.dispatch(batch, self.plan)
-        t_disp = time.perf_counter() - t0
+        # the step's synthetic inputs, drawn and uploaded before the timed region
+        ks, vs, kd, vd = self._draw_new(B)
         qs = [self._draw((B, self.n_q, self.d), 1.0 / math.sqrt(self.d)) for _ in range(self.n_layers)]
-        q_dev = [self._dev(x) for x in qs]  # uploaded before the timed calls
+        q_dev = [self._dev(x) for x in qs]
         s = self.cache.stream()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        out = None
-        for layer in range(self.n_layers):
-            out = self.cache.decode(layer, q_dev[layer], batch, self.plan)
-        e1.record(s)
+        if self.graph_mode:
+            rec = self._step_graph(B, slab_ids, kd, vd, q_dev, e0, e1)
+            out = (self._o_buf[-1][:B], self._lse_buf[-1][:B])
+        else:
+            self._sync_cold()
+            e0.record(s)
+            t_issue = time.perf_counter()
+            self.cache.append([1] * B, kd, vd)
+            batch = self.cache.batch(slab_ids, [r["len"] for r in self.rows])
+            t0 = time.perf_counter()
+            self.ctx.dispatch(batch, self.plan)
+            t_disp = time.perf_counter() - t0
+            out = None
+            for layer in range(self.n_layers):
+                out = self.cache.decode(layer, q_dev[layer], batch, self.plan)
+            t_host = time.perf_counter() - t_issue
+            e1.record(s)
+            rec = {"dispatch_us": t_disp * 1e6, "host_us": t_host * 1e6, "mode": "eager"}
+        self._keep_new([1] * B, ks, vs)
         self._events.append((e0, e1))
         groups = self.plan.groups()
-        self.trace.append({"B": B, "dispatch_us": t_disp * 1e6,
-                           "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
-                                       "n_splits": g["n_splits"]} for g in groups]})
+        rec.update({"B": B, "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
+                                        "n_splits": g["n_splits"]} for g in groups]})
+        self.trace.append(rec)
         if self.keep:
             self.last_q = qs
         self.last_out = out
         return out
+
+    def _step_graph(self, B, slab_ids, kd, vd, q_dev, e0, e1) -> Dict:
+        """The step as one CUDA-graph replay; re-plan and capture when the batch changed or a
+        request would outgrow its planned length."""
+        s = self.cache.stream()
+        for layer in range(self.n_layers):
+            self._k_buf[layer][:B].copy_(kd[layer])
+            self._v_buf[layer][:B].copy_(vd[layer])
+            self._q_buf[layer][:B].copy_(q_dev[layer])
+        lens = [r["len"] for r in self.rows]  # after this step's token
+        key = (B, tuple(slab_ids))
+        if self._graph is not None and key == self._graph_key and all(
+                n <= m for n, m in zip(lens, self._planned)):
+            e0.record(s)
+            t0 = time.perf_counter()
+            self._graph.replay()
+            t_host = time.perf_counter() - t0
+            e1.record(s)
+            self._cold_dirty = True
+            for b in range(B):
+                self.cache.seq_len_host[b] += 1
+            return {"dispatch_us": 0.0, "host_us": t_host * 1e6, "mode": "replay"}
+        # re-plan for the lengths plus a headroom, run this step eagerly (uploading the plan),
+        # then capture the same calls for the steps to come
+        self._sync_cold()
+        self._planned = [min(self.cache.cap, n + self.headroom) for n in lens]
+        batch = gb.Batch(slab_ids, self._planned, self.cache.req_to_slot, self.cache.cap,
+                         seq_len_dev=self.cache.suffix_len)
+        self._graph_batch = batch  # keeps the host arrays the captured calls point to alive
+        t0 = time.perf_counter()
+        self.ctx.dispatch(batch, self.plan)
+        t_disp = time.perf_counter() - t0
+        ws = self.cache.workspace(self.plan)
+
+        def issue():
+            self.ctx.cold_alloc_uniform(1, B, self.cache.req_to_slot, self.cache.suffix_len, self.cache.cap,
+                                        self._slots_buf, torch.cuda.current_stream(self.dev))
+            for layer in range(self.n_layers):
+                self.ctx.cold_append(layer, self._k_buf[layer], self._v_buf[layer], self._slots_buf, B,
+                                     torch.cuda.current_stream(self.dev))
+            for layer in range(self.n_layers):
+                self.ctx.decode_attention(layer, self._q_buf[layer], batch, self.plan, self._o_buf[layer],
+                                          self._lse_buf[layer], ws, ws.numel(), torch.cuda.current_stream(self.dev))
+
+        e0.record(s)
+        t1 = time.perf_counter()
+        issue()
+        t_host = time.perf_counter() - t1
+        e1.record(s)
+        for b in range(B):
+            self.cache.seq_len_host[b] += 1
+        self.ctx.cold_sync(s)  # host ring position exact before the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):  # on torch's capture stream
+            issue()  # recorded, not run
+        self._graph, self._graph_key = g, key
+        self._cold_dirty = True  # the capture moved the host's copy as if it had run
+        return {"dispatch_us": t_disp * 1e6, "host_us": t_host * 1e6, "mode": "capture"}
 
     def finish_trace(self) -> List[Dict]:
         """Fill in each step's GPU time (synchronises)."""
@@ -181,13 +290,13 @@ class DecodeDriver:
 
 def run(*, steps: int = 64, n_layers: int = 2, prefix_lens=(16384, 4096), start_batch: int = 48,
         p_arrive: float = 0.25, p_complete: float = 0.02, prompt=(64, 512), seed: int = 0,
-        max_batch: int = 256) -> Dict:
+        max_batch: int = 256, graph: bool = False, headroom: int = 16) -> Dict:
     """Seeded arrival/completion schedule: each step, with probability p_arrive a request arrives
     (uniform prefix, uniform prompt length in `prompt`), and every active request completes with
     probability p_complete."""
     sched = np.random.default_rng(seed + 1)
     drv = DecodeDriver(prefix_lens=prefix_lens, n_layers=n_layers, max_batch=max_batch,
-                       cap=max(prompt) + steps + 64, seed=seed)
+                       cap=max(prompt) + steps + headroom + 64, seed=seed, graph=graph, headroom=headroom)
     for i in range(start_batch):
         drv.arrive(int(sched.integers(len(prefix_lens))), int(sched.integers(prompt[0], prompt[1] + 1)))
     for _ in range(steps):
@@ -202,12 +311,21 @@ def run(*, steps: int = 64, n_layers: int = 2, prefix_lens=(16384, 4096), start_
     n_dense = sum(1 for t in trace for g in t["groups"] if g["backend"] == "dense")
     gpu = [t["gpu_us"] for t in trace]
     disp = [t["dispatch_us"] for t in trace]
-    return {"steps": steps, "layers": n_layers, "B_min": min(t["B"] for t in trace),
-            "B_max": max(t["B"] for t in trace), "dense_fraction": n_dense / max(1, n_groups),
-            "gpu_us_per_step_median": statistics.median(gpu),
-            "dispatch_us_median": statistics.median(disp),
-            "dispatch_share_of_step": statistics.median(d / g for d, g in zip(disp, gpu)),
-            "trace": trace}
+    host = [t["host_us"] for t in trace]
+    out = {"steps": steps, "layers": n_layers, "graph": graph, "B_min": min(t["B"] for t in trace),
+           "B_max": max(t["B"] for t in trace), "dense_fraction": n_dense / max(1, n_groups),
+           "gpu_us_per_step_median": statistics.median(gpu),
+           "host_us_per_step_median": statistics.median(host),
+           "host_share_of_step": statistics.median(h / g for h, g in zip(host, gpu)),
+           "dispatch_us_median": statistics.median(disp),
+           "dispatch_share_of_step": statistics.median(d / g for d, g in zip(disp, gpu))}
+    modes = {}
+    for t in trace:
+        modes.setdefault(t["mode"], []).append(t["host_us"])
+    out["steps_by_mode"] = {m: len(v) for m, v in modes.items()}
+    out["host_us_median_by_mode"] = {m: statistics.median(v) for m, v in modes.items()}
+    out["trace"] = trace
+    return out
 
 
 def main(argv=None):
@@ -216,8 +334,13 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--trace", action="store_true", help="print every step")
+    ap.add_argument("--graph", action="store_true", help="replay each step from a CUDA graph")
+    ap.add_argument("--headroom", type=int, default=16, help="tokens a graph's plan allows per request")
+    ap.add_argument("--p-arrive", type=float, default=0.25, help="chance of an arrival per step")
+    ap.add_argument("--p-complete", type=float, default=0.02, help="chance per request of completing per step")
     a = ap.parse_args(argv)
-    res = run(steps=a.steps, n_layers=a.layers, seed=a.seed)
+    res = run(steps=a.steps, n_layers=a.layers, seed=a.seed, graph=a.graph, headroom=a.headroom,
+              p_arrive=a.p_arrive, p_complete=a.p_complete)
     trace = res.pop("trace")
     if a.trace:
         for i, t in enumerate(trace):

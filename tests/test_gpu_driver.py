@@ -42,3 +42,47 @@ def test_driver_churn_matches_oracle(cuda_ok):
                                        V[:, j].astype(np.float64), scale)
             assert np.max(np.abs(o[b, h] - o_ref)) <= 1e-2, (b, h)
             assert abs(lse[b, h] - lse_ref) <= 1e-3, (b, h)
+
+
+def test_driver_graph_replay_matches_oracle(cuda_ok):
+    """The step captured in a CUDA graph and replayed (slot allocation, K/V scatter and attention
+    of both layers), with a plan made for a small headroom so that it is re-captured as
+    requests outgrow it and whenever the batch changes; the last layer's attention of every
+    active request equals the oracle's."""
+    from shared_prefix_kv_decode_gb300.decode_driver import DecodeDriver
+
+    n_q, n_kv, d, layers = 32, 8, 128, 2
+    drv = DecodeDriver(prefix_lens=[900, 300], n_layers=layers, n_q=n_q, n_kv=n_kv, head_dim=d, max_batch=64,
+                       cap=512, n_slots=40000, seed=4, keep_logical=True, graph=True, headroom=4)
+    sched = np.random.default_rng(8)
+    for i in range(12):
+        drv.arrive(i % 2, int(sched.integers(1, 150)))
+    for step in range(18):
+        if step in (6, 13):  # churn between quiet stretches
+            drv.complete(int(sched.integers(drv.B)))
+            drv.arrive(int(sched.integers(2)), int(sched.integers(1, 150)))
+        drv.step()
+    trace = drv.finish_trace()
+    modes = [t["mode"] for t in trace]
+    assert modes.count("replay") >= 8 and modes.count("capture") >= 3, modes
+    assert all(t["gpu_us"] > 0 for t in trace)
+    o, lse = drv.last_out
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    q = drv.last_q[layers - 1]
+    scale = OA.softmax_scale(d)
+    for b in range(drv.B):
+        K, V = drv.logical_kv(b, layers - 1)
+        for h in range(n_q):
+            j = OA.kv_head(h, n_q, n_kv)
+            o_ref, lse_ref = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
+                                       V[:, j].astype(np.float64), scale)
+            assert np.max(np.abs(o[b, h] - o_ref)) <= 1e-2, (b, h)
+            assert abs(lse[b, h] - lse_ref) <= 1e-3, (b, h)
+    # once synchronised, the ring position the graph moved on the device accounts for every
+    # token the active requests hold (completed requests gave theirs back; prefixes are in HOT)
+    drv._sync_cold()
+    held = sum(r["len"] for r in drv.rows)
+    assert held == sum(drv.cache.seq_len_host[:drv.B])
+    n_cold = 40000 - drv.cache.n_hot
+    assert drv.cache.ctx.cold_free_count() == n_cold - held
