@@ -321,7 +321,7 @@ granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int32_t layer, 
  *   ws:  device workspace of granikv_prefill_workspace_size(L_p) bytes, 256-byte aligned
  * L_p is the slab's length.  Runs on the tensor-core dense kernel alone (one CTA per 128 query
  * rows and KV head, keys up to the rows' diagonal, o and lse written directly).
- * GRANIKV_ERR_UNSUPPORTED unless the dtype is bf16, head_dim is 128 and n_q/n_kv divides 128. */
+ * GRANIKV_ERR_UNSUPPORTED unless the dtype is bf16 and head_dim is 128. */
 granikv_status granikv_prefill_attention(granikv_ctx* ctx, int32_t layer, int32_t slab_id,
                                          const void* k_new, const void* v_new, const void* q, void* o,
                                          float* lse, void* workspace, size_t ws_bytes,

@@ -16,7 +16,7 @@
 // Every MMA is 128x128x16, so one issuing thread keeps the tensor core fed.
 // The same CTA runs the causal prefill of a slab (a group flagged causal): its "requests" are the
 // slab's own tokens, row r is token r/g, the CTA reads keys only up to its block's last token,
-// and each row masks the keys after its own token in the diagonal tile.
+// and each row masks the keys after its own token in the tiles at the diagonal.
 // Roles:
 //  * warps 0-7, softmax and epilogue: warp w serves TMEM lanes 32*(w%4).. (row r = lane r) and
 //    column half w/4 of each tile.  The two warps of a row quarter swap their half-row maxima
@@ -122,9 +122,10 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   int32_t t0, t1;
   piece_range(gr, it.split, t0, t1);
   // causal prefill: row r is token r/g of the slab and sees keys [0, r/g], so the block's last
-  // token ends the keys this CTA reads (g divides 128, so a block's tokens lie in one tile)
+  // token ends the keys this CTA reads.  Every row sees key 0 in the first tile; a later tile
+  // in which all of a row's keys lie past its token only adds zero weights.
   const bool causal = gr.causal != 0;
-  if (causal) t1 = min(t1, (it.row_block * kM + kM) / g);
+  if (causal) t1 = min(t1, (it.row_block * kM + kM - 1) / g + 1);
   const int n_tiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
   // Q by TMA when the group's requests are consecutive in the batch: the row block is then a

@@ -1130,8 +1130,7 @@ granikv_status granikv_prefill_attention(granikv_ctx* c, int32_t layer, int32_t 
   if ((k_new == nullptr) != (v_new == nullptr)) return GRANIKV_ERR_INVALID;
   if ((uintptr_t)ws % 256) return GRANIKV_ERR_INVALID;
   if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
-  if (c->cfg.dtype != GRANIKV_DTYPE_BF16 || c->cfg.head_dim != 128 || kDenseRows % c->g != 0 || !c->has_tmaps)
-    return GRANIKV_ERR_UNSUPPORTED;
+  if (c->cfg.dtype != GRANIKV_DTYPE_BF16 || c->cfg.head_dim != 128 || !c->has_tmaps) return GRANIKV_ERR_UNSUPPORTED;
   const int32_t L_p = c->slabs[sid].len;
   const PrefillLayout lay = prefill_layout(c, L_p);
   if (ws_bytes < lay.total) return GRANIKV_ERR_INVALID;

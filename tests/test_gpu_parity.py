@@ -271,6 +271,55 @@ def test_cold_free_returns_slots_fifo(cuda_ok):
     cache.ctx.sync_status()
 
 
+def test_cold_alloc_uniform_follows_the_ring(cuda_ok):
+    """The graph-safe allocation (ring position kept on the device) takes exactly the slots the
+    oracle's FIFO ring gives, mixed with the host-driven allocation and frees; when too few are
+    free it pops nothing and reports a device check."""
+    import torch
+    gb = _gb()
+    from shared_prefix_kv_decode_gb300.cache import GraniKVCache
+    order = [int(x) for x in np.random.default_rng(3).permutation(np.arange(20, 100))]
+    cache = GraniKVCache(n_layers=1, n_q=8, n_kv=2, head_dim=64, dtype=gb.DTYPE_F32, n_slots=100,
+                         max_batch=4, cap=64, cold_init_order=order)
+    ring = AL.ColdRing(order)
+    tables = [[], [], [], []]
+    s = cache.stream()
+    k = torch.zeros((40, 2, 64), device="cuda")
+    slots = torch.zeros((16,), dtype=torch.int32, device="cuda")
+    cache.append([3, 0, 5, 1], [k[:9]], [k[:9]])
+    ring.alloc([3, 0, 5, 1], tables)
+    for n in (1, 2, 1):
+        cache.ctx.cold_alloc_uniform(n, 4, cache.req_to_slot, cache.suffix_len, cache.cap, slots, s)
+        want = ring.alloc([n] * 4, tables)
+        assert slots[:4 * n].cpu().tolist() == want
+    cache.ctx.cold_sync(s)
+    assert cache.ctx.cold_free_count() == ring.n_free
+    # frees after device-side allocations, then both kinds again
+    cache.ctx.cold_free(torch.tensor(tables[2][:4], dtype=torch.int32, device="cuda"), 4, s)
+    ring.free(tables[2][:4])
+    cache.ctx.cold_alloc_uniform(1, 3, cache.req_to_slot, cache.suffix_len, cache.cap, slots, s)
+    ring.alloc([1, 1, 1, 0], tables)
+    cache.ctx.cold_sync(s)
+    cache.append([2, 2, 0, 0], [k[:4]], [k[:4]])
+    ring.alloc([2, 2, 0, 0], tables)
+    got = cache.req_to_slot.cpu().numpy()
+    lens = cache.suffix_len.cpu().tolist()
+    for b in range(4):
+        assert lens[b] == len(tables[b]) and list(got[b, :lens[b]]) == tables[b], b
+    cache.ctx.cold_sync(s)
+    assert cache.ctx.cold_free_count() == ring.n_free
+    # asking for more than is free: nothing popped, the device check is reported
+    free = ring.n_free
+    big = free // 4 + 1
+    before = cache.req_to_slot.clone(), cache.suffix_len.clone()
+    cache.ctx.cold_alloc_uniform(big, 4, cache.req_to_slot, cache.suffix_len, cache.cap, None, s)
+    with pytest.raises(gb.DeviceCheckFailed):
+        cache.ctx.sync_status(s)
+    cache.ctx.cold_sync(s)
+    assert cache.ctx.cold_free_count() == free
+    assert torch.equal(cache.req_to_slot, before[0]) and torch.equal(cache.suffix_len, before[1])
+
+
 FULL = {
     "llama8b_single_prefix_16k": (W.llama8b_single_prefix_16k, [0, 17, 40, 63]),
     "hetero_multi_prefix_k8": (W.hetero_multi_prefix_k8, [0, 31, 77, 159]),

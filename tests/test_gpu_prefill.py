@@ -62,7 +62,8 @@ def test_prefill_llama_heads(cuda_ok, L_p):
     _run(32, 8, L_p, 1.0 / math.sqrt(128), seed=L_p)
 
 
-@pytest.mark.parametrize("n_q,n_kv,L_p", [(64, 8, 300), (8, 8, 260), (16, 8, 517), (32, 2, 400)])
+@pytest.mark.parametrize("n_q,n_kv,L_p", [(64, 8, 300), (8, 8, 260), (16, 8, 517), (32, 2, 400),
+                                         (40, 8, 611), (24, 8, 300), (56, 8, 129)])
 def test_prefill_group_sizes(cuda_ok, n_q, n_kv, L_p):
     _run(n_q, n_kv, L_p, 1.0, seed=n_q + L_p)
 
@@ -79,14 +80,21 @@ def test_prefill_full_size_sampled(cuda_ok):
     _run(32, 8, 16384, 1.0 / math.sqrt(128), seed=2, tokens=toks)
 
 
-def test_prefill_refuses_unsupported_group(cuda_ok):
+def test_prefill_qwen_shape_full_size_sampled(cuda_ok):
+    # 40/8 heads: g = 5 does not divide the 128-row block, so blocks straddle tokens and tiles
+    rng = np.random.default_rng(4)
+    toks = sorted(set([0, 1, 25, 26, 127, 128, 8191] + [int(x) for x in rng.integers(0, 8192, size=12)]))
+    _run(40, 8, 8192, 1.0 / math.sqrt(128), seed=5, tokens=toks)
+
+
+def test_prefill_refuses_unsupported(cuda_ok):
     import torch
     from shared_prefix_kv_decode_gb300 import _binding as gb
     from shared_prefix_kv_decode_gb300.cache import GraniKVCache
-    cache = GraniKVCache(n_layers=1, n_q=40, n_kv=8, head_dim=D, dtype=gb.DTYPE_BF16, n_slots=4096,
+    cache = GraniKVCache(n_layers=1, n_q=8, n_kv=2, head_dim=64, dtype=gb.DTYPE_F32, n_slots=4096,
                          max_batch=4, cap=16)
     sid, _ = cache.ctx.hot_alloc(100)
-    q = torch.zeros((100, 40, D), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((100, 8, 64), dtype=torch.float32, device="cuda")
     with pytest.raises(gb.GranikvError) as ei:
         cache.prefill(0, sid, q)
     assert ei.value.status == gb.ERR_UNSUPPORTED
