@@ -10,8 +10,7 @@
 // Per 128-token tile i:
 //     S(i) = Q K(i)^T   (M=128, N=128, K=128: 8 tcgen05.mma from shared memory, fp32 in TMEM)
 //     P(i) = 2^(S(i)*scale*log2e - m)   (softmax warps; bf16, written back over S(i) in TMEM;
-//            two columns per packed f32x2 operation, a third of the exponentials as a polynomial
-//            on the FMA pipe and the rest on MUFU, so the two units share the load)
+//            scale and shift two columns per packed f32x2 operation, exponentials on MUFU)
 //     O   += P(i) V(i)  (M=128, N=128, K=128: 8 tcgen05.mma with A = P(i) read from TMEM)
 // Every MMA is 128x128x16, so one issuing thread keeps the tensor core fed.
 // The same CTA runs the causal prefill of a slab (a group flagged causal): its "requests" are the
@@ -425,23 +424,18 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         tmem_wait_st();
       }
       // P = 2^(s*scale - m) for this half's 64 columns, packed two per 32-bit column and written
-      // over columns [32*half, 32*half + 32) of the S(i) buffer (both halves have read S(i))
-      // two columns per packed f32x2 operation; a third of the exponentials on the FMA pipe
-      // (polynomial), the rest on MUFU, which balances the two units' issue
+      // over columns [32*half, 32*half + 32) of the S(i) buffer (both halves have read S(i)).
+      // Every exponential goes to MUFU: moving a share of them to a polynomial on the FMA pipe
+      // made the tile slower on this GPU (the extra instructions cost more than MUFU time saved)
       const uint64_t scale2 = f2_pack(scale, scale), nm2 = f2_pack(-m_used, -m_used);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial row sums (0.0f bit patterns)
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const uint64_t x = f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), scale2, nm2);
-        uint64_t e;
-        if (k % 3 == 2) {
-          e = ex2_poly3_x2(x);
-        } else {
-          float xa, xb;
-          f2_unpack(x, xa, xb);
-          e = f2_pack(ex2_approx(xa), ex2_approx(xb));
-        }
+        float xa, xb;
+        f2_unpack(x, xa, xb);
+        const uint64_t e = f2_pack(ex2_approx(xa), ex2_approx(xb));
         acc[k & 3] = f2_add(acc[k & 3], e);
         float a, b;
         f2_unpack(e, a, b);

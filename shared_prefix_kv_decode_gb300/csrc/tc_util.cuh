@@ -197,11 +197,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 // three-input maximum (sm_100 family)
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
@@ -214,44 +209,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x for two packed floats on the FMA and integer pipes, for x <= 126 (x below -126 is clamped there, giving a
-// value below 2^-126, i.e. zero for the sums it enters).  Range reduction 2^x = 2^j * 2^f with
-// j = rint(x): adding 1.5 * 2^23 rounds x to an integer that then sits in the low mantissa
-// bits of the sum, and shifting those bits left by 23 adds j to the exponent field of 2^f
-// (the exponent-field construction of Schraudolph, "A fast, compact approximation of the
-// exponential function", Neural Computation 11(4), 1999).  2^f on [-1/2, 1/2] is a cubic
-// minimax fit in relative error (max 7.5e-5 in f32 arithmetic; exp2_poly_fit.py derives the
-// coefficients by linear programming).
-__device__ __forceinline__ uint64_t ex2_poly3_x2(uint64_t x2) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  float xa, xb;
-  f2_unpack(x2, xa, xb);
-  const uint64_t x = f2_pack(fmaxf(xa, -126.0f), fmaxf(xb, -126.0f));
-  const uint64_t t = f2_add(x, f2_pack(kRound, kRound));
-  const uint64_t f = f2_sub(x, f2_sub(t, f2_pack(kRound, kRound)));
-  uint64_t q = f2_fma(f2_pack(0.05517224967479706f, 0.05517224967479706f), f,
-                      f2_pack(0.24261115491390228f, 0.24261115491390228f));
-  q = f2_fma(q, f, f2_pack(0.6932608485221863f, 0.6932608485221863f));
-  q = f2_fma(q, f, f2_pack(0.9999281167984009f, 0.9999281167984009f));
-  float qa, qb, ta, tb;
-  f2_unpack(q, qa, qb);
-  f2_unpack(t, ta, tb);
-  return f2_pack(__int_as_float(__float_as_int(qa) + (__float_as_int(ta) << 23)),
-                 __int_as_float(__float_as_int(qb) + (__float_as_int(tb) << 23)));
-}
-
-// the same for one float
-__device__ __forceinline__ float ex2_poly3(float x) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  x = fmaxf(x, -126.0f);
-  const float t = __fadd_rn(x, kRound);
-  const float f = __fsub_rn(x, __fsub_rn(t, kRound));
-  float q = fmaf(0.05517224967479706f, f, 0.24261115491390228f);
-  q = fmaf(q, f, 0.6932608485221863f);
-  q = fmaf(q, f, 0.9999281167984009f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
 }
 
 }  // namespace granikv
