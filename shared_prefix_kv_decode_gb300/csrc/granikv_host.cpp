@@ -649,7 +649,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       // Automatic split: the piece length whose prefix time (one wave: the longest piece) and
       // suffix time (its work spread over the SMs the prefix CTAs leave) are most nearly equal,
       // i.e. the smallest max of the two.  Costs measured on GB300: a prefix CTA 5 us plus, per
-      // 128-query-row block and token, 0.01 us (dense) or 0.02 us (cascade); the suffix 1.40
+      // 128-query-row block and token, 0.0078 us (dense) or 0.02 us (cascade); the suffix 1.40
       // SM-us per 16 COLD tokens of one group of up to 8 KV heads.
       // The split is also weighed against running the two one after another on all SMs, with
       // the suffix then bound by the bandwidth HBM gives its random 2 KB row reads (about
@@ -665,7 +665,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
         double t_p = 0.0;
         for (int32_t i = 0; i < G; ++i) {
           const int64_t tile = tile_tokens_for(groups[i].impl);
-          const double per_token = groups[i].impl == kImplDenseTc ? 0.01 : 0.02;
+          const double per_token = groups[i].impl == kImplDenseTc ? 0.0078 : 0.02;
           t_p = std::max(t_p, 5.0 + per_token * (double)std::min<int64_t>(cand * tile, groups[i].L_p));
         }
         return t_p;
