@@ -61,6 +61,8 @@ def parse_args(argv=None):
                     help="share of the SMs the prefix work list is sized for when running concurrently "
                          "(0: the library's automatic share)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused-append", action="store_true",
+                    help="append each layer's new K/V with its own launch before the attention call")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=WORKLOAD,
                     help="full-size configuration to time (default: the headline one)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -373,6 +375,8 @@ def run_granikv(args):
     ws_bytes = ctx.workspace_size(ctx.dispatch(probe, plan))
     ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
     ones = [1] * B
+    # the COLD append fused into the attention launches where the tensor-core suffix kernel runs
+    fused = (not args.no_fused_append and spec.dtype == "bf16" and spec.d == 128 and spec.n_q // spec.n_kv <= 8)
     ev_pairs = []
     timed_bytes = []
 
@@ -381,8 +385,9 @@ def run_granikv(args):
         ctx.cold_alloc(ones, cache.req_to_slot, cache.suffix_len, cache.cap, slots, stream)
         for i in range(B):
             seq[i] += 1
-        for layer in range(L):
-            ctx.cold_append(layer, bset["k"][layer], bset["v"][layer], slots, B, stream)
+        if not fused:
+            for layer in range(L):
+                ctx.cold_append(layer, bset["k"][layer], bset["v"][layer], slots, B, stream)
         batch = gb.Batch(slab_ids, seq, cache.req_to_slot, cache.cap)
         ctx.dispatch(batch, plan)
         nbytes = algorithmic_bytes(spec, slab_ids, seq, 2)
@@ -393,8 +398,12 @@ def run_granikv(args):
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
         for layer in range(L):
-            ctx.decode_attention(layer, bset["q"][layer], batch, plan, bset["o"][layer], bset["lse"][layer], ws,
-                                 ws_bytes, stream)
+            if fused:  # the layer's new K/V are written to their slots by the attention launch
+                ctx.decode_attention_append(layer, bset["q"][layer], bset["k"][layer], bset["v"][layer], batch, plan,
+                                            bset["o"][layer], bset["lse"][layer], ws, ws_bytes, stream)
+            else:
+                ctx.decode_attention(layer, bset["q"][layer], batch, plan, bset["o"][layer], bset["lse"][layer], ws,
+                                     ws_bytes, stream)
         if record:
             e1.record(stream)
             ev_pairs.append((e0, e1))
@@ -497,6 +506,7 @@ def run_granikv(args):
                    "L_p": spec.prefix_lens[0] if len(spec.prefix_lens) == 1 else list(spec.prefix_lens), "B": B,
                    "suffix": WORKLOADS[args.workload][1],
                    "layers_per_step": L, "backend": args.backend,
+                   "append": "fused into the attention launch" if fused else "own launch per layer",
                    "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                "n_splits": g["n_splits"]} for g in groups],

@@ -286,6 +286,19 @@ granikv_status granikv_decode_attention(granikv_ctx* ctx, int32_t layer, const v
                                         void* o, float* lse, void* workspace, size_t ws_bytes,
                                         granikv_stream_t stream);
 
+/* granikv_decode_attention with this step's COLD append fused in: row b of k_new and v_new
+ * (device [B, n_kv, head_dim], 16-byte aligned) is the K and V of request b's newest token,
+ * the last one of its COLD list (req_to_slot[b, n-1] with n = seq_len_dev[b] when given, else
+ * seq_len[b]; its slot allocated already, e.g. by granikv_cold_alloc).  The call attends with
+ * those rows and writes them to that slot of this layer's pools, so it equals granikv_cold_append
+ * of the rows followed by granikv_decode_attention, one launch fewer.  GRANIKV_ERR_INVALID if a
+ * request has no COLD token; GRANIKV_ERR_UNSUPPORTED unless the plan's suffix runs on the
+ * tensor-core kernel (bf16, head_dim 128, n_q/n_kv <= 8). */
+granikv_status granikv_decode_attention_append(granikv_ctx* ctx, int32_t layer, const void* q,
+                                               const void* k_new, const void* v_new,
+                                               const granikv_batch* batch, granikv_plan* plan, void* o,
+                                               float* lse, void* workspace, size_t ws_bytes,
+                                               granikv_stream_t stream);
 /* Decode attention without a caller workspace.  The paper has no counterpart: this is for
  * callers that cannot allocate device memory for a workspace, such as a serving engine that has
  * already reserved nearly all of the GPU's memory for its own pools and allocator, or a plain C

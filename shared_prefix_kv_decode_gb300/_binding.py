@@ -133,6 +133,9 @@ _SIGNATURES = [
     ("granikv_decode_attention", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
                                              C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                              C.c_size_t, C.c_void_p]),
+    ("granikv_decode_attention_append", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                                    C.POINTER(_Batch), C.c_void_p, C.c_void_p, C.c_void_p,
+                                                    C.c_void_p, C.c_size_t, C.c_void_p]),
     ("granikv_decode_attention_static", C.c_int32, [C.c_void_p, C.c_int32, C.c_void_p, C.POINTER(_Batch),
                                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     ("granikv_prefill_attention", C.c_int32, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
@@ -451,6 +454,13 @@ class Context:
                                                   plan.handle if plan is not None else None, _ptr(o),
                                                   _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
                "granikv_decode_attention")
+
+    def decode_attention_append(self, layer: int, q, k_new, v_new, batch: Batch, plan: Optional[Plan], o, lse,
+                                workspace, ws_bytes: int, stream=None):
+        _check(self._lib.granikv_decode_attention_append(self.handle, layer, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                                         C.byref(batch.c), plan.handle if plan else None, _ptr(o),
+                                                         _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
+               "granikv_decode_attention_append")
 
     def decode_attention_static(self, layer: int, q, batch: Batch, plan: Plan, o, lse, stream=None):
         """Decode attention on the library's built-in workspace (no caller workspace, nothing

@@ -944,10 +944,14 @@ granikv_status granikv_force_backend(granikv_ctx* c, int32_t backend) {
 
 // ---- decode attention -----------------------------------------------------------------------
 
-granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const void* q,
-                                        const granikv_batch* bt, granikv_plan* p, void* o,
-                                        float* lse, void* ws, size_t ws_bytes,
-                                        granikv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Decode attention of one layer; with k_new/v_new, each request's last COLD token is taken from
+// them and written to its slot by the same launches (the fused COLD append).
+granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* q, const void* k_new,
+                                     const void* v_new, const granikv_batch* bt, granikv_plan* p, void* o,
+                                     float* lse, void* ws, size_t ws_bytes, granikv_stream_t stream) {
   if (!c || !bt || !q || !o || !lse || !ws) return GRANIKV_ERR_INVALID;
   if (layer < 0 || layer >= c->cfg.n_layers) return GRANIKV_ERR_INVALID;
   if (!has_device(c)) return GRANIKV_ERR_NO_DEVICE;
@@ -964,6 +968,14 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   }
   if (!p->valid || p->ctx != c || p->B != bt->B) return GRANIKV_ERR_INVALID;
   if (ws_bytes < workspace_bytes(c, p)) return GRANIKV_ERR_INVALID;
+  if (k_new) {
+    // the fused append lives in the tensor-core suffix kernel (its bulk copies read the rows,
+    // which must start on 16-byte boundaries), and every request needs a token
+    if (!v_new || ((uintptr_t)k_new | (uintptr_t)v_new) % 16) return GRANIKV_ERR_INVALID;
+    if (p->suffix_impl != kImplSuffixMma) return GRANIKV_ERR_UNSUPPORTED;
+    for (int32_t b = 0; b < bt->B; ++b)
+      if (bt->seq_len[b] < 1) return GRANIKV_ERR_INVALID;
+  }
 
   DeviceGuard dg(c->cfg.device);
   cudaStream_t s = (cudaStream_t)stream;
@@ -1013,6 +1025,8 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   a.inject_stall = c->inject_stall;
   c->inject_stall = 0;
   a.live_len = bt->seq_len_dev;
+  a.k_new = k_new;
+  a.v_new = v_new;
   CUtensorMap tmq{};
   a.q_tma = 0;
   if (p->pitem_count[kImplDenseTc] > 0 && c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128)
@@ -1087,6 +1101,25 @@ granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const voi
   }
   if (e == cudaErrorNotSupported) return GRANIKV_ERR_UNSUPPORTED;
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+granikv_status granikv_decode_attention(granikv_ctx* c, int32_t layer, const void* q,
+                                        const granikv_batch* bt, granikv_plan* p, void* o,
+                                        float* lse, void* ws, size_t ws_bytes,
+                                        granikv_stream_t stream) {
+  return decode_attention_impl(c, layer, q, nullptr, nullptr, bt, p, o, lse, ws, ws_bytes, stream);
+}
+
+granikv_status granikv_decode_attention_append(granikv_ctx* c, int32_t layer, const void* q, const void* k_new,
+                                               const void* v_new, const granikv_batch* bt, granikv_plan* p,
+                                               void* o, float* lse, void* ws, size_t ws_bytes,
+                                               granikv_stream_t stream) {
+  if (!k_new || !v_new) return GRANIKV_ERR_INVALID;
+  return decode_attention_impl(c, layer, q, k_new, v_new, bt, p, o, lse, ws, ws_bytes, stream);
 }
 
 // ---- prefill of a HOT slab ------------------------------------------------------------------

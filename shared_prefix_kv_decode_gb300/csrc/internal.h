@@ -114,6 +114,8 @@ struct AttnParams {
   int32_t fused_merge;    // 1: the last producer of a row merges it (no merge kernel)
   int32_t q_tma;          // 1: the q tensor map passed to the dense kernel is valid
   int32_t inject_stall;   // test hook: suffix token-CTA 0 withholds its first tile (see header)
+  const void* k_new;        // [B, n_kv, d] or NULL: K of each request's last COLD token, read from
+  const void* v_new;        // here (not the pool) and written to its slot by the suffix CTA
   const int32_t* live_len;  // [B] device token counts that end each request's suffix segments early
                             // (the plan may cover more tokens than exist yet); NULL: the plan's
 };

@@ -56,7 +56,8 @@ constexpr int kOffSlots = kStages * kStageBytes;
 constexpr int kSlotBytes = kSuffixMaxCtaTokens * 4;  // the CTA's slot ids, loaded once
 constexpr int kSegSmem = 256;                      // segment descriptors staged in shared memory
 constexpr int kOffSegs = kOffSlots + kSlotBytes;
-constexpr int kOffBar = kOffSegs + kSegSmem * (int)sizeof(DevSuffixItem);
+constexpr int kOffNew = kOffSegs + kSegSmem * (int)sizeof(DevSuffixItem);  // newest token per segment
+constexpr int kOffBar = kOffNew + kSegSmem * 4;
 constexpr int kSmemBytes = kOffBar + 8 * 2 * kStages + 16;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kRowStride % 16 == 0 && kStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
@@ -115,6 +116,16 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     __syncthreads();
   }
   auto seg_at = [&](int k) { return k < kSegSmem ? sseg[k] : clamp(p.sitems[seg_begin + k]); };
+  // fused COLD append: each request's newest token (the last of its list) is read from
+  // k_new/v_new row b instead of the pool, and the consumer warps write it to its slot; the
+  // index of that token per segment is staged next to the descriptors
+  const bool fuse_new = p.k_new != nullptr;
+  int32_t* snew = reinterpret_cast<int32_t*>(smem + kOffNew);
+  auto newest_of = [&](int32_t b) { return (p.live_len ? p.live_len[b] : p.reqs[b].seq_len) - 1; };
+  if (fuse_new)
+    for (int k = threadIdx.x; k < min(n_seg, kSegSmem); k += blockDim.x) snew[k] = newest_of(p.sitems[seg_begin + k].b);
+  auto new_at = [&](int k) { return !fuse_new ? -1 : k < kSegSmem ? snew[k] : newest_of(p.sitems[seg_begin + k].b); };
+  const int64_t tok_bytes = (int64_t)p.n_kv * kRowBytes;
   int n_tok = 0;
   for (int sg = seg_begin; sg < seg_end; ++sg) {
     // from global memory: the staged copies are not complete before the barrier below
@@ -138,7 +149,6 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
 
   if (warp == kWarps) {
     // ---------------- producer: one bulk copy per token row (lanes 0-15 K, 16-31 V) -------
-    const int64_t tok_bytes = (int64_t)p.n_kv * kRowBytes;
     const bool is_v = lane >= kTile;
     const char* src_base = static_cast<const char*>(is_v ? p.vpool : p.kpool) + (int64_t)j0 * kRowBytes;
     const int r = lane & (kTile - 1);
@@ -147,8 +157,11 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     bool stop = false;
     // test hook: token-CTA 0 of group 0 withholds its first tile
     const bool skip0 = p.inject_stall != 0 && cta == 0 && group == 0;
+    const char* new_base =
+        fuse_new ? static_cast<const char*>(is_v ? p.v_new : p.k_new) + (int64_t)j0 * kRowBytes : nullptr;
     for (int sg = 0; sg < n_seg && !stop; ++sg) {
       const DevSuffixItem seg = seg_at(sg);
+      const int newest = new_at(sg);
       for (int t = seg.t0; t < seg.t1; t += kTile, ++n) {
         const int st = n % kStages;
         // every lane polls; the warp goes on only if all of them saw the phase complete
@@ -161,7 +174,9 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
         const void* src = g_zero_row;
         if (t + r < seg.t1) {
           const int32_t slot = sslot[pos + (t - seg.t0) + r];
-          if (slot >= p.n_hot && slot < p.n_slots)
+          if (t + r == newest)
+            src = new_base + (int64_t)seg.b * tok_bytes;
+          else if (slot >= p.n_hot && slot < p.n_slots)
             src = src_base + (int64_t)slot * tok_bytes;
           else
             latch_err(p.err, kDevBadSlot);
@@ -216,8 +231,12 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
   load_q(0);
   const uint32_t head_off = (uint32_t)warp * kRowBytes;
   int tile = 0;  // tiles consumed so far
+  int cpos = 0;  // position of the next segment's first token in sslot
   for (int sg = 0; sg < n_seg; ++sg) {
     const DevSuffixItem seg = seg_at(sg);
+    const int seg_pos = cpos;
+    cpos += seg.t1 - seg.t0;
+    const int newest = new_at(sg);
     uint32_t qf[8][2];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -295,6 +314,18 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
           uint32_t a0, a1, a2, a3;
           ldsm_x4_t(vst + r * kRowStride + (mt * 2 + (mi & 1)) * 16, a0, a1, a2, a3);
           mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      // fused append: the step's new token of this request is in this tile (it came from
+      // k_new/v_new); head j's K row (lanes 0-15) and V row (16-31) go from the tile to its slot.
+      // No CTA of this launch reads that slot.
+      if (newest >= t && newest < t + kTile && newest < seg.t1) {
+        const int32_t slot = sslot[seg_pos + (newest - seg.t0)];
+        if (slot >= p.n_hot && slot < p.n_slots) {
+          const uint32_t row = (lane < 16 ? kst : vst) + (uint32_t)(newest - t) * kRowStride + (lane & 15) * 16;
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + (row - sbase));
+          char* pool = static_cast<char*>(const_cast<void*>(lane < 16 ? p.kpool : p.vpool));
+          *reinterpret_cast<uint4*>(pool + (int64_t)slot * tok_bytes + (int64_t)j * kRowBytes + (lane & 15) * 16) = v;
         }
       }
       // this warp is done reading the stage

@@ -390,3 +390,76 @@ def test_single_request(cuda_ok, backend, lens):
     o, lse = _run(lw, backend)
     o_ref, lse_ref = OA.decode_attention(wl)
     assert_close(o, lse, o_ref, lse_ref, "bf16", f"single {lens} {backend}")
+
+
+@pytest.mark.parametrize("n_kv", [8, 16])
+def test_fused_append_equals_append_then_attention(cuda_ok, n_kv):
+    """granikv_decode_attention_append (the step's new K/V read by the suffix kernel and written
+    to their slots by it) gives bit for bit the o, lse and pools of granikv_cold_append followed
+    by granikv_decode_attention; also with a plan made for a headroom and the live lengths read
+    from the device."""
+    import torch
+    gb = _gb()
+    wl = W.small_mixed(2, dtype="bf16", n_q=32, n_kv=n_kv, q_scale=1.0)
+    lw = _load(wl)
+    cache, ctx, spec = lw.cache, lw.cache.ctx, wl.spec
+    B, s = spec.B, lw.cache.stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7)
+    kn = torch.randn((B, n_kv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    vn = torch.randn((B, n_kv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    slots = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ctx.cold_alloc([1] * B, cache.req_to_slot, cache.suffix_len, cache.cap, slots, s)
+    lens = [cache.seq_len_host[b] + 1 for b in range(B)]
+    pools0 = cache.k_pools[0].clone(), cache.v_pools[0].clone()
+    for headroom, live in ((0, None), (5, cache.suffix_len)):
+        batch = gb.Batch(lw.slab_ids, [n + headroom for n in lens], cache.req_to_slot, cache.cap, seq_len_dev=live)
+        plan = ctx.dispatch(batch)
+        ws = cache.workspace(plan)
+        outs = []
+        for fused in (True, False):
+            cache.k_pools[0].copy_(pools0[0])
+            cache.v_pools[0].copy_(pools0[1])
+            o = torch.empty((B, spec.n_q, 128), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((B, spec.n_q), dtype=torch.float32, device="cuda")
+            if fused:
+                ctx.decode_attention_append(0, lw.q, kn, vn, batch, plan, o, lse, ws, ws.numel(), s)
+            else:
+                ctx.cold_append(0, kn, vn, slots, B, s)
+                ctx.decode_attention(0, lw.q, batch, plan, o, lse, ws, ws.numel(), s)
+            ctx.sync_status(s)
+            outs.append((o.clone(), lse.clone(), cache.k_pools[0].clone(), cache.v_pools[0].clone()))
+        for a, b in zip(outs[0], outs[1]):
+            assert torch.equal(a, b), headroom
+    # refusals, before anything is launched
+    bad = gb.Batch(lw.slab_ids, [0] + lens[1:], cache.req_to_slot, cache.cap)
+    if lw.slab_ids[0] >= 0:
+        plan = ctx.dispatch(bad)
+        with pytest.raises(gb.GranikvError) as ei:
+            ctx.decode_attention_append(0, lw.q, kn, vn, bad, plan, o, lse, ws, ws.numel(), s)
+        assert ei.value.status == gb.ERR_INVALID
+    batch = gb.Batch(lw.slab_ids, lens, cache.req_to_slot, cache.cap)
+    plan = ctx.dispatch(batch)
+    flat = kn.view(-1)
+    with pytest.raises(gb.GranikvError) as ei:
+        ctx.decode_attention_append(0, lw.q, flat[1:1 + kn.numel() - 8], vn, batch, plan, o, lse, ws, ws.numel(), s)
+    assert ei.value.status == gb.ERR_INVALID
+
+
+def test_fused_append_needs_the_tensor_core_suffix(cuda_ok):
+    import torch
+    gb = _gb()
+    wl = W.small_mixed(0, dtype="f32", n_q=8, n_kv=2, d=64)
+    lw = _load(wl)
+    cache, ctx, spec = lw.cache, lw.cache.ctx, wl.spec
+    B, s = spec.B, cache.stream()
+    ctx.cold_alloc([1] * B, cache.req_to_slot, cache.suffix_len, cache.cap, None, s)
+    batch = gb.Batch(lw.slab_ids, [cache.seq_len_host[b] + 1 for b in range(B)], cache.req_to_slot, cache.cap)
+    plan = ctx.dispatch(batch)
+    ws = cache.workspace(plan)
+    kn = torch.zeros((B, 2, 64), device="cuda")
+    o = torch.empty((B, 8, 64), device="cuda")
+    lse = torch.empty((B, 8), device="cuda")
+    with pytest.raises(gb.GranikvError) as ei:
+        ctx.decode_attention_append(0, lw.q, kn, kn, batch, plan, o, lse, ws, ws.numel(), s)
+    assert ei.value.status == gb.ERR_UNSUPPORTED
