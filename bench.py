@@ -507,6 +507,7 @@ def run_granikv(args):
                    "suffix": WORKLOADS[args.workload][1],
                    "layers_per_step": L, "backend": args.backend,
                    "append": "fused into the attention launch" if fused else "own launch per layer",
+                   "schedule": plan.schedule(),
                    "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                "n_splits": g["n_splits"]} for g in groups],

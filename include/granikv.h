@@ -247,6 +247,11 @@ granikv_status granikv_plan_destroy(granikv_plan* plan);
 granikv_status granikv_dispatch(granikv_ctx* ctx, const granikv_batch* batch, granikv_plan* plan);
 granikv_status granikv_plan_num_groups(const granikv_plan* plan, int32_t* n_groups);
 granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_group_info* out);
+/* How the plan runs: concurrent = 1 when the prefix and suffix work share the GPU side by side
+ * (one grid, or two kernels on two streams), 0 when they run one after another; the number of
+ * prefix CTAs and of suffix CTAs it launches. */
+granikv_status granikv_plan_schedule(const granikv_plan* plan, int32_t* concurrent, int32_t* prefix_ctas,
+                                     int32_t* suffix_ctas);
 /* Workspace bytes granikv_decode_attention needs for this plan (256-byte aligned pointer). */
 granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan, size_t* bytes);
 

@@ -124,6 +124,8 @@ _SIGNATURES = [
     ("granikv_dispatch", C.c_int32, [C.c_void_p, C.POINTER(_Batch), C.c_void_p]),
     ("granikv_plan_num_groups", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_plan_group", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(GroupInfo)]),
+    ("granikv_plan_schedule", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32),
+                                          C.POINTER(C.c_int32)]),
     ("granikv_workspace_size", C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(C.c_size_t)]),
     ("granikv_set_concurrency", C.c_int32, [C.c_void_p, C.c_int32, C.c_float]),
     ("granikv_set_fused_merge", C.c_int32, [C.c_void_p, C.c_int32]),
@@ -245,6 +247,13 @@ class Plan:
             _check(lib.granikv_plan_group(self.handle, i, C.byref(gi)), "granikv_plan_group")
             out.append(gi.as_dict())
         return out
+
+    def schedule(self) -> dict:
+        """{"concurrent": bool, "prefix_ctas": int, "suffix_ctas": int} of the last dispatch."""
+        a, b, c = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(self._ctx._lib.granikv_plan_schedule(self.handle, C.byref(a), C.byref(b), C.byref(c)),
+               "granikv_plan_schedule")
+        return {"concurrent": bool(a.value), "prefix_ctas": b.value, "suffix_ctas": c.value}
 
     def close(self):
         if self.handle:

@@ -197,9 +197,28 @@ class GraniKVCache:
             self._ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.device)
         return self._ws
 
+    def alloc(self, n_new: Sequence[int], slots_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Pop n_new[b] COLD slots for request b (b < len(n_new)) into its token table, without
+        writing K/V (decode() with k_new/v_new writes the step's new token).  Returns the slots."""
+        N = int(sum(n_new))
+        if slots_out is None:
+            slots_out = torch.empty((max(N, 1),), dtype=torch.int32, device=self.device)
+        self.ctx.cold_alloc(list(n_new), self.req_to_slot, self.suffix_len, self.cap, slots_out, self.stream())
+        for b in range(len(n_new)):
+            self.seq_len_host[b] += int(n_new[b])
+        return slots_out[:N]
+
+    @property
+    def fused_append(self) -> bool:
+        """Whether decode() can write the step's new K/V itself (the tensor-core suffix path)."""
+        return self.dtype == gb.DTYPE_BF16 and self.head_dim == 128 and self.n_q // self.n_kv <= 8
+
     def decode(self, layer: int, q: torch.Tensor, batch: gb.Batch, plan: Optional[gb.Plan] = None,
-               o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
-        """Decode-step attention of q [B, n_q, d] for one layer; returns (o, lse)."""
+               o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None):
+        """Decode-step attention of q [B, n_q, d] for one layer; returns (o, lse).  With k_new and
+        v_new ([B, n_kv, d]), row b is the K/V of request b's newest token (the last of its COLD
+        list, slot already allocated): it is written to that slot by the same launches."""
         if plan is None:
             plan = self.ctx.dispatch(batch)
         B = batch.B
@@ -208,7 +227,11 @@ class GraniKVCache:
         if lse is None:
             lse = torch.empty((B, self.n_q), dtype=torch.float32, device=self.device)
         ws = self.workspace(plan)
-        self.ctx.decode_attention(layer, q, batch, plan, o, lse, ws, ws.numel(), self.stream())
+        if k_new is not None:
+            self.ctx.decode_attention_append(layer, q, k_new.contiguous(), v_new.contiguous(), batch, plan, o, lse,
+                                             ws, ws.numel(), self.stream())
+        else:
+            self.ctx.decode_attention(layer, q, batch, plan, o, lse, ws, ws.numel(), self.stream())
         return o, lse
 
     def prefill(self, layer: int, slab_id: int, q: torch.Tensor, k: Optional[torch.Tensor] = None,

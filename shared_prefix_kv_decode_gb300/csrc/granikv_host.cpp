@@ -685,8 +685,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
           auto_found = true;
         }
       }
+      // serial: the suffix kernel starts only after the prefix kernel's last CTA (its tail and
+      // the second kernel's ramp measured at about 5 us)
       const double t_serial =
-          prefix_time(lo_serial) + std::max(w_s / (double)c->num_sms, suffix_bytes / 5.8e6);
+          prefix_time(lo_serial) + std::max(w_s / (double)c->num_sms, suffix_bytes / 5.8e6) + 5.0;
       if (auto_found && t_serial < best) {
         lo = lo_serial;
         auto_found = false;
@@ -863,6 +865,18 @@ granikv_status granikv_plan_num_groups(const granikv_plan* p, int32_t* n) {
 granikv_status granikv_plan_group(const granikv_plan* p, int32_t i, granikv_group_info* out) {
   if (!p || !out || !p->valid || i < 0 || i >= p->n_groups) return GRANIKV_ERR_INVALID;
   *out = p->info[i];
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_plan_schedule(const granikv_plan* p, int32_t* concurrent, int32_t* prefix_ctas,
+                                     int32_t* suffix_ctas) {
+  if (!p || !p->valid) return GRANIKV_ERR_INVALID;
+  if (concurrent) *concurrent = p->concurrent ? 1 : 0;
+  if (prefix_ctas) *prefix_ctas = p->n_pitems;
+  if (suffix_ctas) {
+    const int32_t head_groups = (p->ctx->cfg.n_kv + 7) / 8;
+    *suffix_ctas = p->suffix_impl == kImplSuffixMma ? p->n_scta * head_groups : p->n_sitems;
+  }
   return GRANIKV_OK;
 }
 

@@ -53,7 +53,7 @@ class DecodeDriver:
     def __init__(self, *, prefix_lens: Sequence[int], n_layers: int = 1, n_q: int = 32, n_kv: int = 8,
                  head_dim: int = 128, max_batch: int = 256, cap: int = 4096, n_slots: int = 1 << 17,
                  seed: int = 0, keep_logical: bool = False, device: int = 0, graph: bool = False,
-                 headroom: int = 16):
+                 headroom: int = 16, fused_append: bool = True):
         self.n_layers, self.n_q, self.n_kv, self.d = n_layers, n_q, n_kv, head_dim
         self.rng = np.random.default_rng(seed)
         self.keep = keep_logical
@@ -80,6 +80,7 @@ class DecodeDriver:
         self.last_out = None
         # graph mode: fixed device buffers the captured step reads and writes
         self.graph_mode, self.headroom = graph, headroom
+        self.fused = fused_append and self.cache.fused_append  # new K/V written by the attention launch
         self._graph = None
         self._graph_key = None
         self._planned: List[int] = []
@@ -189,23 +190,28 @@ class DecodeDriver:
             out = (self._o_buf[-1][:B], self._lse_buf[-1][:B])
         else:
             self._sync_cold()
+            fused = self.fused
             e0.record(s)
             t_issue = time.perf_counter()
-            self.cache.append([1] * B, kd, vd)
+            if fused:  # slots now, the K/V rows written by the attention launches
+                self.cache.alloc([1] * B)
+            else:
+                self.cache.append([1] * B, kd, vd)
             batch = self.cache.batch(slab_ids, [r["len"] for r in self.rows])
             t0 = time.perf_counter()
             self.ctx.dispatch(batch, self.plan)
             t_disp = time.perf_counter() - t0
             out = None
             for layer in range(self.n_layers):
-                out = self.cache.decode(layer, q_dev[layer], batch, self.plan)
+                out = self.cache.decode(layer, q_dev[layer], batch, self.plan,
+                                        k_new=kd[layer] if fused else None, v_new=vd[layer] if fused else None)
             t_host = time.perf_counter() - t_issue
             e1.record(s)
             rec = {"dispatch_us": t_disp * 1e6, "host_us": t_host * 1e6, "mode": "eager"}
         self._keep_new([1] * B, ks, vs)
         self._events.append((e0, e1))
         groups = self.plan.groups()
-        rec.update({"B": B, "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
+        rec.update({"B": B, "concurrent": self.plan.schedule()["concurrent"], "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                         "n_splits": g["n_splits"]} for g in groups]})
         self.trace.append(rec)
         if self.keep:
@@ -246,15 +252,23 @@ class DecodeDriver:
         t_disp = time.perf_counter() - t0
         ws = self.cache.workspace(self.plan)
 
+        fused = self.fused
+
         def issue():
+            st = torch.cuda.current_stream(self.dev)
             self.ctx.cold_alloc_uniform(1, B, self.cache.req_to_slot, self.cache.suffix_len, self.cache.cap,
-                                        self._slots_buf, torch.cuda.current_stream(self.dev))
+                                        self._slots_buf, st)
+            if not fused:
+                for layer in range(self.n_layers):
+                    self.ctx.cold_append(layer, self._k_buf[layer], self._v_buf[layer], self._slots_buf, B, st)
             for layer in range(self.n_layers):
-                self.ctx.cold_append(layer, self._k_buf[layer], self._v_buf[layer], self._slots_buf, B,
-                                     torch.cuda.current_stream(self.dev))
-            for layer in range(self.n_layers):
-                self.ctx.decode_attention(layer, self._q_buf[layer], batch, self.plan, self._o_buf[layer],
-                                          self._lse_buf[layer], ws, ws.numel(), torch.cuda.current_stream(self.dev))
+                if fused:
+                    self.ctx.decode_attention_append(layer, self._q_buf[layer], self._k_buf[layer], self._v_buf[layer],
+                                                     batch, self.plan, self._o_buf[layer], self._lse_buf[layer], ws,
+                                                     ws.numel(), st)
+                else:
+                    self.ctx.decode_attention(layer, self._q_buf[layer], batch, self.plan, self._o_buf[layer],
+                                              self._lse_buf[layer], ws, ws.numel(), st)
 
         e0.record(s)
         t1 = time.perf_counter()
@@ -290,13 +304,14 @@ class DecodeDriver:
 
 def run(*, steps: int = 64, n_layers: int = 2, prefix_lens=(16384, 4096), start_batch: int = 48,
         p_arrive: float = 0.25, p_complete: float = 0.02, prompt=(64, 512), seed: int = 0,
-        max_batch: int = 256, graph: bool = False, headroom: int = 16) -> Dict:
+        max_batch: int = 256, graph: bool = False, headroom: int = 16, fused_append: bool = True) -> Dict:
     """Seeded arrival/completion schedule: each step, with probability p_arrive a request arrives
     (uniform prefix, uniform prompt length in `prompt`), and every active request completes with
     probability p_complete."""
     sched = np.random.default_rng(seed + 1)
     drv = DecodeDriver(prefix_lens=prefix_lens, n_layers=n_layers, max_batch=max_batch,
-                       cap=max(prompt) + steps + headroom + 64, seed=seed, graph=graph, headroom=headroom)
+                       cap=max(prompt) + steps + headroom + 64, seed=seed, graph=graph, headroom=headroom,
+                       fused_append=fused_append)
     for i in range(start_batch):
         drv.arrive(int(sched.integers(len(prefix_lens))), int(sched.integers(prompt[0], prompt[1] + 1)))
     for _ in range(steps):
@@ -338,9 +353,10 @@ def main(argv=None):
     ap.add_argument("--headroom", type=int, default=16, help="tokens a graph's plan allows per request")
     ap.add_argument("--p-arrive", type=float, default=0.25, help="chance of an arrival per step")
     ap.add_argument("--p-complete", type=float, default=0.02, help="chance per request of completing per step")
+    ap.add_argument("--no-fused-append", action="store_true", help="append new K/V with launches of their own")
     a = ap.parse_args(argv)
     res = run(steps=a.steps, n_layers=a.layers, seed=a.seed, graph=a.graph, headroom=a.headroom,
-              p_arrive=a.p_arrive, p_complete=a.p_complete)
+              p_arrive=a.p_arrive, p_complete=a.p_complete, fused_append=not a.no_fused_append)
     trace = res.pop("trace")
     if a.trace:
         for i, t in enumerate(trace):

@@ -224,6 +224,14 @@ def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
     assert n_serial == n_full == 9
     assert n_half == 4
     assert n_half < n_auto < n_full
+    # the plan reports how it runs: side by side on all SMs, or one after the other
+    ctx.set_concurrency(True, 0.0)
+    plan = ctx.dispatch(gb.Batch(slabs, seq, 0, 4096))
+    sched = plan.schedule()
+    assert sched["concurrent"] and sched["prefix_ctas"] == 8 * 2 * n_auto
+    assert sched["prefix_ctas"] + sched["suffix_ctas"] == 152
+    ctx.set_concurrency(False, 0.0)
+    assert not ctx.dispatch(gb.Batch(slabs, seq, 0, 4096)).schedule()["concurrent"]
     for bad in (-0.1, 1.5, float("nan")):
         with pytest.raises(gb.GranikvError):
             ctx.set_concurrency(True, bad)
