@@ -56,6 +56,10 @@ constexpr int kHalfCols = kN / 2;             // S columns per softmax thread
 constexpr int kKSlots = 2;                    // slots of the K ring
 constexpr int kVSlots = 3;                    // slots of the V ring
 constexpr int kSBufs = 3;                     // S/P buffers in TMEM
+// The softmax of a ragged last tile i waits on V(i)'s full barrier by phase parity, while S runs
+// up to kSBufs tiles ahead of PV: with fewer V slots than that, the slot's previous tile may not
+// have landed yet and the parity wait would pass early (measured: wrong values with 2 V slots).
+static_assert(kVSlots >= kSBufs, "the V ring must hold as many tiles as S may run ahead of PV");
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kWarpTmaK = 8, kWarpTmaV = 9, kWarpMma = 10;
