@@ -90,8 +90,8 @@ struct AttnParams {
   const void* q;          // [B, n_q, d]
   void* o;                // [B, n_q, d]
   float* lse;             // [B, n_q]
-  const void* kpool;      // [n_slots, n_kv, d]
-  const void* vpool;
+  void* kpool;            // [n_slots, n_kv, d]; written only by the fused COLD append
+  void* vpool;
   const int32_t* req_to_slot;  // [B, cap]
   int64_t n_slots, n_hot;
   int32_t cap, B, n_q, n_kv, d, g;

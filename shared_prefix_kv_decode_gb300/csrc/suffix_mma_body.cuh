@@ -324,7 +324,7 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
         if (slot >= p.n_hot && slot < p.n_slots) {
           const uint32_t row = (lane < 16 ? kst : vst) + (uint32_t)(newest - t) * kRowStride + (lane & 15) * 16;
           const uint4 v = *reinterpret_cast<const uint4*>(smem + (row - sbase));
-          char* pool = static_cast<char*>(const_cast<void*>(lane < 16 ? p.kpool : p.vpool));
+          char* pool = static_cast<char*>(lane < 16 ? p.kpool : p.vpool);
           *reinterpret_cast<uint4*>(pool + (int64_t)slot * tok_bytes + (int64_t)j * kRowBytes + (lane & 15) * 16) = v;
         }
       }
