@@ -23,8 +23,9 @@
 //    both have read their half of S(i), each writes its half of P(i) over S(i)'s columns.  Two
 //    softmax warps per SM sub-partition keep the exponential units and issue slots busy.
 //  * warps 8 and 9, TMA loads (two 64-dim halves per tile, 128-byte swizzle), each in a warp of
-//    its own: warp 8 fills a 2-slot K ring whose slots free up as soon as S(i) completes, warp 9
-//    a 3-slot V ring freed by PV(i).
+//    its own: warp 8 fills a 3-slot K ring whose slots free up as soon as S(i) completes, warp 9
+//    a 2-slot V ring freed by PV(i); warp 9 also zeroes the rows of a ragged last V tile past
+//    the piece's end before PV may use it.
 //  * warp 10, the MMAs, issued as their inputs become ready: S(j) up to three tiles ahead of
 //    the PV products (three S/P buffers in TMEM), PV(i) once the softmax has written P(i).
 // The K producer initialises the barriers and issues the first K and V tiles before the Q
@@ -53,13 +54,11 @@ constexpr int kM = kDenseRows;                // 128 query rows per CTA
 constexpr int kN = kDenseTile;                // 128 tokens per tile
 static_assert(kN == 128, "the TMEM layout and the MMA shapes below assume 128-token tiles");
 constexpr int kHalfCols = kN / 2;             // S columns per softmax thread
-constexpr int kKSlots = 2;                    // slots of the K ring
-constexpr int kVSlots = 3;                    // slots of the V ring
+constexpr int kKSlots = 3;                    // slots of the K ring
+constexpr int kVSlots = 2;                    // slots of the V ring
 constexpr int kSBufs = 3;                     // S/P buffers in TMEM
-// The softmax of a ragged last tile i waits on V(i)'s full barrier by phase parity, while S runs
-// up to kSBufs tiles ahead of PV: with fewer V slots than that, the slot's previous tile may not
-// have landed yet and the parity wait would pass early (measured: wrong values with 2 V slots).
-static_assert(kVSlots >= kSBufs, "the V ring must hold as many tiles as S may run ahead of PV");
+// Only in-order waiters use the V barriers (the MMA for PV(i), the V producer for the tiles it
+// issued), so two V slots suffice; the ragged last V tile is cleared by the V producer itself.
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kWarpTmaK = 8, kWarpTmaV = 9, kWarpMma = 10;
@@ -94,7 +93,8 @@ enum : int {
   kBarDrain = kBarPvDone + kSBufs,          // all MMAs done -> teardown
   kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter (64 arrivals)
   kBarQFull = kBarPair + 4,                 // Q tile loaded by TMA -> MMA
-  kNumBars = kBarQFull + 1
+  kBarVZero = kBarQFull + 1,                // ragged last V tile cleared past its end -> MMA
+  kNumBars = kBarVZero + 1
 };
 static_assert(8 * kNumBars + 16 <= kBarArea, "barrier area");
 
@@ -130,6 +130,8 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   const bool causal = gr.causal != 0;
   if (causal) t1 = min(t1, (it.row_block * kM + kM - 1) / g + 1);
   const int n_tiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
+  const int valid_last = n_tiles > 0 ? (t1 - t0) - (n_tiles - 1) * kN : kN;  // tokens of the last tile
+  const bool ragged = valid_last < kN;
   const bool slab_ok = gr.slab_off >= 0 && gr.slab_off + gr.L_p <= p.n_hot && n_tiles > 0;
   // Q by TMA when the group's requests are consecutive in the batch: the row block is then a
   // (64 dims, g heads, 128/g requests) box of q [B, n_q, 128]; otherwise the threads gather it
@@ -222,6 +224,29 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         issue_tile(is_k, i);
         issued = i + 1;
       }
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (!is_k && ragged && issued == n_tiles) {
+      // the last V tile runs past the piece: once it has landed (this warp issued it after its
+      // slot's previous tile was consumed, so the parity wait is unambiguous), zero its rows
+      // from `valid_last` on, so that 0 * garbage cannot reach O, then let the MMA use it
+      const int last = n_tiles - 1;
+      bool landed = mbar_wait_bounded(bar(kBarVFull + last % kVSlots), (last / kVSlots) & 1, abort_flag, p.err,
+                                      kDevTimeout, kWaitLimitNs);
+      landed = __all_sync(0xffffffffu, landed);
+      if (landed) {
+        const uint32_t vt = sV + (last % kVSlots) * kTile;
+        for (int idx = lane; idx < (kN - valid_last) * 16; idx += 32) {
+          const int r = valid_last + idx / 16;
+          const uint32_t a = vt + ((idx >> 3) & 1) * kHalf + r * 128 + (idx & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarVZero));
+      }
+    }
+    if (lane == 0) {
       // never leave with a copy in flight: wait for every issued tile (and Q) to land
       if (is_k && q_tma && slab_ok) {
         const uint64_t t_start = globaltimer_ns();
@@ -273,7 +298,8 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
           const int st = i % kVSlots;
           const int sb = i % kSBufs;
           if (mbar_test_wait(bar(kBarPFull + sb), (i / kSBufs) & 1) &&
-              mbar_test_wait(bar(kBarVFull + st), (i / kVSlots) & 1)) {
+              mbar_test_wait(bar(kBarVFull + st), (i / kVSlots) & 1) &&
+              (!ragged || i != n_tiles - 1 || mbar_test_wait(bar(kBarVZero), 0))) {
             tc_fence_after();
             const uint32_t pa = tmem + (uint32_t)(sb * kN);  // P(i): 64 columns, two tokens per column
             const uint64_t dv = dv0 + (uint64_t)((st * kTile) >> 4);
@@ -452,21 +478,6 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         l += la + lb;
       }
       GRANIKV_TMEM_ST32(tmem + lane_off + (uint32_t)(sb * kN + half * 32), pk);
-      // zero V rows past the piece in the last tile so 0 * garbage cannot reach O (the V tile
-      // must have landed first); half h clears the 64-dim half h of those rows
-      if (valid < kN) {
-        ok = mbar_wait_bounded(bar(kBarVFull + i % kVSlots), (i / kVSlots) & 1, abort_flag, p.err, kDevTimeout,
-                               kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        if (r >= valid) {
-          const uint32_t vrow = sV + (i % kVSlots) * kTile + half * kHalf + r * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + c * 16), "r"(0u) : "memory");
-        }
-        fence_proxy_async_smem();
-      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + sb));
