@@ -16,9 +16,11 @@ its row, so the active requests always occupy table rows 0..B-1.
 The per-step trace holds B, the groups (M_eff, backend, pieces), the host time of the dispatch
 call, the host time to issue the whole step and the GPU time of the step's attention calls.
 
-Graph mode (B.5 "Per-Step Dispatch Overhead"; SURVEY's CUDA-graph capture of the step): the
-step's slot allocation (granikv_cold_alloc_uniform), K/V scatter and attention calls of every
-layer are captured once in a CUDA graph and replayed step after step.  The plan is made for the
+Graph mode ("B.5 Per-Step Dispatch Overhead": the per-step host work must stay small; "B.2 Full
+ShareGPT Lp x B matrix": the serving engine runs decode steps from pre-allocated CUDA graphs):
+the step's slot allocation (granikv_cold_alloc_uniform) and attention calls of every layer (the
+new K/V written by them, or by granikv_cold_append where that path is not available) are
+captured once in a CUDA graph and replayed step after step.  The plan is made for the
 requests' lengths plus a headroom and the kernels read the lengths that exist from the device
 (granikv_batch.seq_len_dev), so one capture serves until the batch changes or a request would
 outgrow its planned length; then the step runs eagerly once (which also uploads the new plan)
