@@ -190,7 +190,8 @@ granikv_status granikv_cold_append(granikv_ctx* ctx, int32_t layer, const void* 
  * A prefix is used whole: a request reuses the deepest admitted prefix whose full token
  * sequence starts its own, and attends over all of it (L_p = its length).  Nested prefixes each
  * own a slab of their full length.  Prefix handles are never reused.  The LRU clock advances
- * on insert, on a match that takes a reference, on acquire and on release. -------------- */
+ * on insert, on a match that takes a reference, on acquire and on release.  An index, like its
+ * context, is not thread-safe. -------------------------------------------------------------- */
 
 typedef struct granikv_index granikv_index;
 
@@ -255,9 +256,12 @@ granikv_status granikv_plan_schedule(const granikv_plan* plan, int32_t* concurre
 /* Workspace bytes granikv_decode_attention needs for this plan (256-byte aligned pointer). */
 granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan, size_t* bytes);
 
-/* Prefix/suffix concurrency of the tensor-core path: when on (the default), the suffix kernel
- * runs on a library-owned stream forked from and joined back into the caller's stream, next to
- * the prefix kernel.  prefix_sm_share in (0, 1) splits the SMs: the prefix work list is sized
+/* Prefix/suffix concurrency of the tensor-core path: when on (the default), the prefix and
+ * suffix work run side by side -- in one grid (dense prefix CTAs and suffix token-CTAs, one per
+ * SM) when every prefix group is dense, else as two kernels, the suffix one on a library-owned
+ * stream forked from and joined back into the caller's stream.  The automatic share (below) may
+ * still pick the one-after-the-other plan when its estimate is lower (granikv_plan_schedule
+ * tells which).  prefix_sm_share in (0, 1) splits the SMs: the prefix work list is sized
  * for that share and the suffix gets the SMs the prefix CTAs leave; 0 (the default) picks the
  * share from the step's estimated prefix and suffix work; 1 sizes both for all SMs, and the
  * suffix fills SMs as the prefix frees them.  When off, the prefix, suffix and merge kernels
@@ -285,7 +289,10 @@ granikv_status granikv_force_backend(granikv_ctx* ctx, int32_t backend);
  *   lse: device [B, n_q] float32;  workspace: device, >= granikv_workspace_size bytes,
  *   256-byte aligned, not touched by the caller between calls that share a plan.
  * plan: from granikv_dispatch on this batch; NULL runs the dispatcher into the context's own
- * plan.  Its work list is copied into the workspace on first use with that workspace. */
+ * plan.  Its work list is copied into the workspace on first use with that workspace, so to
+ * capture the call in a CUDA graph, make one call with that plan and workspace first: the
+ * captured call then holds only the launches (see granikv_batch.seq_len_dev for replaying one
+ * plan over several steps). */
 granikv_status granikv_decode_attention(granikv_ctx* ctx, int32_t layer, const void* q,
                                         const granikv_batch* batch, granikv_plan* plan,
                                         void* o, float* lse, void* workspace, size_t ws_bytes,
