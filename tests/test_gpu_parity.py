@@ -463,3 +463,43 @@ def test_fused_append_needs_the_tensor_core_suffix(cuda_ok):
     with pytest.raises(gb.GranikvError) as ei:
         ctx.decode_attention_append(0, lw.q, kn, kn, batch, plan, o, lse, ws, ws.numel(), s)
     assert ei.value.status == gb.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["llama8b_single_prefix_16k", "qwen_tp1_16k"])
+def test_fused_append_full_size(cuda_ok, name):
+    """At full size, in the launch configuration the benchmark times (automatic split, one grid),
+    one decode step with the fused append equals append + attention bit for bit, and the
+    split is the one the benchmark reports."""
+    import torch
+    gb = _gb()
+    wl = FULL[name][0](0)
+    lw = _load(wl)
+    cache, ctx, spec = lw.cache, lw.cache.ctx, wl.spec
+    B, s = spec.B, cache.stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3)
+    kn = torch.randn((B, spec.n_kv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    vn = torch.randn((B, spec.n_kv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    slots = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ctx.cold_alloc([1] * B, cache.req_to_slot, cache.suffix_len, cache.cap, slots, s)
+    batch = gb.Batch(lw.slab_ids, [cache.seq_len_host[b] + 1 for b in range(B)], cache.req_to_slot, cache.cap)
+    plan = ctx.dispatch(batch)
+    sched = plan.schedule()
+    assert sched["concurrent"] and sched["prefix_ctas"] + sched["suffix_ctas"] == 152
+    ws = cache.workspace(plan)
+    pools0 = cache.k_pools[0].clone(), cache.v_pools[0].clone()
+    outs = []
+    for fused in (True, False):
+        cache.k_pools[0].copy_(pools0[0])
+        cache.v_pools[0].copy_(pools0[1])
+        o = torch.empty((B, spec.n_q, 128), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, spec.n_q), dtype=torch.float32, device="cuda")
+        if fused:
+            ctx.decode_attention_append(0, lw.q, kn, vn, batch, plan, o, lse, ws, ws.numel(), s)
+        else:
+            ctx.cold_append(0, kn, vn, slots, B, s)
+            ctx.decode_attention(0, lw.q, batch, plan, o, lse, ws, ws.numel(), s)
+        ctx.sync_status(s)
+        outs.append((o.clone(), lse.clone(), cache.k_pools[0].clone(), cache.v_pools[0].clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
