@@ -473,7 +473,35 @@ def _mut_lse_no_max(q, K, V, scale):
     return (w / w.sum()) @ V, math.log(w.sum())
 
 
+def _mut_prefill_excludes_self(q, K, V, tokens=None, heads=None):
+    L, n_q, d = q.shape
+    tokens = list(range(L)) if tokens is None else list(tokens)
+    heads = list(range(n_q)) if heads is None else list(heads)
+    o = np.zeros((len(tokens), len(heads), d))
+    lse = np.zeros((len(tokens), len(heads)))
+    for a, t in enumerate(tokens):
+        for c, h in enumerate(heads):
+            j = A.kv_head(h, n_q, K.shape[1])
+            o[a, c], lse[a, c] = A.attend(q[t, h], K[:t, j], V[:t, j], A.softmax_scale(d))
+    return o, lse
+
+
+def _mut_prefill_sees_next(q, K, V, tokens=None, heads=None):
+    L, n_q, d = q.shape
+    tokens = list(range(L)) if tokens is None else list(tokens)
+    heads = list(range(n_q)) if heads is None else list(heads)
+    o = np.zeros((len(tokens), len(heads), d))
+    lse = np.zeros((len(tokens), len(heads)))
+    for a, t in enumerate(tokens):
+        for c, h in enumerate(heads):
+            j = A.kv_head(h, n_q, K.shape[1])
+            o[a, c], lse[a, c] = A.attend(q[t, h], K[:t + 2, j], V[:t + 2, j], A.softmax_scale(d))
+    return o, lse
+
+
 MUTATIONS = {
+    "prefill_excludes_own_token": ("causal_prefill", _mut_prefill_excludes_self),
+    "prefill_sees_next_token": ("causal_prefill", _mut_prefill_sees_next),
     "scale_ignored": ("attend", _mut_scale_ignored),
     "k_v_swapped": ("attend", _mut_kv_swapped),
     "last_token_dropped": ("attend", _mut_drop_last),

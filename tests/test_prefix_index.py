@@ -236,3 +236,48 @@ def test_index_destroy_returns_its_slabs(granikv_lib):
     assert side.ctx.hot_stats() == (100, 10)
     side.x.close()
     assert side.ctx.hot_stats() == (100, 100)
+
+
+# planted mistakes in the oracle: each must be caught by the hand-derived scenario
+
+class _ShortestMatch(PrefixIndexOracle):
+    def match(self, tokens, acquire=False):
+        t = tuple(int(x) for x in tokens)
+        hits = [pid for pid, e in self.entries.items() if t[:len(e["tokens"])] == e["tokens"]]
+        if not hits:
+            return self._none()
+        best = min(hits, key=lambda pid: len(self.entries[pid]["tokens"]))
+        if acquire:
+            self.acquire(best)
+        return self.info(best)
+
+
+class _MostRecentlyUsedEviction(PrefixIndexOracle):
+    def _tick(self):
+        self.clock -= 1  # later use sorts first: evicts the most recently used
+        return self.clock
+
+
+class _FutileEviction(PrefixIndexOracle):
+    def insert(self, tokens):
+        # evicts every idle HOT prefix whenever the new one does not fit at once
+        t = tuple(int(x) for x in tokens)
+        if not any(e["tokens"] == t for e in self.entries.values()) and not self._fits(self.hot, len(t)):
+            for pid in [p for p, e in self.entries.items() if e["refs"] == 0 and e["slab"] >= 0]:
+                self.hot.free_slab(self.entries.pop(pid)["slab"])
+        return super().insert(tokens)
+
+
+class _HandlesReused(PrefixIndexOracle):
+    def insert(self, tokens):
+        self.next_id = min(set(range(len(self.entries) + 1)) - set(self.entries))
+        return super().insert(tokens)
+
+
+@pytest.mark.parametrize("cls", [_ShortestMatch, _MostRecentlyUsedEviction, _FutileEviction, _HandlesReused])
+def test_planted_oracle_mistake_is_caught(cls):
+    class Side(OracleSide):
+        def __init__(self, n_hot, max_slabs):
+            self.x = cls(n_hot, max_slabs=max_slabs)
+    with pytest.raises(AssertionError):
+        run_scenario(Side)
