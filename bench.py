@@ -375,8 +375,8 @@ def run_granikv(args):
     ws_bytes = ctx.workspace_size(ctx.dispatch(probe, plan))
     ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
     ones = [1] * B
-    # the COLD append fused into the attention launches where the tensor-core suffix kernel runs
-    fused = (not args.no_fused_append and spec.dtype == "bf16" and spec.d == 128 and spec.n_q // spec.n_kv <= 8)
+    # the COLD append fused into the attention launches
+    fused = not args.no_fused_append
     ev_pairs = []
     timed_bytes = []
 

@@ -304,8 +304,7 @@ granikv_status granikv_decode_attention(granikv_ctx* ctx, int32_t layer, const v
  * seq_len[b]; its slot allocated already, e.g. by granikv_cold_alloc).  The call attends with
  * those rows and writes them to that slot of this layer's pools, so it equals granikv_cold_append
  * of the rows followed by granikv_decode_attention, one launch fewer.  GRANIKV_ERR_INVALID if a
- * request has no COLD token; GRANIKV_ERR_UNSUPPORTED unless the plan's suffix runs on the
- * tensor-core kernel (bf16, head_dim 128, n_q/n_kv <= 8). */
+ * request has no COLD token or k_new/v_new are not 16-byte aligned. */
 granikv_status granikv_decode_attention_append(granikv_ctx* ctx, int32_t layer, const void* q,
                                                const void* k_new, const void* v_new,
                                                const granikv_batch* batch, granikv_plan* plan, void* o,

@@ -210,8 +210,9 @@ class GraniKVCache:
 
     @property
     def fused_append(self) -> bool:
-        """Whether decode() can write the step's new K/V itself (the tensor-core suffix path)."""
-        return self.dtype == gb.DTYPE_BF16 and self.head_dim == 128 and self.n_q // self.n_kv <= 8
+        """decode() can write the step's new K/V itself (granikv_decode_attention_append), on
+        every path of the library."""
+        return True
 
     def decode(self, layer: int, q: torch.Tensor, batch: gb.Batch, plan: Optional[gb.Plan] = None,
                o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,

@@ -983,10 +983,9 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
   if (!p->valid || p->ctx != c || p->B != bt->B) return GRANIKV_ERR_INVALID;
   if (ws_bytes < workspace_bytes(c, p)) return GRANIKV_ERR_INVALID;
   if (k_new) {
-    // the fused append lives in the tensor-core suffix kernel (its bulk copies read the rows,
-    // which must start on 16-byte boundaries), and every request needs a token
+    // the suffix kernels take each request's newest token from k_new/v_new (the tensor-core one
+    // with bulk copies, whose rows must start on 16-byte boundaries); every request needs a token
     if (!v_new || ((uintptr_t)k_new | (uintptr_t)v_new) % 16) return GRANIKV_ERR_INVALID;
-    if (p->suffix_impl != kImplSuffixMma) return GRANIKV_ERR_UNSUPPORTED;
     for (int32_t b = 0; b < bt->B; ++b)
       if (bt->seq_len[b] < 1) return GRANIKV_ERR_INVALID;
   }

@@ -127,6 +127,10 @@ __global__ void __launch_bounds__(256) suffix_generic_kernel(AttnParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t tok_stride = (int64_t)p.n_kv * p.d;
   const int32_t* table = p.req_to_slot + (int64_t)it.b * p.cap;
+  // fused COLD append: the request's newest token is read from k_new/v_new (row b), and the warp
+  // of each KV head's first query head writes it to the token's slot; no CTA of this launch reads
+  // that slot from the pool
+  const int32_t newest = p.k_new ? (p.live_len ? p.live_len[it.b] : p.reqs[it.b].seq_len) - 1 : -1;
   for (int32_t h = warp; h < p.n_q; h += blockDim.x >> 5) {
     const int32_t j = h / p.g;
     float q[VPL];
@@ -140,9 +144,24 @@ __global__ void __launch_bounds__(256) suffix_generic_kernel(AttnParams p) {
         if (lane == 0) latch(p.err, kDevBadSlot);
         continue;
       }
+      T* kslot = static_cast<T*>(p.kpool) + slot * tok_stride + (int64_t)j * p.d;
+      T* vslot = static_cast<T*>(p.vpool) + slot * tok_stride + (int64_t)j * p.d;
+      const T* krow = kslot;
+      const T* vrow = vslot;
+      if (t == newest) {
+        const T* kn = static_cast<const T*>(p.k_new) + (int64_t)it.b * tok_stride + (int64_t)j * p.d;
+        const T* vn = static_cast<const T*>(p.v_new) + (int64_t)it.b * tok_stride + (int64_t)j * p.d;
+        if (h % p.g == 0)
+          for (int32_t i = lane; i < p.d; i += 32) {
+            kslot[i] = kn[i];
+            vslot[i] = vn[i];
+          }
+        krow = kn;
+        vrow = vn;
+      }
       float k[VPL], v[VPL];
-      load_row<VPL>((const T*)p.kpool + slot * tok_stride + (int64_t)j * p.d + lane * VPL, k);
-      load_row<VPL>((const T*)p.vpool + slot * tok_stride + (int64_t)j * p.d + lane * VPL, v);
+      load_row<VPL>(krow + lane * VPL, k);
+      load_row<VPL>(vrow + lane * VPL, v);
       float dot = 0.f;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) dot += q[i] * k[i];

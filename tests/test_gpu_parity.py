@@ -446,23 +446,40 @@ def test_fused_append_equals_append_then_attention(cuda_ok, n_kv):
     assert ei.value.status == gb.ERR_INVALID
 
 
-def test_fused_append_needs_the_tensor_core_suffix(cuda_ok):
+def test_fused_append_generic_path(cuda_ok):
+    """fp32 and a head size without a tensor-core kernel: the generic suffix kernel takes the
+    newest token from k_new/v_new and writes it to its slot, bit for bit as append + attention."""
     import torch
     gb = _gb()
-    wl = W.small_mixed(0, dtype="f32", n_q=8, n_kv=2, d=64)
+    wl = W.small_mixed(4, dtype="f32", n_q=8, n_kv=2, d=64)
     lw = _load(wl)
     cache, ctx, spec = lw.cache, lw.cache.ctx, wl.spec
     B, s = spec.B, cache.stream()
-    ctx.cold_alloc([1] * B, cache.req_to_slot, cache.suffix_len, cache.cap, None, s)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    kn = torch.randn((B, 2, 64), generator=gen, device="cuda")
+    vn = torch.randn((B, 2, 64), generator=gen, device="cuda")
+    slots = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ctx.cold_alloc([1] * B, cache.req_to_slot, cache.suffix_len, cache.cap, slots, s)
     batch = gb.Batch(lw.slab_ids, [cache.seq_len_host[b] + 1 for b in range(B)], cache.req_to_slot, cache.cap)
     plan = ctx.dispatch(batch)
     ws = cache.workspace(plan)
-    kn = torch.zeros((B, 2, 64), device="cuda")
-    o = torch.empty((B, 8, 64), device="cuda")
-    lse = torch.empty((B, 8), device="cuda")
-    with pytest.raises(gb.GranikvError) as ei:
-        ctx.decode_attention_append(0, lw.q, kn, kn, batch, plan, o, lse, ws, ws.numel(), s)
-    assert ei.value.status == gb.ERR_UNSUPPORTED
+    pools0 = cache.k_pools[0].clone(), cache.v_pools[0].clone()
+    outs = []
+    for fused in (True, False):
+        cache.k_pools[0].copy_(pools0[0])
+        cache.v_pools[0].copy_(pools0[1])
+        o = torch.empty((B, 8, 64), device="cuda")
+        lse = torch.empty((B, 8), device="cuda")
+        if fused:
+            ctx.decode_attention_append(0, lw.q, kn, vn, batch, plan, o, lse, ws, ws.numel(), s)
+        else:
+            ctx.cold_append(0, kn, vn, slots, B, s)
+            ctx.decode_attention(0, lw.q, batch, plan, o, lse, ws, ws.numel(), s)
+        ctx.sync_status(s)
+        outs.append((o.clone(), lse.clone(), cache.k_pools[0].clone(), cache.v_pools[0].clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
 
 
 @pytest.mark.parametrize("name", ["llama8b_single_prefix_16k", "qwen_tp1_16k"])
