@@ -737,9 +737,12 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int32_t n_scta = 0;
   int64_t q_base = 1, q_extra = 0;  // token-CTA k streams q_base tiles, plus one if k < q_extra
   if (T > 0) {
-    // one wave over the suffix's SMs, unless a CTA would then stream more tokens than it can
+    // one wave over the suffix's SMs, with at least kMinCtaTiles tiles per token-CTA (a CTA's
+    // set-up and first-tile latency cost about as much as three tiles, and every CTA adds a
+    // record per request it touches), unless a CTA would then stream more tokens than it can
     // stage slot ids for
-    n_scta = (int32_t)std::min<int64_t>(suffix_sms, T);
+    constexpr int64_t kMinCtaTiles = 4;
+    n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + kMinCtaTiles - 1) / kMinCtaTiles);
     n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens / kSTile - 1) / (kSuffixMaxCtaTokens / kSTile));
     q_base = T / n_scta;
     q_extra = T % n_scta;
