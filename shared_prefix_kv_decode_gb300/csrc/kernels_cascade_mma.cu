@@ -9,7 +9,11 @@
 // the group's (request, head-in-group) pairs of KV head j (grouped-query packing), so every
 // K/V tile staged in shared memory serves up to 128 queries.  Eight warps own 16 rows each:
 //     S = Q . K^T   (16 x 64 per warp per tile)       P = softmax part,   O += P . V
-// with m16n8k16 bf16 MMAs, fp32 accumulators and a running (max, sum) per row.  K/V tiles of
+// with m16n8k16 bf16 MMAs, fp32 accumulators and a running (max, sum) per row.  A block of at
+// most 16 rows (B * g <= 16: a few requests) would leave seven warps without rows and every
+// tile waiting on one warp's chain; there all eight warps take the same rows, each its own 8
+// tokens of every tile (S by m16n8k16, P V by m16n8k8), and their eight states are merged by
+// log-sum-exp in shared memory at the end, into warp 0, which writes the record.  K/V tiles of
 // 64 tokens x 128 dims (16 KB each) move through a 3-stage cp.async ring with 16-byte chunks,
 // XOR-swizzled so ldmatrix reads are conflict-free.  The piece's partial state (normalised o
 // and lse per row) goes to the request's record for that piece.
@@ -80,8 +84,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) issue(s, s);
 
-  // Q as A fragments: rows r_lo = base + lane/4 and r_hi = r_lo + 8 of this warp
-  const int32_t rbase = it.row_block * kRows + warp * 16;
+  // Q as A fragments: rows r_lo = base + lane/4 and r_hi = r_lo + 8 of this warp (of the block
+  // for every warp when the block's rows fit one warp)
+  const bool split = rows - it.row_block * kRows <= 16;
+  const int32_t rbase = it.row_block * kRows + (split ? 0 : warp * 16);
   const bool warp_active = rbase < rows;
   uint32_t qf[8][4];
   int32_t b_lo = -1, h_lo = 0, b_hi = -1, h_hi = 0;
@@ -123,6 +129,61 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
     const uint32_t kst = sbase + stage * kStageBytes;
     const uint32_t vst = kst + kTileBytes;
     const int valid = min(kTok, t1 - t0 - tile * kTok);
+
+    if (split) {
+      // this warp's 8 tokens of the tile: S (16 x 8) = Q K_w^T, one n-tile, 8 k-steps
+      const int mi = lane >> 3;
+      const int trow = warp * 8 + (lane & 7);
+      float sw[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + swz(trow, kq * 4 + mi), b0, b1, b2, b3);
+        mma_bf16_16816(sw, qf[kq * 2][0], qf[kq * 2][1], qf[kq * 2][2], qf[kq * 2][3], b0, b1);
+        mma_bf16_16816(sw, qf[kq * 2 + 1][0], qf[kq * 2 + 1][1], qf[kq * 2 + 1][2], qf[kq * 2 + 1][3], b2, b3);
+      }
+      const int c0 = warp * 8 + 2 * (lane & 3);
+      sw[0] = c0 < valid ? sw[0] * scale : -INFINITY;
+      sw[1] = c0 + 1 < valid ? sw[1] * scale : -INFINITY;
+      sw[2] = c0 < valid ? sw[2] * scale : -INFINITY;
+      sw[3] = c0 + 1 < valid ? sw[3] * scale : -INFINITY;
+      float mx_lo = fmaxf(sw[0], sw[1]), mx_hi = fmaxf(sw[2], sw[3]);
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, off));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, off));
+      }
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float mu_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+      const float mu_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+      const float al_lo = exp2f(m_lo - mu_lo), al_hi = exp2f(m_hi - mu_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      const float p0 = exp2f(sw[0] - mu_lo), p1 = exp2f(sw[1] - mu_lo);
+      const float p2 = exp2f(sw[2] - mu_hi), p3 = exp2f(sw[3] - mu_hi);
+      l_lo = l_lo * al_lo + (p0 + p1);
+      l_hi = l_hi * al_hi + (p2 + p3);
+      const uint32_t a0 = pack_bf16(p0, p1), a1 = pack_bf16(p2, p3);
+      // O += P V_w: one k-step of 8 tokens, 16 n-tiles of 8 dims
+#pragma unroll
+      for (int dq = 0; dq < 4; ++dq) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + swz(trow, dq * 4 + mi), b0, b1, b2, b3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float(&od)[4] = o[dq * 4 + i];
+          od[0] *= al_lo;
+          od[1] *= al_lo;
+          od[2] *= al_hi;
+          od[3] *= al_hi;
+        }
+        mma_bf16_1688(o[dq * 4 + 0], a0, a1, b0);
+        mma_bf16_1688(o[dq * 4 + 1], a0, a1, b1);
+        mma_bf16_1688(o[dq * 4 + 2], a0, a1, b2);
+        mma_bf16_1688(o[dq * 4 + 3], a0, a1, b3);
+      }
+      continue;
+    }
 
     // S = Q K^T over 64 tokens: 8 n-tiles of 8 tokens
     float s[8][4];
@@ -202,6 +263,80 @@ __global__ void __launch_bounds__(kWarps * 32, 1) cascade_mma_kernel(AttnParams 
     }
   }
   cp_async_wait<0>();
+  if (split) {
+    // Merge the eight warps' states of the block's 16 rows (each over its own tokens) by
+    // log-sum-exp, in the ring's shared memory, into warp 0's registers in the layout below.
+    constexpr int kR = 16;
+    float* so = reinterpret_cast<float*>(smem);  // [warp][row][dim]
+    float* sm = so + kWarps * kR * kD;           // [warp][row] running max (log2 units)
+    float* sl = sm + kWarps * kR;                // [warp][row] sum
+    float* sc = sl + kWarps * kR;                // [row][dim] merged, unnormalised
+    float* sM = sc + kR * kD;                    // [row]
+    float* sL = sM + kR;                         // [row]
+    static_assert((kWarps * kR * kD + 2 * kWarps * kR + kR * kD + 2 * kR) * 4 <= kSmemBytes, "merge space");
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, off);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, off);
+    }
+    const int gq = lane >> 2, tq = lane & 3;
+    __syncthreads();  // every warp is done reading the ring
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) {
+      *reinterpret_cast<float2*>(so + (warp * kR + gq) * kD + dt * 8 + 2 * tq) = make_float2(o[dt][0], o[dt][1]);
+      *reinterpret_cast<float2*>(so + (warp * kR + gq + 8) * kD + dt * 8 + 2 * tq) = make_float2(o[dt][2], o[dt][3]);
+    }
+    if (tq == 0) {
+      sm[warp * kR + gq] = m_lo;
+      sm[warp * kR + gq + 8] = m_hi;
+      sl[warp * kR + gq] = l_lo;
+      sl[warp * kR + gq + 8] = l_hi;
+    }
+    __syncthreads();
+    {
+      const int r = tid >> 4;          // 16 threads a row
+      const int d0 = (tid & 15) * 8;   // 8 dims a thread
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, sm[w * kR + r]);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float den = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = sm[w * kR + r];
+          const float a = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+          den += a * sl[w * kR + r];
+          const float4* src = reinterpret_cast<const float4*>(so + (w * kR + r) * kD + d0);
+          const float4 x = src[0], y = src[1];
+          acc[0] += a * x.x; acc[1] += a * x.y; acc[2] += a * x.z; acc[3] += a * x.w;
+          acc[4] += a * y.x; acc[5] += a * y.y; acc[6] += a * y.z; acc[7] += a * y.w;
+        }
+      }
+      float4* dst = reinterpret_cast<float4*>(sc + r * kD + d0);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      if ((tid & 15) == 0) {
+        sM[r] = mx;
+        sL[r] = den;
+      }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) {
+      const float2 x = *reinterpret_cast<const float2*>(sc + gq * kD + dt * 8 + 2 * tq);
+      const float2 y = *reinterpret_cast<const float2*>(sc + (gq + 8) * kD + dt * 8 + 2 * tq);
+      o[dt][0] = x.x;
+      o[dt][1] = x.y;
+      o[dt][2] = y.x;
+      o[dt][3] = y.y;
+    }
+    m_lo = sM[gq];
+    m_hi = sM[gq + 8];
+    l_lo = tq == 0 ? sL[gq] : 0.f;  // the quad sum below restores the row's sum
+    l_hi = tq == 0 ? sL[gq + 8] : 0.f;
+  }
   if (!warp_active) return;
 
   // full row sums over the quad, normalise, write each row's record for this piece

@@ -43,6 +43,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A * B + D, m16n8k8, bf16 inputs, fp32 accumulators.  A (16 x 8) is two registers: rows
+// lane/4 and lane/4 + 8, columns 2*(lane%4) and the next, which is the C layout of one 8-column
+// n-tile packed to bf16.
+__device__ __forceinline__ void mma_bf16_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
 // Transpose an 8x8 matrix of 16-bit elements held one row-pair per thread (fragment layout).
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;

@@ -392,6 +392,30 @@ def test_single_request(cuda_ok, backend, lens):
     assert_close(o, lse, o_ref, lse_ref, "bf16", f"single {lens} {backend}")
 
 
+@pytest.mark.parametrize("shape,prefix_lens,group_sizes", [
+    ((32, 8), [5000, 3001, 777, 2500], [1, 2, 4, 5]),
+    ((40, 8), [4100, 1500], [3, 4]),
+])
+@pytest.mark.parametrize("q_scale", [1.0 / math.sqrt(128), 1.0])
+def test_cascade_small_row_blocks(cuda_ok, shape, prefix_lens, group_sizes, q_scale):
+    """The cascade kernel on groups whose query rows fit one warp (B_g * g <= 16: 4, 8, 16 and
+    15 rows), where the eight warps split each tile's tokens and merge their states, next to
+    groups of 20 rows in the same launch; prefixes of many tiles with ragged last tiles."""
+    n_q, n_kv = shape
+    req_prefix = [i for i, n in enumerate(group_sizes) for _ in range(n)]
+    rng = np.random.default_rng(sum(prefix_lens) + n_q)
+    spec = W.WorkloadSpec(name="cascade_small_blocks", dtype="bf16", n_q=n_q, n_kv=n_kv, d=128,
+                          prefix_lens=list(prefix_lens), req_prefix=req_prefix,
+                          suffix_lens=[int(x) for x in rng.integers(0, 40, size=len(req_prefix))],
+                          q_scale=q_scale, n_slots=65536)
+    wl = W.Workload(spec, 21)
+    lw = _load(wl)
+    o, lse = _run(lw, "cascade")
+    assert all(gr["backend"] == _gb().BACKEND_CASCADE for gr in lw.cache.ctx.dispatch(lw.batch).groups())
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"cascade small blocks {shape} {group_sizes}")
+
+
 @pytest.mark.parametrize("n_kv", [8, 16])
 def test_fused_append_equals_append_then_attention(cuda_ok, n_kv):
     """granikv_decode_attention_append (the step's new K/V read by the suffix kernel and written
