@@ -204,6 +204,19 @@ def test_dispatch_host_time_under_budget(granikv_lib):
     assert per < 200e-6
 
 
+def test_suffix_ctas_take_at_least_four_tiles(granikv_lib):
+    """Suffix token-CTAs: one wave over the SMs left to the suffix, with at least four 16-token
+    tiles each (counted per request, a partial last tile included), because a CTA's set-up and
+    first tile cost about three tiles and each CTA adds a record for every request it touches."""
+    ctx = _host_ctx(n_slots=200000, m_sat=4)
+    sid, _ = ctx.hot_alloc(16384)
+    for suffix, want in [([16], 1), ([64], 1), ([65], 2), ([300], 5), ([17, 17], 1), ([33] * 3, 3)]:
+        sched = ctx.dispatch(gb.Batch([sid] * len(suffix), suffix, 0, 4096)).schedule()
+        assert sched["suffix_ctas"] == want, (suffix, sched)
+    big = ctx.dispatch(gb.Batch([sid] * 64, [300] * 64, 0, 4096)).schedule()
+    assert big["suffix_ctas"] == 152 - big["prefix_ctas"]
+
+
 def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
     """The prefix work list is sized for the prefix's share of the SMs (152 on a host-only
     context): all SMs when serial or at share 1, fewer pieces at share 0.5, and the automatic
