@@ -245,6 +245,14 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
+def host_cores_note() -> str:
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except Exception:
+        aff = None
+    return f"os.cpu_count()={os.cpu_count()}, affinity {aff}, BLAS threads {cpu_threads()}"
+
+
 def oracle_sample(wl, requests):
     import oracle.attention as OA
     t = time.perf_counter()
@@ -262,7 +270,7 @@ def cpu_baseline(wl, seconds: float):
     t = oracle_sample(wl, reqs)
     return {"value": n / t, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"{n} of {B} requests of {wl.spec.name}, one layer, fp64 numpy oracle "
-                      f"({t:.1f} s; host cores: os.cpu_count()={os.cpu_count()})"}
+                      f"({t:.1f} s; host cores: {host_cores_note()})"}
 
 
 # ---- the reference arm: the oracle on the host cores ----------------------------------------
@@ -290,7 +298,8 @@ def run_reference(args):
                        "head_dim": wl.spec.d, "L_p": wl.spec.prefix_lens[0],
                        "B": B, "sample_per_step": f"{per_step} requests, one layer"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                             "sample": f"{per_step} requests per step of {wl.spec.name}, one layer"},
+                             "sample": f"{per_step} requests per step of {wl.spec.name}, one layer "
+                                       f"(host cores: {host_cores_note()})"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
