@@ -97,6 +97,16 @@ struct granikv_plan {
   const void* uploaded_ws = nullptr;
   uint64_t uploaded_version = ~0ull;
   bool valid = false;
+  // granikv_dispatch's working arrays, kept with the plan so that the dispatches of a serving
+  // loop reuse their capacity instead of allocating each step
+  struct Scratch {
+    std::vector<int32_t> slot_of_slab;  // slab id -> group, -1 between dispatches
+    std::vector<int32_t> grp_slab, grp_count, req_group, begin, group_req, fill, scta_begin;
+    std::vector<DevGroup> groups;
+    std::vector<DevReq> reqs;
+    std::vector<DevSuffixItem> sitems;
+    std::vector<DevPrefixItem> pitems;
+  } scratch;
 };
 
 namespace {
@@ -554,11 +564,22 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const int32_t n_kv = c->cfg.n_kv;
 
   // 1. group requests by slab id, in order of first appearance; members in request order
-  thread_local std::vector<int32_t> slot_of_slab;
-  slot_of_slab.assign(c->slabs.size(), -1);
-  std::vector<int32_t> grp_slab;
-  std::vector<int32_t> grp_count;
-  std::vector<int32_t> req_group(B, -1);
+  granikv_plan::Scratch& w = p->scratch;
+  std::vector<int32_t>& slot_of_slab = w.slot_of_slab;
+  if (slot_of_slab.size() != c->slabs.size()) slot_of_slab.assign(c->slabs.size(), -1);
+  std::vector<int32_t>& grp_slab = w.grp_slab;
+  std::vector<int32_t>& grp_count = w.grp_count;
+  grp_slab.clear();
+  grp_count.clear();
+  struct ResetSlots {  // leave slot_of_slab all -1 again, whichever way this call returns
+    std::vector<int32_t>& map;
+    const std::vector<int32_t>& used;
+    ~ResetSlots() {
+      for (int32_t sid : used) map[sid] = -1;
+    }
+  } reset_slots{slot_of_slab, grp_slab};
+  std::vector<int32_t>& req_group = w.req_group;
+  req_group.assign(B, -1);
   for (int32_t b = 0; b < B; ++b) {
     int32_t sid = bt->slab_id[b];
     int32_t L = bt->seq_len[b];
@@ -579,9 +600,11 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const int32_t G = (int32_t)grp_slab.size();
 
   // 2. backend per group: M_eff = B_g * n_q / n_kv, dense iff M_eff >= M_sat
-  std::vector<DevGroup> groups(G);
+  std::vector<DevGroup>& groups = w.groups;
+  groups.assign(G, DevGroup{});
   p->info.assign(G, granikv_group_info{});
-  std::vector<int32_t> begin(G + 1, 0);
+  std::vector<int32_t>& begin = w.begin;
+  begin.assign(G + 1, 0);
   for (int32_t i = 0; i < G; ++i) begin[i + 1] = begin[i] + grp_count[i];
   for (int32_t i = 0; i < G; ++i) {
     DevGroup& dg = groups[i];
@@ -749,9 +772,11 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   }
 
   // 5. records and work items
-  std::vector<int32_t> group_req(begin[G]);
+  std::vector<int32_t>& group_req = w.group_req;
+  group_req.resize(begin[G]);
   {
-    std::vector<int32_t> fill(begin.begin(), begin.end() - 1);
+    std::vector<int32_t>& fill = w.fill;
+    fill.assign(begin.begin(), begin.end() - 1);
     for (int32_t b = 0; b < B; ++b)
       if (req_group[b] >= 0) group_req[fill[req_group[b]]++] = b;
   }
@@ -764,9 +789,12 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       contiguous = group_req[dg.req_begin + k] == group_req[dg.req_begin] + k;
     if (contiguous && dg.n_req > 0) dg.q_b0 = group_req[dg.req_begin];
   }
-  std::vector<DevReq> reqs(B);
-  std::vector<DevSuffixItem> sitems;
-  std::vector<int32_t> scta_begin(n_scta + 1, 0);
+  std::vector<DevReq>& reqs = w.reqs;
+  reqs.assign(B, DevReq{});
+  std::vector<DevSuffixItem>& sitems = w.sitems;
+  sitems.clear();
+  std::vector<int32_t>& scta_begin = w.scta_begin;
+  scta_begin.assign(n_scta + 1, 0);
   sitems.reserve(B + n_scta + 1);
   int64_t rec = 0;
   int32_t cta = 0;
@@ -804,7 +832,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
   // prefix items grouped by kernel; within a group the row blocks of one (KV head, piece)
   // are adjacent so they share the piece's K/V through L2
-  std::vector<DevPrefixItem> pitems;
+  std::vector<DevPrefixItem>& pitems = w.pitems;
+  pitems.clear();
   for (int32_t impl = 0; impl < kNumImpl; ++impl) {
     p->pitem_first[impl] = (int32_t)pitems.size();
     for (int32_t i = 0; i < G; ++i) {
@@ -817,30 +846,33 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     p->pitem_count[impl] = (int32_t)pitems.size() - p->pitem_first[impl];
   }
 
-  // 6. pack the device image
+  // 6. pack the device image: each array at a 16-byte boundary, the padding between them 0
+  struct Section {
+    const void* src;
+    size_t bytes;
+    size_t align;
+  };
+  const Section sections[] = {
+      {groups.data(), sizeof(DevGroup) * G, 16},
+      {group_req.data(), sizeof(int32_t) * group_req.size(), 16},
+      {reqs.data(), sizeof(DevReq) * B, 16},
+      {pitems.data(), sizeof(DevPrefixItem) * pitems.size(), 16},
+      {sitems.data(), sizeof(DevSuffixItem) * sitems.size(), 16},
+      {scta_begin.data(), sizeof(int32_t) * scta_begin.size(), 256},
+  };
+  size_t* const offs[] = {&p->off_groups, &p->off_group_req, &p->off_req, &p->off_pitems, &p->off_sitems, &p->off_scta};
   size_t off = 0;
-  p->off_groups = off;
-  off = align_up(off + sizeof(DevGroup) * G, 16);
-  p->off_group_req = off;
-  off = align_up(off + sizeof(int32_t) * group_req.size(), 16);
-  p->off_req = off;
-  off = align_up(off + sizeof(DevReq) * B, 16);
-  p->off_pitems = off;
-  off = align_up(off + sizeof(DevPrefixItem) * pitems.size(), 16);
-  p->off_sitems = off;
-  off = align_up(off + sizeof(DevSuffixItem) * sitems.size(), 16);
-  p->off_scta = off;
-  off = align_up(off + sizeof(int32_t) * scta_begin.size(), 256);
-  p->blob.assign(off, 0);
-  if (G) std::memcpy(p->blob.data() + p->off_groups, groups.data(), sizeof(DevGroup) * G);
-  if (!group_req.empty())
-    std::memcpy(p->blob.data() + p->off_group_req, group_req.data(), sizeof(int32_t) * group_req.size());
-  std::memcpy(p->blob.data() + p->off_req, reqs.data(), sizeof(DevReq) * B);
-  if (!pitems.empty())
-    std::memcpy(p->blob.data() + p->off_pitems, pitems.data(), sizeof(DevPrefixItem) * pitems.size());
-  if (!sitems.empty())
-    std::memcpy(p->blob.data() + p->off_sitems, sitems.data(), sizeof(DevSuffixItem) * sitems.size());
-  std::memcpy(p->blob.data() + p->off_scta, scta_begin.data(), sizeof(int32_t) * scta_begin.size());
+  for (int k = 0; k < 6; ++k) {
+    *offs[k] = off;
+    off = align_up(off + sections[k].bytes, sections[k].align);
+  }
+  p->blob.resize(off);
+  for (int k = 0; k < 6; ++k) {
+    unsigned char* dst = p->blob.data() + *offs[k];
+    if (sections[k].bytes) std::memcpy(dst, sections[k].src, sections[k].bytes);
+    const size_t end = k + 1 < 6 ? *offs[k + 1] : off;
+    std::memset(dst + sections[k].bytes, 0, end - *offs[k] - sections[k].bytes);
+  }
   p->n_groups = G;
   p->n_pitems = (int32_t)pitems.size();
   p->n_sitems = (int32_t)sitems.size();
