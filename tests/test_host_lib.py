@@ -217,6 +217,32 @@ def test_suffix_ctas_take_at_least_four_tiles(granikv_lib):
     assert big["suffix_ctas"] == 152 - big["prefix_ctas"]
 
 
+def test_reused_plan_equals_fresh_plan(granikv_lib):
+    """A plan dispatched again and again (its working arrays reused, invalid batches in between)
+    reports for each batch exactly what a fresh plan reports: groups, schedule and workspace."""
+    rng = np.random.default_rng(7)
+    for n_q, n_kv in [(32, 8), (40, 8)]:
+        ctx = _host_ctx(n_slots=800000, max_slabs=16, n_q=n_q, n_kv=n_kv, m_sat=64)
+        sids = [ctx.hot_alloc(int(L))[0] for L in rng.integers(1, 20000, size=6)]
+        long_lived = ctx.plan()
+        for t in range(120):
+            B = int(rng.choice([1, 3, 16, 64, 200, 1024]))
+            slabs = [int(rng.choice(sids[: 1 + t % len(sids)])) if rng.random() > 0.05 else -1 for _ in range(B)]
+            seq = [int(x) for x in rng.integers(0, 600, size=B)]
+            if t % 9 == 0:
+                slabs[0], seq[0] = -1, 0  # no prefix and no tokens: refused
+                with pytest.raises(gb.GranikvError):
+                    ctx.dispatch(gb.Batch(slabs, seq, 0, 4096), long_lived)
+                continue
+            seq = [L if (s >= 0 or L > 0) else 1 for s, L in zip(slabs, seq)]
+            batch = gb.Batch(slabs, seq, 0, 4096)
+            ctx.dispatch(batch, long_lived)
+            fresh = ctx.dispatch(batch, ctx.plan())
+            assert long_lived.groups() == fresh.groups()
+            assert long_lived.schedule() == fresh.schedule()
+            assert ctx.workspace_size(long_lived) == ctx.workspace_size(fresh)
+
+
 def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
     """The prefix work list is sized for the prefix's share of the SMs (152 on a host-only
     context): all SMs when serial or at share 1, fewer pieces at share 0.5, and the automatic
