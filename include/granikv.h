@@ -244,7 +244,10 @@ granikv_status granikv_plan_destroy(granikv_plan* plan);
 /* Group the batch's requests by HOT slab, compute M_eff = B_g * n_q / n_kv per group, choose
  * DENSE iff M_eff >= M_sat (unless a backend is forced), and lay out the step's work: prefix
  * splits, suffix chunks and partial-state records.  GRANIKV_ERR_INVALID for an unknown slab,
- * a request with neither prefix nor tokens, seq_len > cap, or B > max_batch. */
+ * a request with neither prefix nor tokens, seq_len > cap, or B > max_batch.  The plan keeps
+ * the dispatcher's working arrays, so dispatching into the same plan step after step allocates
+ * host memory only while batches grow; a plan, like its context, is used by one thread at a
+ * time. */
 granikv_status granikv_dispatch(granikv_ctx* ctx, const granikv_batch* batch, granikv_plan* plan);
 granikv_status granikv_plan_num_groups(const granikv_plan* plan, int32_t* n_groups);
 granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_group_info* out);
