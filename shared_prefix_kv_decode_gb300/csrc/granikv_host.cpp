@@ -11,8 +11,10 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -93,9 +95,8 @@ struct granikv_plan {
   int32_t pitem_count[kNumImpl] = {0, 0, 0, 0};
   std::vector<granikv_group_info> info;
   std::vector<int32_t> group_impl;
-  uint64_t version = 0;
-  const void* uploaded_ws = nullptr;
-  uint64_t uploaded_version = ~0ull;
+  uint64_t uid = 0;      // unique over the process (never reused), so a workspace record can name it
+  uint64_t version = 0;  // bumped by every dispatch into this plan
   bool valid = false;
   // granikv_dispatch's working arrays, kept with the plan so that the dispatches of a serving
   // loop reuse their capacity instead of allocating each step
@@ -204,6 +205,49 @@ int32_t tile_tokens_for(int32_t impl) {
     case kImplCascadeMma: return kCascadeTile;
     default: return kGenericTile;
   }
+}
+
+// Which plan image each workspace holds at its front.  A decode call copies its plan's work list
+// into the workspace only when the record for that address names another plan, another
+// dispatch of the same plan, or nothing; whatever else writes a workspace's front (a prefill,
+// an upload by another plan or context, the built-in static workspace's next user) replaces or
+// drops the record.  Process-wide, since several contexts may share one buffer.  Bounded: the
+// oldest records are dropped first, which only costs a re-upload.
+struct WsRecord {
+  const void* ws;
+  uint64_t plan_uid;  // 0: the front holds no plan image (e.g. a prefill's)
+  uint64_t version;
+};
+std::mutex g_ws_mutex;
+std::vector<WsRecord> g_ws_records;
+std::atomic<uint64_t> g_next_plan_uid{1};
+constexpr size_t kMaxWsRecords = 64;
+
+bool ws_holds(const void* ws, uint64_t uid, uint64_t version) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (const WsRecord& r : g_ws_records)
+    if (r.ws == ws) return r.plan_uid == uid && r.version == version;
+  return false;
+}
+
+void ws_record(const void* ws, uint64_t uid, uint64_t version) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (size_t i = 0; i < g_ws_records.size(); ++i)
+    if (g_ws_records[i].ws == ws) {
+      g_ws_records.erase(g_ws_records.begin() + i);
+      break;
+    }
+  if (g_ws_records.size() >= kMaxWsRecords) g_ws_records.erase(g_ws_records.begin());
+  g_ws_records.push_back({ws, uid, version});
+}
+
+void ws_forget(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  for (size_t i = 0; i < g_ws_records.size(); ++i)
+    if (g_ws_records[i].ws == ws) {
+      g_ws_records.erase(g_ws_records.begin() + i);
+      return;
+    }
 }
 
 }  // namespace
@@ -324,7 +368,6 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
       if (c->d_ring) cudaFree(c->d_ring);
       if (c->d_err) cudaFree(c->d_err);
       if (c->d_stage) cudaFree(c->d_stage);
-    if (c->d_ring_pos) cudaFree(c->d_ring_pos);
       if (c->d_ring_pos) cudaFree(c->d_ring_pos);
       if (c->ev_fork) cudaEventDestroy(c->ev_fork);
       if (c->ev_join) cudaEventDestroy(c->ev_join);
@@ -345,6 +388,7 @@ granikv_status granikv_destroy(granikv_ctx* c) {
     if (c->d_ring) cudaFree(c->d_ring);
     if (c->d_err) cudaFree(c->d_err);
     if (c->d_stage) cudaFree(c->d_stage);
+    if (c->d_ring_pos) cudaFree(c->d_ring_pos);
     if (c->ev_fork) cudaEventDestroy(c->ev_fork);
     if (c->ev_join) cudaEventDestroy(c->ev_join);
     if (c->aux) cudaStreamDestroy(c->aux);
@@ -544,6 +588,7 @@ granikv_status granikv_plan_create(granikv_ctx* c, granikv_plan** out) {
   granikv_plan* p = new (std::nothrow) granikv_plan();
   if (!p) return GRANIKV_ERR_INVALID;
   p->ctx = c;
+  p->uid = g_next_plan_uid.fetch_add(1);
   *out = p;
   return GRANIKV_OK;
 }
@@ -1030,13 +1075,13 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
   unsigned char* wsb = (unsigned char*)ws;
   int32_t* tickets = (int32_t*)(wsb + tickets_offset(c, p));
   const size_t tickets_bytes = sizeof(int32_t) * (size_t)p->B * c->cfg.n_q;
-  if (p->uploaded_ws != ws || p->uploaded_version != p->version) {
+  if (!ws_holds(ws, p->uid, p->version)) {
+    ws_forget(ws);  // a failed copy leaves the front unknown
     cudaError_t e = cudaMemcpyAsync(wsb, p->blob.data(), p->blob.size(), cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess && p->fused) e = cudaMemsetAsync(tickets, 0, tickets_bytes, s);
     if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
     c->n_copies += 1;
-    p->uploaded_ws = ws;
-    p->uploaded_version = p->version;
+    ws_record(ws, p->uid, p->version);
   }
   AttnParams a{};
   a.q = q;
@@ -1254,6 +1299,7 @@ granikv_status granikv_prefill_attention(granikv_ctx* c, int32_t layer, int32_t 
   for (int32_t rb = lay.row_blocks - 1; rb >= 0; --rb)
     for (int32_t j = 0; j < n_kv; ++j) items[n_items++] = DevPrefixItem{0, j, rb, 0};
   unsigned char* wsb = static_cast<unsigned char*>(ws);
+  ws_record(ws, 0, 0);  // the front no longer holds a decode plan's image
   cudaError_t e = cudaMemcpyAsync(wsb, blob.data(), blob.size(), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return GRANIKV_ERR_CUDA;
   c->n_copies += 1;
@@ -1337,9 +1383,7 @@ int32_t granikv_internal_device(const granikv_ctx* c, int* device) {
   return GRANIKV_OK;
 }
 
-void granikv_internal_plan_forget_upload(granikv_plan* p) {
-  if (p) p->uploaded_ws = nullptr;
-}
+void granikv_internal_forget_workspace(const void* ws) { ws_forget(ws); }
 
 void granikv_internal_hot_if_released(const granikv_ctx* c, const int32_t* slabs, int32_t n,
                                       int64_t* largest_free, int32_t* free_ids) {

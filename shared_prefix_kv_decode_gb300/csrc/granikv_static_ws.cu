@@ -63,8 +63,8 @@ extern "C" granikv_status granikv_decode_attention_static(granikv_ctx* ctx, int3
   if (st != GRANIKV_OK) return st;
   void* ws = nullptr;
   if (static_workspace_address(device, &ws) != cudaSuccess) return GRANIKV_ERR_CUDA;
-  // The array may hold another plan's work list and tickets from an earlier call: make this
-  // call copy its own work list in and zero its tickets again.
-  granikv_internal_plan_forget_upload(plan);
+  // The array may hold another plan's work list and tickets from an earlier call (of any
+  // context): make this call copy its own work list in and zero its tickets again.
+  granikv_internal_forget_workspace(ws);
   return granikv_decode_attention(ctx, layer, q, batch, plan, o, lse, ws, kStaticWorkspaceBytes, stream);
 }

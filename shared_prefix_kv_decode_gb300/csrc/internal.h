@@ -164,7 +164,9 @@ struct granikv_plan;
 namespace granikv {
 // Host-side helpers shared between the library's translation units (not part of the C ABI).
 int32_t granikv_internal_device(const granikv_ctx* ctx, int* device);        // a granikv_status
-void granikv_internal_plan_forget_upload(granikv_plan* plan);
+// Drop the record of which plan image a workspace holds, so the next decode call on it copies
+// its work list in again (and zeroes its merge tickets).
+void granikv_internal_forget_workspace(const void* ws);
 // HOT pool as it would be if the live slabs slabs[0..n) were released as well (nothing is
 // changed): the largest free extent, and the number of unused slab ids.
 void granikv_internal_hot_if_released(const granikv_ctx* ctx, const int32_t* slabs, int32_t n,

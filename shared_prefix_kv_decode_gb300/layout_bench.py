@@ -25,24 +25,31 @@ import sys
 
 
 def build(L_p: int, B: int, suffix: int, paged: bool, seed: int = 0):
+    """The batch of one shared prefix of L_p tokens and B requests with `suffix` own tokens
+    each, values from the seeded workload generator (``workloads.dispatch_sweep_cell``), placed
+    in the HOT layout or the paged-equivalent one.  Returns (cache, batch, q, workload)."""
+    import numpy as np
     import torch
+    import workloads as W
     from . import _binding as gb
     from .cache import GraniKVCache
 
-    n_q, n_kv, d = 32, 8, 128
+    wl = W.dispatch_sweep_cell(L_p, B, seed=seed, suffix_len=suffix)
+    n_q, n_kv, d = wl.spec.n_q, wl.spec.n_kv, wl.spec.d
     cold_tokens = B * (suffix + (L_p if paged else 0))
     n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil((cold_tokens + 1024) / 0.8)) + 8)
     cap = suffix + (L_p if paged else 0) + 64
     cache = GraniKVCache(n_layers=1, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
                          max_batch=B, cap=cap)
     dev = cache.device
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(seed)
-    kp = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    vp = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    ks = torch.randn((B, suffix, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    vs = torch.randn((B, suffix, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    q = (torch.randn((B, n_q, d), generator=gen, device=dev) / math.sqrt(d)).to(torch.bfloat16)
+
+    def on_dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device=dev).to(torch.bfloat16)
+
+    kp, vp = on_dev(wl.prefix_k(0)), on_dev(wl.prefix_v(0))
+    ks = on_dev(np.stack([wl.suffix_k(b) for b in range(B)]))
+    vs = on_dev(np.stack([wl.suffix_v(b) for b in range(B)]))
+    q = on_dev(wl.q)
     if paged:
         # each request's COLD table: its private copy of the prefix, then its suffix
         for b in range(B):
@@ -54,7 +61,7 @@ def build(L_p: int, B: int, suffix: int, paged: bool, seed: int = 0):
         cache.append([suffix] * B, [ks.reshape(-1, n_kv, d)], [vs.reshape(-1, n_kv, d)])
         slab_ids = [sid] * B
     batch = cache.batch(slab_ids)
-    return cache, batch, q
+    return cache, batch, q, wl
 
 
 def time_call(cache, batch, q, backend: int, reps: int, flush):
@@ -96,13 +103,13 @@ def main(argv=None):
         scratch.fill_(1)
 
     out = {"L_p": a.lp, "B": a.b, "suffix": a.suffix}
-    cache, batch, q = build(a.lp, a.b, a.suffix, paged=False)
+    cache, batch, q, _ = build(a.lp, a.b, a.suffix, paged=False)
     out["hot_dense_us"], o_d, _ = time_call(cache, batch, q, gb.BACKEND_DENSE, a.reps, flush)
     out["hot_cascade_us"], o_c, _ = time_call(cache, batch, q, gb.BACKEND_CASCADE, a.reps, flush)
     o_hot = o_d.float()
     del cache
     torch.cuda.empty_cache()
-    cache, batch, q = build(a.lp, a.b, a.suffix, paged=True)
+    cache, batch, q, _ = build(a.lp, a.b, a.suffix, paged=True)
     out["paged_us"], o_p, _ = time_call(cache, batch, q, gb.BACKEND_AUTO, a.reps, flush)
     out["max_abs_diff_hot_vs_paged"] = float((o_hot - o_p.float()).abs().max())
     out["speedup_dense_vs_paged"] = out["paged_us"] / out["hot_dense_us"]

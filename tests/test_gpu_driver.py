@@ -11,6 +11,17 @@ from oracle import attention as OA
 pytestmark = pytest.mark.gpu
 
 
+def _assert_batch_close(o, lse, o_ref, lse_ref, what):
+    """The parity bounds of every decode test: o max-abs <= 1e-2, mean-abs <= 1e-3 and relative
+    L2 error <= 1e-2 (near-uniform softmax rows make |o| small, where the max-abs bound alone
+    says little); lse max-abs <= 1e-3."""
+    err = np.abs(o - o_ref)
+    rel = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
+    info = f"{what}: max {err.max():.3e} mean {err.mean():.3e} rel {rel:.3e}"
+    assert err.max() <= 1e-2 and err.mean() <= 1e-3 and rel <= 1e-2, info
+    assert np.abs(lse - lse_ref).max() <= 1e-3, info
+
+
 def test_driver_churn_matches_oracle(cuda_ok):
     from shared_prefix_kv_decode_gb300.decode_driver import DecodeDriver
 
@@ -34,14 +45,15 @@ def test_driver_churn_matches_oracle(cuda_ok):
     lse = lse.cpu().numpy()
     q = drv.last_q[0]
     scale = OA.softmax_scale(d)
+    o_ref = np.zeros((drv.B, n_q, d))
+    lse_ref = np.zeros((drv.B, n_q))
     for b in range(drv.B):
         K, V = drv.logical_kv(b, 0)
         for h in range(n_q):
             j = OA.kv_head(h, n_q, n_kv)
-            o_ref, lse_ref = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
-                                       V[:, j].astype(np.float64), scale)
-            assert np.max(np.abs(o[b, h] - o_ref)) <= 1e-2, (b, h)
-            assert abs(lse[b, h] - lse_ref) <= 1e-3, (b, h)
+            o_ref[b, h], lse_ref[b, h] = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
+                                                   V[:, j].astype(np.float64), scale)
+    _assert_batch_close(o[:drv.B], lse[:drv.B], o_ref, lse_ref, "churn, eager")
 
 
 def test_driver_graph_replay_matches_oracle(cuda_ok):
@@ -71,14 +83,15 @@ def test_driver_graph_replay_matches_oracle(cuda_ok):
     lse = lse.cpu().numpy()
     q = drv.last_q[layers - 1]
     scale = OA.softmax_scale(d)
+    o_ref = np.zeros((drv.B, n_q, d))
+    lse_ref = np.zeros((drv.B, n_q))
     for b in range(drv.B):
         K, V = drv.logical_kv(b, layers - 1)
         for h in range(n_q):
             j = OA.kv_head(h, n_q, n_kv)
-            o_ref, lse_ref = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
-                                       V[:, j].astype(np.float64), scale)
-            assert np.max(np.abs(o[b, h] - o_ref)) <= 1e-2, (b, h)
-            assert abs(lse[b, h] - lse_ref) <= 1e-3, (b, h)
+            o_ref[b, h], lse_ref[b, h] = OA.attend(q[b, h].astype(np.float64), K[:, j].astype(np.float64),
+                                                   V[:, j].astype(np.float64), scale)
+    _assert_batch_close(o[:drv.B], lse[:drv.B], o_ref, lse_ref, "churn, graph replay")
     # once synchronised, the ring position the graph moved on the device accounts for every
     # token the active requests hold (completed requests gave theirs back; prefixes are in HOT)
     drv._sync_cold()

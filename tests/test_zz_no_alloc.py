@@ -2,9 +2,10 @@
 memory (a serving engine that already owns almost all GPU memory, a plain C host holding only
 pointers), run on the library's built-in workspace array.
 
-Through the C ABI, on two calls in a row, it must give what granikv_decode_attention gives with
-a caller workspace, within the parity tolerances; a plan that needs more than the built-in
-16 MiB is refused before anything is enqueued.  This file is collected last on purpose.
+Through the C ABI, on two calls in a row, it must give bit for bit what granikv_decode_attention
+gives with a caller workspace (and the oracle's result within the parity tolerances), also when
+calls of two plans alternate on the one array; a plan that needs more than the built-in 16 MiB
+is refused before anything is enqueued.  This file is collected last on purpose.
 """
 
 import ctypes as C
@@ -24,10 +25,26 @@ def _close(a, b, la, lb):
     assert np.abs(la - lb).max() <= 1e-3
 
 
-def test_static_workspace_matches_caller_workspace(cuda_ok):
+def _static_call(ctx, plan, batch, q, n_q, stream):
     import torch
     from shared_prefix_kv_decode_gb300 import _binding as gb
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((q.shape[0], n_q), float("nan"), dtype=torch.float32, device=q.device)
+    st = ctx._lib.granikv_decode_attention_static(ctx.handle, 0, C.c_void_p(q.data_ptr()), C.byref(batch.c),
+                                                  plan.handle, C.c_void_p(o.data_ptr()), C.c_void_p(lse.data_ptr()),
+                                                  C.c_void_p(stream.cuda_stream))
+    assert st == gb.OK, gb.status_string(st)
+    ctx.sync_status(stream)
+    return o, lse
+
+
+def test_static_workspace_matches_caller_workspace(cuda_ok):
+    """Two calls in a row through the C ABI equal the caller-workspace call bit for bit (the
+    kernels and their work split are the same, only the workspace's address differs), and the
+    oracle within the parity tolerances."""
+    import torch
     from shared_prefix_kv_decode_gb300.workload_io import load_workload
+    import oracle.attention as OA
 
     wl = W.medium_shared(3, q_scale=1.0)
     lw = load_workload(wl)
@@ -36,18 +53,41 @@ def test_static_workspace_matches_caller_workspace(cuda_ok):
     plan = ctx.dispatch(lw.batch)
     o_ref, lse_ref = lw.cache.decode(0, lw.q, lw.batch, plan)
     ctx.sync_status(stream)
-    o_ref = o_ref.float().cpu().numpy()
-    lse_ref = lse_ref.cpu().numpy()
     for call in range(2):
-        o = torch.full_like(lw.q, float("nan"))
-        lse = torch.full((wl.spec.B, wl.spec.n_q), float("nan"), dtype=torch.float32, device=lw.q.device)
-        st = ctx._lib.granikv_decode_attention_static(ctx.handle, 0, C.c_void_p(lw.q.data_ptr()),
-                                                      C.byref(lw.batch.c), plan.handle,
-                                                      C.c_void_p(o.data_ptr()), C.c_void_p(lse.data_ptr()),
-                                                      C.c_void_p(stream.cuda_stream))
-        assert st == gb.OK, gb.status_string(st)
+        o, lse = _static_call(ctx, plan, lw.batch, lw.q, wl.spec.n_q, stream)
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), call
+    o_or, lse_or = OA.decode_attention(wl)
+    _close(o.float().cpu().numpy(), o_or, lse.cpu().numpy(), lse_or)
+
+
+def test_static_workspace_alternating_plans(cuda_ok):
+    """Plan A, then plan B (another batch, merged by the last producer of each row, so its merge
+    tickets live in the shared array), then plan A again: each call re-copies its own work list
+    into the one array and equals its caller-workspace call bit for bit."""
+    import torch
+    from shared_prefix_kv_decode_gb300 import _binding as gb
+    from shared_prefix_kv_decode_gb300.workload_io import load_workload
+
+    wl = W.medium_shared(4, q_scale=1.0)
+    lw = load_workload(wl)
+    cache, ctx = lw.cache, lw.cache.ctx
+    stream = cache.stream()
+    n_b = 25
+    batch_b = gb.Batch(lw.slab_ids[:n_b], cache.seq_len_host[:n_b], cache.req_to_slot, cache.cap)
+    q_b = lw.q[:n_b].contiguous()
+    plan_a = ctx.dispatch(lw.batch)
+    ctx.set_fused_merge(True)
+    plan_b = ctx.dispatch(batch_b)
+    ctx.set_fused_merge(False)
+    ref = {}
+    for name, plan, batch, q in (("a", plan_a, lw.batch, lw.q), ("b", plan_b, batch_b, q_b)):
+        o, lse = cache.decode(0, q, batch, plan)
         ctx.sync_status(stream)
-        _close(o.float().cpu().numpy(), o_ref, lse.cpu().numpy(), lse_ref)
+        ref[name] = (o.clone(), lse.clone())
+    for name in ("a", "b", "a", "b"):
+        plan, batch, q = (plan_a, lw.batch, lw.q) if name == "a" else (plan_b, batch_b, q_b)
+        o, lse = _static_call(ctx, plan, batch, q, wl.spec.n_q, stream)
+        assert torch.equal(o, ref[name][0]) and torch.equal(lse, ref[name][1]), name
 
 
 def test_static_workspace_refuses_oversized_plans(cuda_ok):

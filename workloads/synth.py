@@ -346,14 +346,16 @@ def qwen_tp1_16k(seed: int = 0, q_scale: Optional[float] = None) -> Workload:
     return Workload(spec, seed)
 
 
-def dispatch_sweep_cell(L_p: int, B: int, seed: int = 0, suffix_len: int = 256) -> Workload:
+def dispatch_sweep_cell(L_p: int, B: int, seed: int = 0, suffix_len: int = 256,
+                        needles: Sequence[tuple] = ()) -> Workload:
     """One cell of the dense/cascade crossover sweep: Llama shape, one prefix, fixed suffix."""
     n_cold = B * suffix_len + 1024
     n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil(n_cold / 0.8)) + 8)
     spec = WorkloadSpec(
         name=f"sweep_Lp{L_p}_B{B}", dtype="bf16", n_q=32, n_kv=8, d=128,
         prefix_lens=[L_p], req_prefix=[0] * B, suffix_lens=[suffix_len] * B,
-        q_scale=1.0 / math.sqrt(128.0), n_slots=n_slots, schedule_max_chunk=suffix_len)
+        q_scale=1.0 / math.sqrt(128.0), n_slots=n_slots, schedule_max_chunk=suffix_len,
+        needles=list(needles))
     return Workload(spec, seed)
 
 
