@@ -72,8 +72,8 @@ typedef struct granikv_config {
   int32_t device;     /* CUDA device ordinal                           */
   int64_t n_slots;    /* slots per pool                                */
   double hot_fraction;/* f_p in (0, 1); 0 selects the default 0.2       */
-  void* const* k_pool;/* host array [n_layers] of device pointers      */
-  void* const* v_pool;/* host array [n_layers] of device pointers      */
+  void* const* k_pool;/* host array [n_layers] of device pointers, 16-byte aligned */
+  void* const* v_pool;/* host array [n_layers] of device pointers, 16-byte aligned */
   const int32_t* cold_init_order; /* host [n_slots - n_hot]: initial COLD free-ring content, a
                                      permutation of [n_hot, n_slots); NULL = ascending order   */
   int32_t m_sat;      /* dense iff M_eff >= m_sat; 0 selects the built-in GB300 fit       */

@@ -91,8 +91,9 @@ struct granikv_plan {
   bool fused = false;       // the last producer of a row merges it (no merge kernel)
   bool concurrent = false;  // suffix kernel on the auxiliary stream next to the prefix kernel
   int32_t suffix_impl = kImplGeneric;
-  int32_t pitem_first[kNumImpl] = {0, 0, 0, 0};  // prefix items are ordered by implementation
-  int32_t pitem_count[kNumImpl] = {0, 0, 0, 0};
+  int32_t merge_warps = 1;  // warps of the merge kernel per (request, head) row
+  int32_t pitem_first[kNumImpl] = {};  // prefix items are ordered by implementation
+  int32_t pitem_count[kNumImpl] = {};
   std::vector<granikv_group_info> info;
   std::vector<int32_t> group_impl;
   uint64_t uid = 0;      // unique over the process (never reused), so a workspace record can name it
@@ -140,6 +141,7 @@ bool has_device(const granikv_ctx* c) { return c && !c->cfg.host_only && c->d_ri
 int32_t prefix_impl_for(const granikv_ctx* c, int32_t backend) {
   if (c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128) {
     if (backend == GRANIKV_BACKEND_DENSE && (c->has_tmaps || c->cfg.host_only)) return kImplDenseTc;
+    if (c->g <= kCascadeStreamCols * kCascadeStreamWarps) return kImplCascadeStream;
     return kImplCascadeMma;
   }
   return kImplGeneric;
@@ -191,20 +193,47 @@ bool encode_q_map(CUtensorMap* m, const void* q, int32_t B, int32_t n_q, int32_t
   return r == CUDA_SUCCESS;
 }
 
-int32_t rows_per_cta_for(int32_t impl) {
+// Streaming cascade: consumer warps per KV head for a group of n_req requests, the fewest (so
+// the most KV heads per CTA, whole 2 KB slot rows at one warp) whose 16 * sub query columns hold
+// the group's columns, or at least one request's g columns.
+int32_t stream_sub_for(int32_t n_req, int32_t g) {
+  const int64_t cols = (int64_t)n_req * g;
+  int32_t sub = 1;
+  while (sub < kCascadeStreamWarps && ((int64_t)kCascadeStreamCols * sub < cols || kCascadeStreamCols * sub < g)) sub *= 2;
+  return sub;
+}
+
+// Query rows (request, head-in-group pairs of one KV head) one CTA of a prefix kernel takes;
+// the streaming cascade kernel takes whole requests, as many as fit its query columns.
+int32_t rows_per_cta_for(int32_t impl, int32_t g, int32_t sub) {
   switch (impl) {
     case kImplDenseTc: return kDenseRows;
     case kImplCascadeMma: return kCascadeRows;
+    case kImplCascadeStream: return (kCascadeStreamCols * sub / g) * g;
     default: return kGenericRows;
   }
 }
 
-int32_t tile_tokens_for(int32_t impl) {
+int32_t tile_tokens_for(int32_t impl, int32_t sub) {
   switch (impl) {
     case kImplDenseTc: return kDenseTile;
     case kImplCascadeMma: return kCascadeTile;
+    case kImplCascadeStream: return kCascadeStreamTile * sub;
     default: return kGenericTile;
   }
+}
+
+// KV heads one CTA of the streaming cascade kernel covers.
+int32_t stream_heads(int32_t sub) { return kCascadeStreamWarps / sub; }
+
+// CTAs of one L_p piece of a group: one per (KV head, row block), or for the streaming cascade
+// kernel one per (group of 8 / sub KV heads, column chunk).
+int64_t ctas_per_piece(const DevGroup& dg, int32_t n_kv) {
+  if (dg.impl == kImplCascadeStream) {
+    const int32_t hpc = stream_heads(dg.sub);
+    return (int64_t)((n_kv + hpc - 1) / hpc) * dg.row_blocks;
+  }
+  return (int64_t)n_kv * dg.row_blocks;
 }
 
 // Which plan image each workspace holds at its front.  A decode call copies its plan's work list
@@ -315,6 +344,12 @@ granikv_status granikv_create(const granikv_config* cfg, granikv_ctx** out) {
       delete c;
       return GRANIKV_ERR_INVALID;
     }
+    // the tensor-core kernels move pool rows with bulk copies, which need 16-byte alignment
+    for (int32_t l = 0; l < cfg->n_layers; ++l)
+      if (((uintptr_t)cfg->k_pool[l] | (uintptr_t)cfg->v_pool[l]) % 16) {
+        delete c;
+        return GRANIKV_ERR_INVALID;
+      }
     std::vector<int32_t> init(c->n_cold);
     if (cfg->cold_init_order) {
       std::vector<char> seen(c->n_cold, 0);
@@ -664,7 +699,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     dg.req_begin = begin[i];
     dg.backend = backend;
     dg.impl = prefix_impl_for(c, backend);
-    dg.rows_per_cta = rows_per_cta_for(dg.impl);
+    dg.sub = dg.impl == kImplCascadeStream ? stream_sub_for(grp_count[i], g) : 0;
+    dg.rows_per_cta = rows_per_cta_for(dg.impl, g, dg.sub);
     dg.row_blocks = (m_eff + dg.rows_per_cta - 1) / dg.rows_per_cta;
   }
   // Fused merge when every kernel of the step is a tensor-core kernel; then the suffix may run
@@ -694,15 +730,15 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   {
     int64_t max_tiles = 1;
     for (int32_t i = 0; i < G; ++i) {
-      const int64_t tile = tile_tokens_for(groups[i].impl);
+      const int64_t tile = tile_tokens_for(groups[i].impl, groups[i].sub);
       max_tiles = std::max<int64_t>(max_tiles, (groups[i].L_p + tile - 1) / tile);
     }
     auto ctas_for = [&](int64_t piece_tiles) {
       int64_t n = 0;
       for (int32_t i = 0; i < G; ++i) {
-        const int64_t tile = tile_tokens_for(groups[i].impl);
+        const int64_t tile = tile_tokens_for(groups[i].impl, groups[i].sub);
         const int64_t t = (groups[i].L_p + tile - 1) / tile;
-        n += (int64_t)n_kv * groups[i].row_blocks * ((t + piece_tiles - 1) / piece_tiles);
+        n += ctas_per_piece(groups[i], n_kv) * ((t + piece_tiles - 1) / piece_tiles);
       }
       return n;
     };
@@ -717,8 +753,9 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       // Automatic split: the piece length whose prefix time (one wave: the longest piece) and
       // suffix time (its work spread over the SMs the prefix CTAs leave) are most nearly equal,
       // i.e. the smallest max of the two.  Costs measured on GB300: a prefix CTA 5 us plus, per
-      // 128-query-row block and token, 0.0078 us (dense) or 0.02 us (cascade); the suffix 1.40
-      // SM-us per 16 COLD tokens of one group of up to 8 KV heads.
+      // 128-query-row block and token, 0.0078 us (dense) or 0.02 us (warp-MMA cascade), or per
+      // token of a group of eight KV heads 0.09 us (streaming cascade, 4 KB a token); the suffix
+      // 1.40 SM-us per 16 COLD tokens of one group of up to 8 KV heads.
       // The split is also weighed against running the two one after another on all SMs, with
       // the suffix then bound by the bandwidth HBM gives its random 2 KB row reads (about
       // 5.8 TB/s measured), and the step's bytes bounding either way at about 5.9 TB/s.
@@ -732,9 +769,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       auto prefix_time = [&](int64_t cand) {
         double t_p = 0.0;
         for (int32_t i = 0; i < G; ++i) {
-          const int64_t tile = tile_tokens_for(groups[i].impl);
-          const double per_token = groups[i].impl == kImplDenseTc ? 0.0078 : 0.02;
-          t_p = std::max(t_p, 5.0 + per_token * (double)std::min<int64_t>(cand * tile, groups[i].L_p));
+          const int64_t tile = tile_tokens_for(groups[i].impl, groups[i].sub);
+          const double per_token = groups[i].impl == kImplDenseTc ? 0.0078
+                                   : groups[i].impl == kImplCascadeStream
+                                       ? 0.09 * std::min(n_kv, stream_heads(groups[i].sub)) / 8.0
+                                       : 0.02;
+          const double fixed = groups[i].impl == kImplCascadeStream ? 3.0 : 5.0;
+          t_p = std::max(t_p, fixed + per_token * (double)std::min<int64_t>(cand * tile, groups[i].L_p));
         }
         return t_p;
       };
@@ -765,7 +806,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     }
     for (int32_t i = 0; i < G; ++i) {
       DevGroup& dg = groups[i];
-      const int64_t tile = tile_tokens_for(dg.impl);
+      const int64_t tile = tile_tokens_for(dg.impl, dg.sub);
       const int64_t t = (dg.L_p + tile - 1) / tile;
       const int64_t n_splits = (t + lo - 1) / lo;
       const int64_t base = t / n_splits;
@@ -775,7 +816,6 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       dg.n_long = (int32_t)(t - base * n_splits);
       dg.q_b0 = -1;
       dg.causal = 0;
-      dg.pad = 0;
     }
     // the tensor-core prefix kernels hold one SM per CTA; the suffix gets every other SM (an
     // automatic split that found no piece length leaving the suffix an SM shares them all)
@@ -884,7 +924,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     for (int32_t i = 0; i < G; ++i) {
       const DevGroup& dg = groups[i];
       if (dg.impl != impl) continue;
-      for (int32_t j = 0; j < n_kv; ++j)
+      const int32_t units = impl == kImplCascadeStream ? (int32_t)(ctas_per_piece(dg, n_kv) / dg.row_blocks) : n_kv;
+      for (int32_t j = 0; j < units; ++j)
         for (int32_t s = 0; s < dg.n_splits; ++s)
           for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
     }
@@ -927,6 +968,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   for (int32_t b = 0; b < B; ++b) p->n_prefix_records += reqs[b].n_prefix;
   p->n_scta = n_scta;
   p->suffix_impl = suffix_impl;
+  {
+    // the merge gives a row with many records (a cascade step over all SMs has one per L_p
+    // piece) several warps, so that each loads at most two batches of eight records
+    int32_t max_parts = 0;
+    for (int32_t b = 0; b < B; ++b) max_parts = std::max(max_parts, reqs[b].n_parts);
+    p->merge_warps = max_parts <= 16 ? 1 : max_parts <= 32 ? 2 : max_parts <= 64 ? 4 : 8;
+  }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;
   p->group_impl.resize(G);
@@ -1146,28 +1194,39 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
       r = launch_cascade_mma(a, p->pitem_first[kImplCascadeMma], p->pitem_count[kImplCascadeMma], st);
       c->n_kernels += 1;
     }
+    if (r == cudaSuccess && p->pitem_count[kImplCascadeStream] > 0) {
+      // waits (griddepcontrol.wait) for its stream predecessor before reading q or the pools
+      r = launch_cascade_stream(a, p->pitem_first[kImplCascadeStream], p->pitem_count[kImplCascadeStream], st, true);
+      c->n_kernels += 1;
+    }
     if (r == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
       if (!c->has_tmaps) return cudaErrorNotSupported;
-      const bool first = p->pitem_count[kImplGeneric] == 0 && p->pitem_count[kImplCascadeMma] == 0;
+      const bool first = p->pitem_count[kImplGeneric] == 0 && p->pitem_count[kImplCascadeMma] == 0 &&
+                         p->pitem_count[kImplCascadeStream] == 0;
       r = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
                           c->tmap_v[layer], tmq, st, first);
       c->n_kernels += 1;
     }
     return r;
   };
-  const bool one_launch = p->concurrent && c->has_tmaps && p->n_pitems > 0 &&
-                          p->pitem_count[kImplDenseTc] == p->n_pitems && p->suffix_impl == kImplSuffixMma &&
-                          p->n_sitems > 0;
-  if (one_launch) {
-    // the dense prefix items and the suffix token-CTAs side by side in one grid, then the
-    // merge: both chained to their stream predecessor by programmatic dependent launch
-    e = launch_prefix_suffix_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
-                                c->tmap_v[layer], tmq, a.scta_begin, p->n_scta, s, true);
+  auto launch_merge_k = [&](bool pdl) -> cudaError_t {
     c->n_kernels += 1;
-    if (e == cudaSuccess && !p->fused) {
-      e = launch_merge(c->cfg.dtype, a, s, true);
-      c->n_kernels += 1;
-    }
+    if (c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128) return launch_merge_rows(a, p->merge_warps, s, pdl);
+    return launch_merge(c->cfg.dtype, a, s, pdl);
+  };
+  const int32_t n_dense = p->pitem_count[kImplDenseTc], n_casc = p->pitem_count[kImplCascadeStream];
+  const bool one_launch = p->concurrent && p->n_pitems > 0 && n_dense + n_casc == p->n_pitems &&
+                          (n_dense == 0 || c->has_tmaps) && p->suffix_impl == kImplSuffixMma && p->n_sitems > 0;
+  if (one_launch) {
+    // the prefix items (dense and streaming cascade) and the suffix token-CTAs side by side in
+    // one grid, then the merge: both chained to their stream predecessor by programmatic
+    // dependent launch
+    const CUtensorMap& tk = c->has_tmaps ? c->tmap_k[layer] : tmq;
+    const CUtensorMap& tv = c->has_tmaps ? c->tmap_v[layer] : tmq;
+    e = launch_prefix_suffix_tc(a, p->pitem_first[kImplDenseTc], n_dense, p->pitem_first[kImplCascadeStream], n_casc,
+                                tk, tv, tmq, a.scta_begin, p->n_scta, s, true);
+    c->n_kernels += 1;
+    if (e == cudaSuccess && !p->fused) e = launch_merge_k(true);
   } else if (p->concurrent) {
     // fork: the suffix kernel runs on the auxiliary stream next to the prefix kernel (enqueued
     // first, so the longer prefix work starts first); join before anything else on the stream
@@ -1177,19 +1236,15 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
     if (e == cudaSuccess) e = launch_suffix(c->aux, false);
     if (e == cudaSuccess) e = cudaEventRecord(c->ev_join, c->aux);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_join, 0);
-    if (e == cudaSuccess && !p->fused) {
-      e = launch_merge(c->cfg.dtype, a, s, false);
-      c->n_kernels += 1;
-    }
+    if (e == cudaSuccess && !p->fused) e = launch_merge_k(false);
   } else {
     e = launch_prefix(s);
     // the suffix kernel follows a prefix kernel of this call, the merge the suffix kernel
-    const bool after_prefix = p->n_pitems > 0 && p->pitem_count[kImplDenseTc] > 0;
+    const bool after_prefix = p->n_pitems > 0 && n_dense + n_casc > 0;
     if (e == cudaSuccess) e = launch_suffix(s, after_prefix && p->suffix_impl == kImplSuffixMma);
     if (e == cudaSuccess && !p->fused) {
       const bool after_suffix = p->n_sitems > 0 && p->suffix_impl == kImplSuffixMma;
-      e = launch_merge(c->cfg.dtype, a, s, after_suffix);
-      c->n_kernels += 1;
+      e = launch_merge_k(after_suffix);
     }
   }
   if (e == cudaErrorNotSupported) return GRANIKV_ERR_UNSUPPORTED;

@@ -31,6 +31,7 @@ enum Impl : int32_t {
   kImplCascadeMma = 1,// bf16, head_dim 128: warp-level tensor-core cascade kernel
   kImplDenseTc = 2,   // bf16, head_dim 128: tcgen05/TMEM dense kernel
   kImplSuffixMma = 3, // bf16, head_dim 128, g <= 8: warp-level tensor-core suffix kernel
+  kImplCascadeStream = 4,  // bf16, head_dim 128, g <= 16: cascade over whole 2 KB slot rows
 };
 
 // Geometry of each prefix kernel: query rows per CTA and tokens per tile.  The planner and the
@@ -38,6 +39,10 @@ enum Impl : int32_t {
 constexpr int kGenericRows = 16, kGenericTile = 32;
 constexpr int kCascadeRows = 128, kCascadeTile = 64;
 constexpr int kDenseRows = 128, kDenseTile = 128;
+// The streaming cascade kernel: eight consumer warps, each over 16-token sub-tiles and at most 16
+// query columns (request, head-in-group pairs) of one KV head; with `sub` warps per KV head a
+// CTA covers 8 / sub KV heads and 16 * sub columns of each.
+constexpr int kCascadeStreamTile = 16, kCascadeStreamCols = 16, kCascadeStreamWarps = 8;
 // Largest number of COLD tokens one suffix CTA streams (its slot ids are staged in shared memory).
 constexpr int kSuffixMaxCtaTokens = 4096;
 
@@ -57,7 +62,7 @@ struct DevGroup {        // one prefix group: the requests sharing one HOT slab
   int32_t q_b0;          // dense: the group's requests are q_b0, q_b0+1, ... (q rows by TMA), else -1
   int32_t causal;        // dense prefill of the slab's own tokens: request b of the group is token b
                          // of the slab and attends keys [0, b] (0 for decode groups)
-  int32_t pad;
+  int32_t sub;           // streaming cascade: consumer warps per KV head (1, 2, 4, 8), else 0
 };
 static_assert(sizeof(DevGroup) == 64, "DevGroup layout");
 
@@ -78,7 +83,8 @@ struct DevReq {          // per request of the batch
 };
 
 struct DevPrefixItem {   // one CTA of a prefix kernel
-  int32_t group, kv_head, row_block, split;
+  int32_t group, kv_head, row_block, split;  // the streaming cascade kernel: kv_head is the index of
+                                             // a group of eight KV heads, row_block a column chunk
 };
 
 struct DevSuffixItem {   // one CTA of a suffix kernel
@@ -148,13 +154,19 @@ cudaError_t launch_suffix_mma(const AttnParams& p, const int32_t* cta_begin, int
 cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, const CUtensorMap& tmq, cudaStream_t s, bool pdl);
-// One launch for both: CTAs [0, n_dense) run dense prefix items first_item.., the rest the
-// suffix token-CTAs (n_scta per KV-head group of eight).
-cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_item, int32_t n_dense, const CUtensorMap& tmk,
-                                    const CUtensorMap& tmv, const CUtensorMap& tmq, const int32_t* cta_begin,
-                                    int32_t n_scta, cudaStream_t s, bool pdl);
+cudaError_t launch_cascade_stream(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s, bool pdl);
+// One launch for the prefix and suffix work: CTAs [0, n_dense) run dense prefix items
+// first_dense.., the next n_casc the streaming cascade items first_casc.., the rest the suffix
+// token-CTAs (n_scta per KV-head group of eight).
+cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_dense, int32_t n_dense, int32_t first_casc,
+                                    int32_t n_casc, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                    const CUtensorMap& tmq, const int32_t* cta_begin, int32_t n_scta, cudaStream_t s,
+                                    bool pdl);
+// The merge kernel, bf16 and head_dim 128, with `warps_per_row` warps (1, 2, 4 or 8) sharing
+// each row's records.
+cudaError_t launch_merge_rows(const AttnParams& p, int32_t warps_per_row, cudaStream_t s, bool pdl);
 
-constexpr int kNumImpl = 4;
+constexpr int kNumImpl = 5;
 
 }  // namespace granikv
 

@@ -294,36 +294,51 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
   return dtype == 1 ? launch_suffix_t<__nv_bfloat16>(p, s) : launch_suffix_t<float>(p, s);
 }
 
-// bf16, head_dim 128: one warp per (request, head), lane owns 4 elements; one pass over the
-// records with a running log-sum-exp, up to eight records' loads in flight at a time (a row of
-// the automatic split has five to nine records, so it is merged in one or two memory round
-// trips).  Records are read with streaming loads (they are not read again).  Two CTAs per SM
-// (at most 128 registers per thread): with programmatic dependent launch the CTAs become
-// resident as the decode CTAs leave, spread over about 128 SMs rather than packed four to an
-// SM on the first ones freed, which measured 1.5-2 us shorter from the release to the end.
+// bf16, head_dim 128: W warps per (request, head) row (W = 1, 2, 4 or 8), lane owns 4
+// elements.  Warp w of a row takes the row's records w, w + W, w + 2W, ... in one pass with a
+// running log-sum-exp, up to eight records' loads in flight at a time; the W partial states are
+// then combined in shared memory, in warp order, by the row's first warp.  A row of the
+// one-grid split has five to nine records (W = 1: one or two memory round trips); a cascade step
+// over all SMs has one record per L_p piece, up to ~150, which W = 8 covers in three round trips.
+// Records are read with streaming loads (they are not read again).  Two CTAs per SM (at most 128
+// registers per thread): with programmatic dependent launch the CTAs become resident as the
+// decode CTAs leave, spread over about 128 SMs rather than packed four to an SM on the first
+// ones freed, which measured 1.5-2 us shorter from the release to the end.
 constexpr int kMergeBatch = 8;
 
+template <int W>
 __global__ void __launch_bounds__(256, 2) merge_bf16_d128_kernel(AttnParams p) {
+  constexpr int kRowsPerCta = 8 / W;
+  __shared__ float4 s_acc[W > 1 ? 8 : 1][32];
+  __shared__ float s_m[W > 1 ? 8 : 1], s_den[W > 1 ? 8 : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // b * n_q + h
-  if (row >= (int64_t)p.B * p.n_q) return;
-  const int32_t b = (int32_t)(row / p.n_q);
-  const int32_t h = (int32_t)(row % p.n_q);
-  const DevReq r = p.reqs[b];  // the plan: written before the kernels of the call
-  grid_dep_wait();             // the records are complete once the kernels before this one are
+  const int part = warp % W;
+  const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + warp / W;  // b * n_q + h
+  const bool have = row < (int64_t)p.B * p.n_q;
+  DevReq r{0, 0, 0, 0};
+  int32_t h = 0;
+  if (have) {
+    const int32_t b = (int32_t)(row / p.n_q);
+    h = (int32_t)(row % p.n_q);
+    r = p.reqs[b];  // the plan: written before the kernels of the call
+  }
+  grid_dep_wait();  // the records are complete once the kernels before this one are
   grid_dep_launch_dependents();
   const float* lse_rec = p.rec_lse + (int64_t)r.rec_base * p.n_q + h;
   const float4* orec = reinterpret_cast<const float4*>(p.rec_o + ((int64_t)r.rec_base * p.n_q + h) * 128) + lane;
-  const int64_t lstride = p.n_q;
-  const int64_t ostride = (int64_t)p.n_q * 32;  // float4s between consecutive records of a row
+  const int64_t lstride = (int64_t)p.n_q * W;
+  const int64_t ostride = (int64_t)p.n_q * 32 * W;  // float4s between this warp's consecutive records
+  lse_rec += (int64_t)part * p.n_q;
+  orec += (int64_t)part * p.n_q * 32;
+  const int32_t n_mine = have && r.n_parts > part ? (r.n_parts - part + W - 1) / W : 0;
   float m = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int32_t i = 0; i < r.n_parts; i += kMergeBatch) {
+  for (int32_t i = 0; i < n_mine; i += kMergeBatch) {
     float l[kMergeBatch];
     float4 x[kMergeBatch];
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const bool ok = i + u < r.n_parts;
+      const bool ok = i + u < n_mine;
       l[u] = ok ? __ldcs(lse_rec + (i + u) * lstride) : -INFINITY;
       x[u] = ok ? __ldcs(orec + (i + u) * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -348,12 +363,58 @@ __global__ void __launch_bounds__(256, 2) merge_bf16_d128_kernel(AttnParams p) {
     }
     m = mb;
   }
+  if constexpr (W > 1) {
+    s_acc[warp][lane] = acc;
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_den[warp] = den;
+    }
+    __syncthreads();
+    if (part != 0) return;
+    float M = m;
+#pragma unroll
+    for (int q = 1; q < W; ++q) M = fmaxf(M, s_m[warp + q]);
+    if (M != -INFINITY) {
+      const float a0 = ex2_approx((m - M) * kLog2e);
+      den *= a0;
+      acc.x *= a0;
+      acc.y *= a0;
+      acc.z *= a0;
+      acc.w *= a0;
+#pragma unroll
+      for (int q = 1; q < W; ++q) {
+        const float a = ex2_approx((s_m[warp + q] - M) * kLog2e);  // 0 for a warp without records
+        const float4 y = s_acc[warp + q][lane];
+        den += a * s_den[warp + q];
+        acc.x += a * y.x;
+        acc.y += a * y.y;
+        acc.z += a * y.z;
+        acc.w += a * y.w;
+      }
+    }
+    m = M;
+  }
+  if (!have) return;
   const float inv = den > 0.f ? 1.f / den : 0.f;
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * 128)[lane] =
       make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   if (lane == 0) p.lse[row] = den > 0.f ? m + logf(den) : -INFINITY;
+}
+
+template <int W>
+cudaError_t launch_merge_w(const AttnParams& p, cudaStream_t s, bool pdl) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = prefer_max_shared(merge_bf16_d128_kernel<W>);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t rows = (int64_t)p.B * p.n_q;
+  const int64_t per_cta = 8 / W;
+  return launch_kernel(merge_bf16_d128_kernel<W>, dim3((unsigned)((rows + per_cta - 1) / per_cta)), dim3(256), 0, s,
+                       pdl, p);
 }
 
 template <typename T, int VPL>
@@ -380,17 +441,18 @@ cudaError_t launch_merge_t(const AttnParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_merge(int32_t dtype, const AttnParams& p, cudaStream_t s, bool pdl) {
-  if (dtype == 1 && p.d == 128) {
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaError_t e = prefer_max_shared(merge_bf16_d128_kernel);
-      if (e != cudaSuccess) return e;
-      attr_done = true;
-    }
-    const int64_t rows = (int64_t)p.B * p.n_q;
-    return launch_kernel(merge_bf16_d128_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, pdl, p);
-  }
+  if (dtype == 1 && p.d == 128) return launch_merge_w<1>(p, s, pdl);
   return dtype == 1 ? launch_merge_t<__nv_bfloat16>(p, s) : launch_merge_t<float>(p, s);
+}
+
+cudaError_t launch_merge_rows(const AttnParams& p, int32_t warps_per_row, cudaStream_t s, bool pdl) {
+  switch (warps_per_row) {
+    case 1: return launch_merge_w<1>(p, s, pdl);
+    case 2: return launch_merge_w<2>(p, s, pdl);
+    case 4: return launch_merge_w<4>(p, s, pdl);
+    case 8: return launch_merge_w<8>(p, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace granikv

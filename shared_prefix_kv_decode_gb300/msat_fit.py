@@ -7,11 +7,12 @@ measure M_sat = 1024 on A100 and say other GPUs need a re-fit ("Limitations").
 This sweeps the Llama-3.1-8B attention shape (32/8/128, bf16) over
 L_p in {512, 2048, 8192, 16384, 32768} x B in {1, 8, 32, 128, 256, 512} with 256 COLD tokens
 per request, timing decode attention with the backend forced to DENSE, forced to CASCADE, and
-dispatched (AUTO).  The L2 is flushed before every timed call.  M_sat is the grid threshold
-whose dispatch loses the least time against the faster backend of each cell (summed log
-slowdown over the table).
+dispatched (AUTO).  The L2 is flushed before every timed call (or, with --layers N, before every
+decode step of N back-to-back calls on N layers' own pools).  M_sat is the grid threshold whose
+dispatch loses the least time against the faster backend of each cell (summed log slowdown over
+the table).
 
-  python -m shared_prefix_kv_decode_gb300.msat_fit [--reps 20] [--json out.json]
+  python -m shared_prefix_kv_decode_gb300.msat_fit [--reps 20] [--layers 32] [--json out.json]
 """
 
 from __future__ import annotations
@@ -27,25 +28,31 @@ BS = [1, 8, 32, 128, 256, 512]
 SUFFIX = 256
 
 
-def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch):
+def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1):
+    """Median microseconds of one decode-attention call per backend.  layers = 1: a single call
+    after an L2 flush.  layers > 1: a decode step of that many back-to-back calls, one per layer
+    (each layer its own pools, so no layer's bytes are in L2 for the next), after one flush; the
+    call time is the step's time over the layers."""
     from .cache import GraniKVCache
 
     n_q, n_kv, d = 32, 8, 128
     n_cold = B * SUFFIX + 1024
     n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil(n_cold / 0.8)) + 8)
-    cache = GraniKVCache(n_layers=1, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
+    cache = GraniKVCache(n_layers=layers, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
                          max_batch=B, cap=SUFFIX + 64)
     dev = cache.device
     gen = torch.Generator(device=dev)
     gen.manual_seed(L_p * 1000 + B)
     k = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
     v = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    sid = cache.admit_prefix(L_p, [k], [v])
+    sid = cache.admit_prefix(L_p, [k] * layers, [v] * layers)
     kn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
     vn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    cache.append([SUFFIX] * B, [kn], [vn])
+    cache.append([SUFFIX] * B, [kn] * layers, [vn] * layers)
     q = (torch.randn((B, n_q, d), generator=gen, device=dev) / math.sqrt(d)).to(torch.bfloat16)
     batch = cache.batch([sid] * B)
+    if serial:  # prefix, suffix and merge one after another, each kernel on all SMs
+        cache.ctx.set_concurrency(False, 0.0)
     out = {}
     stream = cache.stream()
     for name, backend in (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE), ("auto", gb.BACKEND_AUTO)):
@@ -59,10 +66,11 @@ def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            cache.decode(0, q, batch, plan, o, lse)
+            for layer in range(layers):
+                cache.decode(layer, q, batch, plan, o, lse)
             e1.record(stream)
             e1.synchronize()
-            times.append(e0.elapsed_time(e1) * 1000.0)
+            times.append(e0.elapsed_time(e1) * 1000.0 / layers)
         out[name] = statistics.median(times)
         out[name + "_backend"] = gb.BACKEND_NAMES[plan.groups()[0]["backend"]]
     cache.ctx.sync_status(stream)
@@ -97,6 +105,9 @@ def main(argv=None):
     ap.add_argument("--json", default=None)
     ap.add_argument("--lps", default=",".join(map(str, LPS)))
     ap.add_argument("--bs", default=",".join(map(str, BS)))
+    ap.add_argument("--serial", action="store_true", help="run each kernel on its own (for profiling)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="time decode steps of this many back-to-back layer calls (default: single calls)")
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
@@ -108,7 +119,7 @@ def main(argv=None):
     rows = []
     for L_p in [int(x) for x in a.lps.split(",")]:
         for B in [int(x) for x in a.bs.split(",")]:
-            r = _time_cell(L_p, B, a.reps, None, flush, gb, torch)
+            r = _time_cell(L_p, B, a.reps, None, flush, gb, torch, serial=a.serial, layers=a.layers)
             row = {"L_p": L_p, "B": B, "m_eff": 4 * B, "dense_us": r["dense"], "cascade_us": r["cascade"],
                    "auto_us": r["auto"], "auto_backend": r["auto_backend"]}
             rows.append(row)

@@ -446,12 +446,14 @@ def test_full_size_whole_batch_through_the_benchmarked_call(cuda_ok):
     assert_close(o, lse, o_ref, lse_ref, "bf16", "llama8b whole batch, fused append")
 
 
-@pytest.mark.parametrize("shape", [(32, 16), (8, 8), (64, 8), (16, 2)])
+@pytest.mark.parametrize("shape", [(32, 16), (8, 8), (64, 8), (16, 2), (64, 2)])
 @pytest.mark.parametrize("backend", BACKENDS)
 def test_head_shapes(cuda_ok, shape, backend):
     """GQA shapes besides the configurations': more than eight KV heads (two head groups in the
-    suffix kernel), one query head per KV head (g = 1), g = 8, and two KV heads; bf16, d = 128,
-    the small mixed batch (ragged prefixes, a prefix-only and a prefix-less request)."""
+    suffix and streaming cascade kernels), one query head per KV head (g = 1), g = 8, two KV
+    heads, and g = 32 (beyond the streaming cascade kernel's 16 query columns: the warp-MMA
+    cascade kernel and the CUDA-core suffix kernel); bf16, d = 128, the small mixed batch (ragged
+    prefixes, a prefix-only and a prefix-less request)."""
     n_q, n_kv = shape
     wl = W.small_mixed(4, dtype="bf16", n_q=n_q, n_kv=n_kv, q_scale=1.0)
     lw = _load(wl)

@@ -246,8 +246,9 @@ def test_reused_plan_equals_fresh_plan(granikv_lib):
 def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
     """The prefix work list is sized for the prefix's share of the SMs (152 on a host-only
     context): all SMs when serial or at share 1, fewer pieces at share 0.5, and the automatic
-    share (0) in between for a step whose prefix work outweighs its suffix work."""
-    ctx = _host_ctx(n_slots=200000)
+    share (0) in between for a step whose prefix work outweighs its suffix work.  Dense backend
+    (M_sat 4): 128-row blocks, two per KV head at B = 64."""
+    ctx = _host_ctx(n_slots=200000, m_sat=4)
     sid, _ = ctx.hot_alloc(16384)
     slabs, seq = [sid] * 64, [300] * 64
 
