@@ -379,9 +379,12 @@ def run_granikv(args):
     plan = ctx.plan()
     slab_ids = lw.slab_ids
     seq = list(cache.seq_len_host[:B])
-    # workspace sized for the largest plan of the run (suffixes grow by one token per step)
-    probe = gb.Batch(slab_ids, [x + extra for x in seq], cache.req_to_slot, cache.cap)
-    ws_bytes = ctx.workspace_size(ctx.dispatch(probe, plan))
+    # workspace sized for the largest plan of the run: suffixes grow by one token per step, and
+    # the dispatcher's prefix/suffix split (so the record count) may change with them
+    ws_bytes = 0
+    for k in range(1, extra + 1):
+        probe = gb.Batch(slab_ids, [x + k for x in seq], cache.req_to_slot, cache.cap)
+        ws_bytes = max(ws_bytes, ctx.workspace_size(ctx.dispatch(probe, plan)))
     ws = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
     ones = [1] * B
     # the COLD append fused into the attention launches

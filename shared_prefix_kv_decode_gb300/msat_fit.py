@@ -96,6 +96,22 @@ def fit_msat(rows, g=4):
     return min(cands, key=lambda m: (round(regret(m), 12), -m))
 
 
+def fit_msat_strict(rows, g=4, min_lp=2048):
+    """The stricter reading: the smallest grid M_eff from which on the dense backend is no
+    slower than the cascade one at every L_p >= min_lp (that M_eff and every larger one); one
+    past the largest M_eff when no such value exists."""
+    meffs = sorted({r["B"] * g for r in rows})
+    for m in meffs:
+        if all(r["dense_us"] <= r["cascade_us"] for r in rows if r["B"] * g >= m and r["L_p"] >= min_lp):
+            return m
+    return 2 * meffs[-1]
+
+
+def dispatch_ratio(row):
+    """Dispatched time over the faster single backend's, for one measured cell."""
+    return row["auto_us"] / min(row["dense_us"], row["cascade_us"])
+
+
 def main(argv=None):
     import torch
     from . import _binding as gb
@@ -126,7 +142,10 @@ def main(argv=None):
             print(json.dumps(row), flush=True)
             torch.cuda.empty_cache()
     m_sat = fit_msat(rows)
-    print(f"# fitted M_sat = {m_sat}")
+    m_strict = fit_msat_strict(rows)
+    worst = max(rows, key=dispatch_ratio)
+    print(f"# fitted M_sat = {m_sat} (least regret); strict rule: {m_strict}; "
+          f"worst dispatched / best backend: {dispatch_ratio(worst):.3f} at L_p {worst['L_p']} B {worst['B']}")
     print("| L_p | B | M_eff | dense us | cascade us | auto us | auto -> | best/auto |")
     print("|---|---|---|---|---|---|---|---|")
     for r in rows:
@@ -135,7 +154,8 @@ def main(argv=None):
               f"{r['auto_us']:.1f} | {r['auto_backend']} | {best / r['auto_us']:.3f} |")
     if a.json:
         with open(a.json, "w") as f:
-            json.dump({"rows": rows, "m_sat": m_sat}, f, indent=1)
+            json.dump({"rows": rows, "m_sat": m_sat, "m_sat_strict": m_strict, "layers": a.layers, "reps": a.reps},
+                      f, indent=1)
     return 0
 
 
