@@ -25,10 +25,11 @@ namespace {
 constexpr int32_t kDefaultMaxSlabs = 1024;
 constexpr int32_t kDefaultMaxBatch = 4096;
 // Dense/cascade crossover on GB300 for the Llama-3.1-8B shape, re-fitted from the L_p x B
-// sweep of msat_fit.py (the pages' A100 value is 1024 and they state other GPUs need a re-fit).
-// With the tcgen05 dense kernel the fit lands on the sweep's smallest M_eff (4): the dense
-// backend is at least as fast as the cascade one almost everywhere on this GPU, and far faster
-// from M_eff = 128 on.
+// sweep of msat_fit.py, recorded in msat_gb300.json next to this package (the pages' A100 value
+// is 1024 and they state other GPUs need a re-fit).  Both fit rules land on the sweep's smallest
+// M_eff (4): the tcgen05 dense kernel is the faster backend in every cell of the sweep.  The
+// streaming cascade kernel comes within 2-8 % at M_eff <= 32 (both are bandwidth-bound there)
+// and falls far behind above, where its warp-level MMAs run out of throughput.
 constexpr int32_t kDefaultMsat = 4;
 
 struct Extent {
@@ -970,10 +971,11 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->suffix_impl = suffix_impl;
   {
     // the merge gives a row with many records (a cascade step over all SMs has one per L_p
-    // piece) several warps, so that each loads at most two batches of eight records
+    // piece) several warps, so that each loads its share in one batch (8, 8, 16 or 24 records
+    // a warp for 1, 2, 4 or 8 warps)
     int32_t max_parts = 0;
     for (int32_t b = 0; b < B; ++b) max_parts = std::max(max_parts, reqs[b].n_parts);
-    p->merge_warps = max_parts <= 16 ? 1 : max_parts <= 32 ? 2 : max_parts <= 64 ? 4 : 8;
+    p->merge_warps = max_parts <= 8 ? 1 : max_parts <= 16 ? 2 : max_parts <= 64 ? 4 : 8;
   }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;

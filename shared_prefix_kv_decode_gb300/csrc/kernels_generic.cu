@@ -296,18 +296,24 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
 
 // bf16, head_dim 128: W warps per (request, head) row (W = 1, 2, 4 or 8), lane owns 4
 // elements.  Warp w of a row takes the row's records w, w + W, w + 2W, ... in one pass with a
-// running log-sum-exp, up to eight records' loads in flight at a time; the W partial states are
-// then combined in shared memory, in warp order, by the row's first warp.  A row of the
-// one-grid split has five to nine records (W = 1: one or two memory round trips); a cascade step
-// over all SMs has one record per L_p piece, up to ~150, which W = 8 covers in three round trips.
+// running log-sum-exp, 8, 8, 16 or 24 records' loads in flight at a time (W = 1, 2, 4, 8); the W
+// partial states are then combined in shared memory, in warp order, by the row's first warp.  A
+// row of the one-grid split has five to nine records (one memory round trip); a cascade step
+// over all SMs has one record per L_p piece, up to ~150, which W = 8 also covers in one.
 // Records are read with streaming loads (they are not read again).  Two CTAs per SM (at most 128
 // registers per thread): with programmatic dependent launch the CTAs become resident as the
 // decode CTAs leave, spread over about 128 SMs rather than packed four to an SM on the first
 // ones freed, which measured 1.5-2 us shorter from the release to the end.
-constexpr int kMergeBatch = 8;
+// Records per warp loaded together: one memory round trip for rows of up to W * kBatch records.
+template <int W>
+struct MergeCfg {
+  static constexpr int kBatch = W >= 8 ? 24 : W >= 4 ? 16 : 8;
+  static constexpr int kMinBlocks = W >= 4 ? 1 : 2;  // registers for the larger batches
+};
 
 template <int W>
-__global__ void __launch_bounds__(256, 2) merge_bf16_d128_kernel(AttnParams p) {
+__global__ void __launch_bounds__(256, MergeCfg<W>::kMinBlocks) merge_bf16_d128_kernel(AttnParams p) {
+  constexpr int kMergeBatch = MergeCfg<W>::kBatch;
   constexpr int kRowsPerCta = 8 / W;
   __shared__ float4 s_acc[W > 1 ? 8 : 1][32];
   __shared__ float s_m[W > 1 ? 8 : 1], s_den[W > 1 ? 8 : 1];

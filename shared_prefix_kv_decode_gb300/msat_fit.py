@@ -55,24 +55,31 @@ def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers
         cache.ctx.set_concurrency(False, 0.0)
     out = {}
     stream = cache.stream()
-    for name, backend in (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE), ("auto", gb.BACKEND_AUTO)):
+    names = (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE), ("auto", gb.BACKEND_AUTO))
+    plans, outs = {}, {}
+    for name, backend in names:
         cache.ctx.force_backend(backend)
-        plan = cache.ctx.dispatch(batch)
-        o, lse = cache.decode(0, q, batch, plan)
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(reps):
+        plans[name] = cache.ctx.dispatch(batch, cache.ctx.plan())
+        outs[name] = cache.decode(0, q, batch, plans[name])
+        out[name + "_backend"] = gb.BACKEND_NAMES[plans[name].groups()[0]["backend"]]
+    torch.cuda.synchronize()
+    # the three plans take turns within every repetition, so that slow drift of the GPU's
+    # state is not read as a difference between them
+    times = {name: [] for name, _ in names}
+    for _ in range(reps):
+        for name, _ in names:
+            o, lse = outs[name]
             flush()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for layer in range(layers):
-                cache.decode(layer, q, batch, plan, o, lse)
+                cache.decode(layer, q, batch, plans[name], o, lse)
             e1.record(stream)
             e1.synchronize()
-            times.append(e0.elapsed_time(e1) * 1000.0 / layers)
-        out[name] = statistics.median(times)
-        out[name + "_backend"] = gb.BACKEND_NAMES[plan.groups()[0]["backend"]]
+            times[name].append(e0.elapsed_time(e1) * 1000.0 / layers)
+    for name, _ in names:
+        out[name] = statistics.median(times[name])
     cache.ctx.sync_status(stream)
     return out
 

@@ -37,3 +37,32 @@ def test_many_losses_above_move_it():
 def test_always_and_never():
     assert fit_msat(_rows(lambda L, B: True)) == 4
     assert fit_msat(_rows(lambda L, B: False)) > 4 * 256
+
+
+def test_committed_gb300_sweep_fits_the_built_in_threshold():
+    """The GB300 sweep committed with the package (the table the built-in M_sat comes from):
+    both fit rules give the library's default M_sat of 4 (the dense backend from the smallest
+    M_eff of the grid), and the dispatched call is within 2 % of the faster single backend in
+    every cell ("3 GraniKV", per-step dispatch: never slower than either backend alone)."""
+    import json
+    import os
+    from shared_prefix_kv_decode_gb300 import msat_fit as MF
+    path = os.path.join(os.path.dirname(MF.__file__), "msat_gb300.json")
+    with open(path) as f:
+        d = json.load(f)
+    rows = d["rows"]
+    assert len(rows) == 30 and {r["L_p"] for r in rows} == {512, 2048, 8192, 16384, 32768}
+    assert MF.fit_msat(rows) == d["m_sat"] == 4
+    assert MF.fit_msat_strict(rows) == d["m_sat_strict"] == 4
+    worst = max(rows, key=MF.dispatch_ratio)
+    assert MF.dispatch_ratio(worst) <= 1.02, worst
+
+
+def test_strict_rule_on_hand_tables():
+    from shared_prefix_kv_decode_gb300.msat_fit import fit_msat_strict
+    # dense wins from B = 32 on at every L_p >= 2048, loses below (the L_p = 512 row is ignored)
+    rows = _rows(lambda L, B: B >= 32 or L == 512)
+    assert fit_msat_strict(rows) == 128
+    # one loss at B = 128 (L_p 8192) pushes the strict threshold past it
+    rows = _rows(lambda L, B: B >= 32 and not (B == 128 and L == 8192))
+    assert fit_msat_strict(rows) == 1024
