@@ -246,8 +246,10 @@ granikv_status granikv_plan_destroy(granikv_plan* plan);
  * splits, suffix chunks and partial-state records.  GRANIKV_ERR_INVALID for an unknown slab,
  * a request with neither prefix nor tokens, seq_len > cap, or B > max_batch.  The plan keeps
  * the dispatcher's working arrays, so dispatching into the same plan step after step allocates
- * host memory only while batches grow; a plan, like its context, is used by one thread at a
- * time. */
+ * host memory only while batches grow, and when a batch has the same slab ids as the plan's
+ * last one (the same requests, lengths grown) its grouping and prefix work items are reused;
+ * the plan is the same as a fresh dispatch of the batch would make.  A plan, like its context,
+ * is used by one thread at a time. */
 granikv_status granikv_dispatch(granikv_ctx* ctx, const granikv_batch* batch, granikv_plan* plan);
 granikv_status granikv_plan_num_groups(const granikv_plan* plan, int32_t* n_groups);
 granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_group_info* out);
@@ -256,6 +258,10 @@ granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_g
  * prefix CTAs and of suffix CTAs it launches. */
 granikv_status granikv_plan_schedule(const granikv_plan* plan, int32_t* concurrent, int32_t* prefix_ctas,
                                      int32_t* suffix_ctas);
+/* Diagnostics (no counterpart in the paper): copy the plan's device image -- the work list that
+ * granikv_decode_attention copies to the front of the workspace -- into host memory.  *size
+ * receives its length; nothing is copied when cap is smaller (then GRANIKV_ERR_INVALID). */
+granikv_status granikv_plan_image(const granikv_plan* plan, void* out, size_t cap, size_t* size);
 /* Workspace bytes granikv_decode_attention needs for this plan (256-byte aligned pointer). */
 granikv_status granikv_workspace_size(granikv_ctx* ctx, const granikv_plan* plan, size_t* bytes);
 

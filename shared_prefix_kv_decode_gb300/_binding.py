@@ -144,6 +144,7 @@ _SIGNATURES = [
                                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t,
                                               C.c_void_p]),
     ("granikv_prefill_workspace_size", C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(C.c_size_t)]),
+    ("granikv_plan_image", C.c_int32, [C.c_void_p, C.c_void_p, C.c_size_t, C.POINTER(C.c_size_t)]),
     ("granikv_set_checks", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_inject_stall", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_sync_status", C.c_int32, [C.c_void_p, C.c_void_p]),
@@ -254,6 +255,15 @@ class Plan:
         _check(self._ctx._lib.granikv_plan_schedule(self.handle, C.byref(a), C.byref(b), C.byref(c)),
                "granikv_plan_schedule")
         return {"concurrent": bool(a.value), "prefix_ctas": b.value, "suffix_ctas": c.value}
+
+    def image(self) -> bytes:
+        """The plan's device image (the work list copied into the workspace), for diagnostics."""
+        lib = self._ctx._lib
+        n = C.c_size_t()
+        lib.granikv_plan_image(self.handle, None, 0, C.byref(n))
+        buf = C.create_string_buffer(max(n.value, 1))
+        _check(lib.granikv_plan_image(self.handle, buf, n.value, C.byref(n)), "granikv_plan_image")
+        return buf.raw[:n.value]
 
     def close(self):
         if self.handle:

@@ -109,6 +109,16 @@ struct granikv_plan {
     std::vector<DevReq> reqs;
     std::vector<DevSuffixItem> sitems;
     std::vector<DevPrefixItem> pitems;
+    // What the last successful dispatch derived from the batch's slab ids alone (the groups,
+    // their members, whether each group's requests are consecutive) and from the groups' shapes
+    // alone (the prefix work items): a serving loop re-dispatches the same requests step after
+    // step with only their lengths grown, and then rebuilds neither.
+    bool groups_cached = false;
+    std::vector<int32_t> cache_slab_id;   // the batch's slab ids
+    std::vector<Slab> cache_slab;         // each group's slab (offset, length) when cached
+    std::vector<char> grp_contig;         // group's requests consecutive in the batch
+    bool pitems_cached = false;
+    std::vector<int32_t> pitems_key;      // the group fields the prefix items depend on
   } scratch;
 };
 
@@ -646,37 +656,63 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
 
   // 1. group requests by slab id, in order of first appearance; members in request order
   granikv_plan::Scratch& w = p->scratch;
-  std::vector<int32_t>& slot_of_slab = w.slot_of_slab;
-  if (slot_of_slab.size() != c->slabs.size()) slot_of_slab.assign(c->slabs.size(), -1);
   std::vector<int32_t>& grp_slab = w.grp_slab;
   std::vector<int32_t>& grp_count = w.grp_count;
-  grp_slab.clear();
-  grp_count.clear();
-  struct ResetSlots {  // leave slot_of_slab all -1 again, whichever way this call returns
-    std::vector<int32_t>& map;
-    const std::vector<int32_t>& used;
-    ~ResetSlots() {
-      for (int32_t sid : used) map[sid] = -1;
-    }
-  } reset_slots{slot_of_slab, grp_slab};
   std::vector<int32_t>& req_group = w.req_group;
-  req_group.assign(B, -1);
-  for (int32_t b = 0; b < B; ++b) {
-    int32_t sid = bt->slab_id[b];
-    int32_t L = bt->seq_len[b];
-    if (L < 0 || L > bt->cap) return GRANIKV_ERR_INVALID;
-    if (sid < 0) {
-      if (L == 0) return GRANIKV_ERR_INVALID;
-      continue;
+  int64_t T_all = 0;    // COLD tokens of the batch
+  int64_t T_tiles = 0;  // their 16-token tiles, counted per request
+  // the groups of the last dispatch stand if the batch has the same slab ids and each group's
+  // slab is still the same live extent
+  bool same_groups = w.groups_cached && (int32_t)w.cache_slab_id.size() == B &&
+                     std::memcmp(w.cache_slab_id.data(), bt->slab_id, sizeof(int32_t) * (size_t)B) == 0;
+  for (size_t i = 0; same_groups && i < grp_slab.size(); ++i) {
+    const int32_t sid = grp_slab[i];
+    same_groups = sid < (int32_t)c->slabs.size() && c->slabs[sid].live && c->slabs[sid].off == w.cache_slab[i].off &&
+                  c->slabs[sid].len == w.cache_slab[i].len;
+  }
+  w.groups_cached = false;  // set again once this dispatch succeeds
+  w.pitems_cached = w.pitems_cached && same_groups;
+  if (same_groups) {
+    for (int32_t b = 0; b < B; ++b) {
+      const int32_t L = bt->seq_len[b];
+      if (L < 0 || L > bt->cap || (L == 0 && bt->slab_id[b] < 0)) return GRANIKV_ERR_INVALID;
+      T_all += L;
+      T_tiles += (L + 15) / 16;
     }
-    if (sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live) return GRANIKV_ERR_INVALID;
-    if (slot_of_slab[sid] < 0) {
-      slot_of_slab[sid] = (int32_t)grp_slab.size();
-      grp_slab.push_back(sid);
-      grp_count.push_back(0);
+  } else {
+    w.pitems_cached = false;
+    std::vector<int32_t>& slot_of_slab = w.slot_of_slab;
+    if (slot_of_slab.size() != c->slabs.size()) slot_of_slab.assign(c->slabs.size(), -1);
+    grp_slab.clear();
+    grp_count.clear();
+    struct ResetSlots {  // leave slot_of_slab all -1 again, whichever way this call returns
+      std::vector<int32_t>& map;
+      const std::vector<int32_t>& used;
+      ~ResetSlots() {
+        for (int32_t sid : used) map[sid] = -1;
+      }
+    } reset_slots{slot_of_slab, grp_slab};
+    req_group.resize(B);
+    for (int32_t b = 0; b < B; ++b) {
+      int32_t sid = bt->slab_id[b];
+      int32_t L = bt->seq_len[b];
+      req_group[b] = -1;
+      if (L < 0 || L > bt->cap) return GRANIKV_ERR_INVALID;
+      T_all += L;
+      T_tiles += (L + 15) / 16;
+      if (sid < 0) {
+        if (L == 0) return GRANIKV_ERR_INVALID;
+        continue;
+      }
+      if (sid >= (int32_t)c->slabs.size() || !c->slabs[sid].live) return GRANIKV_ERR_INVALID;
+      if (slot_of_slab[sid] < 0) {
+        slot_of_slab[sid] = (int32_t)grp_slab.size();
+        grp_slab.push_back(sid);
+        grp_count.push_back(0);
+      }
+      req_group[b] = slot_of_slab[sid];
+      grp_count[slot_of_slab[sid]]++;
     }
-    req_group[b] = slot_of_slab[sid];
-    grp_count[slot_of_slab[sid]]++;
   }
   const int32_t G = (int32_t)grp_slab.size();
 
@@ -706,8 +742,6 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   }
   // Fused merge when every kernel of the step is a tensor-core kernel; then the suffix may run
   // next to the prefix on its own share of the SMs.
-  int64_t T_all = 0;
-  for (int32_t b = 0; b < B; ++b) T_all += bt->seq_len[b];
   const bool fast_suffix_pre = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   bool fused = c->fused_merge && (fast_suffix_pre || T_all == 0);
   for (int32_t i = 0; i < G; ++i)
@@ -760,12 +794,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       // The split is also weighed against running the two one after another on all SMs, with
       // the suffix then bound by the bandwidth HBM gives its random 2 KB row reads (about
       // 5.8 TB/s measured), and the step's bytes bounding either way at about 5.9 TB/s.
-      double w_s = 0.0, suffix_bytes = 0.0, prefix_bytes = 0.0;
       const int64_t head_groups = (n_kv + 7) / 8;
-      for (int32_t b = 0; b < B; ++b) {
-        w_s += 1.40 * (double)head_groups * (double)((bt->seq_len[b] + 15) / 16);
-        suffix_bytes += 4.0 * n_kv * c->cfg.head_dim * (double)bt->seq_len[b];
-      }
+      const double w_s = 1.40 * (double)head_groups * (double)T_tiles;
+      const double suffix_bytes = 4.0 * n_kv * c->cfg.head_dim * (double)T_all;
+      double prefix_bytes = 0.0;
       for (int32_t i = 0; i < G; ++i) prefix_bytes += 4.0 * n_kv * c->cfg.head_dim * (double)groups[i].L_p;
       auto prefix_time = [&](int64_t cand) {
         double t_p = 0.0;
@@ -839,8 +871,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   //    token-CTA (stream-K); each request segment inside a run is one work item and record.
   //    Cuts fall on tile boundaries of the request, so a CTA's time follows its tile count.
   constexpr int64_t kSTile = 16;
-  int64_t T = 0;
-  for (int32_t b = 0; b < B; ++b) T += (bt->seq_len[b] + kSTile - 1) / kSTile;
+  static_assert(kSTile == 16, "the tile count above uses 16-token tiles");
+  const int64_t T = T_tiles;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
   int32_t n_scta = 0;
@@ -859,66 +891,88 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
 
   // 5. records and work items
   std::vector<int32_t>& group_req = w.group_req;
-  group_req.resize(begin[G]);
-  {
+  if (!same_groups) {
+    group_req.resize(begin[G]);
     std::vector<int32_t>& fill = w.fill;
     fill.assign(begin.begin(), begin.end() - 1);
     for (int32_t b = 0; b < B; ++b)
       if (req_group[b] >= 0) group_req[fill[req_group[b]]++] = b;
+    w.grp_contig.assign(G, 0);
+    for (int32_t i = 0; i < G; ++i) {
+      bool contiguous = grp_count[i] > 0;
+      for (int32_t k = 1; k < grp_count[i] && contiguous; ++k)
+        contiguous = group_req[begin[i] + k] == group_req[begin[i]] + k;
+      w.grp_contig[i] = contiguous ? 1 : 0;
+    }
   }
   // dense groups whose requests are consecutive in the batch load their q rows by TMA boxes
   for (int32_t i = 0; i < G; ++i) {
     DevGroup& dg = groups[i];
-    if (dg.impl != kImplDenseTc || kDenseRows % g != 0) continue;
-    bool contiguous = true;
-    for (int32_t k = 1; k < dg.n_req && contiguous; ++k)
-      contiguous = group_req[dg.req_begin + k] == group_req[dg.req_begin] + k;
-    if (contiguous && dg.n_req > 0) dg.q_b0 = group_req[dg.req_begin];
+    if (dg.impl == kImplDenseTc && kDenseRows % g == 0 && w.grp_contig[i]) dg.q_b0 = group_req[dg.req_begin];
   }
   std::vector<DevReq>& reqs = w.reqs;
-  reqs.assign(B, DevReq{});
+  reqs.resize(B);
   std::vector<DevSuffixItem>& sitems = w.sitems;
-  sitems.clear();
   std::vector<int32_t>& scta_begin = w.scta_begin;
   scta_begin.assign(n_scta + 1, 0);
-  sitems.reserve(B + n_scta + 1);
+  // at most one item per request plus one per token-CTA boundary
+  sitems.resize((size_t)B + n_scta + 1);
+  DevSuffixItem* si = sitems.data();
+  int32_t n_si = 0;
   int64_t rec = 0;
   int32_t cta = 0;
   int64_t used = 0;
+  int64_t quota = q_base + (0 < q_extra ? 1 : 0);
+  int32_t max_parts = 0;
   for (int32_t b = 0; b < B; ++b) {
     DevReq& r = reqs[b];
-    r.rec_base = (int32_t)rec;
-    r.n_prefix = req_group[b] >= 0 ? groups[req_group[b]].n_splits : 0;
+    const int32_t n_prefix = req_group[b] >= 0 ? groups[req_group[b]].n_splits : 0;
     const int32_t L = bt->seq_len[b];
+    r.rec_base = (int32_t)rec;
+    r.n_prefix = n_prefix;
     r.seq_len = L;
     int32_t k = 0;
     const int64_t n_t = (L + kSTile - 1) / kSTile;
     for (int64_t t = 0; t < n_t;) {
-      const int64_t quota = q_base + (cta < q_extra ? 1 : 0);
       const int64_t take = std::min<int64_t>(n_t - t, quota - used);
-      DevSuffixItem it;
+      DevSuffixItem& it = si[n_si++];
       it.b = b;
       it.t0 = (int32_t)(t * kSTile);
       it.t1 = (int32_t)std::min<int64_t>((t + take) * kSTile, L);
-      it.rec = (int32_t)(rec + r.n_prefix + k);
-      sitems.push_back(it);
+      it.rec = (int32_t)(rec + n_prefix + k);
       ++k;
       t += take;
       used += take;
       if (used == quota) {
         ++cta;
-        if (cta <= n_scta) scta_begin[std::min(cta, n_scta)] = (int32_t)sitems.size();
+        if (cta <= n_scta) scta_begin[std::min(cta, n_scta)] = n_si;
         used = 0;
+        quota = q_base + (cta < q_extra ? 1 : 0);
       }
     }
-    r.n_parts = r.n_prefix + k;
+    r.n_parts = n_prefix + k;
+    max_parts = std::max(max_parts, r.n_parts);
     rec += r.n_parts;
   }
-  for (int32_t i = std::min(cta + 1, n_scta); i <= n_scta; ++i) scta_begin[i] = (int32_t)sitems.size();
+  sitems.resize(n_si);
+  for (int32_t i = std::min(cta + 1, n_scta); i <= n_scta; ++i) scta_begin[i] = n_si;
   if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
   // prefix items grouped by kernel; within a group the row blocks of one (KV head, piece)
   // are adjacent so they share the piece's K/V through L2
   std::vector<DevPrefixItem>& pitems = w.pitems;
+  // the items depend on the groups' kernels and shapes only (and the KV heads)
+  {
+    std::vector<int32_t> key_now;
+    key_now.reserve((size_t)G * 6 + 1);
+    key_now.push_back(n_kv);
+    for (int32_t i = 0; i < G; ++i) {
+      const DevGroup& dg = groups[i];
+      key_now.insert(key_now.end(), {dg.impl, dg.sub, dg.n_splits, dg.row_blocks, dg.split_len, dg.n_long});
+    }
+    if (w.pitems_cached && key_now != w.pitems_key) w.pitems_cached = false;
+    if (!w.pitems_cached) w.pitems_key.swap(key_now);
+  }
+  if (!w.pitems_cached) {
   pitems.clear();
   for (int32_t impl = 0; impl < kNumImpl; ++impl) {
     p->pitem_first[impl] = (int32_t)pitems.size();
@@ -931,6 +985,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
           for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
     }
     p->pitem_count[impl] = (int32_t)pitems.size() - p->pitem_first[impl];
+  }
   }
 
   // 6. pack the device image: each array at a 16-byte boundary, the padding between them 0
@@ -973,14 +1028,18 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     // the merge gives a row with many records (a cascade step over all SMs has one per L_p
     // piece) several warps, so that each loads its share in one batch (8, 8, 16 or 24 records
     // a warp for 1, 2, 4 or 8 warps)
-    int32_t max_parts = 0;
-    for (int32_t b = 0; b < B; ++b) max_parts = std::max(max_parts, reqs[b].n_parts);
     p->merge_warps = max_parts <= 8 ? 1 : max_parts <= 16 ? 2 : max_parts <= 64 ? 4 : 8;
   }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
+  // this dispatch succeeded: its groups and prefix items may serve the next one
+  w.cache_slab_id.assign(bt->slab_id, bt->slab_id + B);
+  w.cache_slab.resize(G);
+  for (int32_t i = 0; i < G; ++i) w.cache_slab[i] = c->slabs[grp_slab[i]];
+  w.groups_cached = true;
+  w.pitems_cached = true;
   p->version++;
   p->valid = true;
   return GRANIKV_OK;
@@ -1047,6 +1106,14 @@ size_t tickets_offset(const granikv_ctx* c, const granikv_plan* p) {
   return lse_offset(c, p) + align_up(sizeof(float) * max_records * c->cfg.n_q, 256);
 }
 }  // namespace
+
+granikv_status granikv_plan_image(const granikv_plan* p, void* out, size_t cap, size_t* size) {
+  if (!p || !size || !p->valid) return GRANIKV_ERR_INVALID;
+  *size = p->blob.size();
+  if (cap < p->blob.size() || (!out && !p->blob.empty())) return GRANIKV_ERR_INVALID;
+  if (!p->blob.empty()) std::memcpy(out, p->blob.data(), p->blob.size());
+  return GRANIKV_OK;
+}
 
 granikv_status granikv_workspace_size(granikv_ctx* c, const granikv_plan* p, size_t* bytes) {
   if (!c || !p || !bytes || !p->valid || p->ctx != c) return GRANIKV_ERR_INVALID;

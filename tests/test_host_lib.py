@@ -241,6 +241,45 @@ def test_reused_plan_equals_fresh_plan(granikv_lib):
             assert long_lived.groups() == fresh.groups()
             assert long_lived.schedule() == fresh.schedule()
             assert ctx.workspace_size(long_lived) == ctx.workspace_size(fresh)
+            assert long_lived.image() == fresh.image()
+
+
+def test_reused_groups_follow_lengths_slabs_and_settings(granikv_lib):
+    """The same requests dispatched step after step with their lengths grown (the plan reuses
+    its grouping and prefix work items), with a slab freed and its id given to another extent
+    in between, and with the backend rule changed: every plan's device image is byte for byte
+    that of a fresh dispatch of the same batch."""
+    rng = np.random.default_rng(11)
+    ctx = _host_ctx(n_slots=800000, max_slabs=16, m_sat=64)
+    s0, _ = ctx.hot_alloc(5000)
+    s1, _ = ctx.hot_alloc(16384)
+    plan = ctx.plan()
+    B = 40
+    slabs = [s0 if b % 3 == 0 else s1 for b in range(B)]
+    seq = [int(x) for x in rng.integers(1, 400, size=B)]
+    for step in range(60):
+        seq = [L + 1 for L in seq]
+        if step == 20:  # the slab of group 0 goes away; its id is reused for a longer extent
+            ctx.hot_free(s0)
+            s0b, _ = ctx.hot_alloc(7000)
+            assert s0b == s0
+        if step == 35:
+            ctx.set_msat(1024)  # every group switches backend
+        if step == 45:
+            ctx.force_backend(gb.BACKEND_DENSE)
+        batch = gb.Batch(slabs, seq, 0, 4096)
+        ctx.dispatch(batch, plan)
+        fresh = ctx.dispatch(batch, ctx.plan())
+        assert plan.groups() == fresh.groups(), step
+        assert plan.image() == fresh.image(), step
+        assert ctx.workspace_size(plan) == ctx.workspace_size(fresh), step
+    # an invalid batch with the same slab ids (a length past cap) in between leaves nothing
+    # stale behind
+    with pytest.raises(gb.GranikvError):
+        ctx.dispatch(gb.Batch(slabs, [5000] * B, 0, 4096), plan)
+    batch = gb.Batch(slabs, seq, 0, 4096)
+    ctx.dispatch(batch, plan)
+    assert plan.image() == ctx.dispatch(batch, ctx.plan()).image()
 
 
 def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
