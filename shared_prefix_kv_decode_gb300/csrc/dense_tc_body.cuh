@@ -17,11 +17,13 @@
 // slab's own tokens, row r is token r/g, the CTA reads keys only up to its block's last token,
 // and each row masks the keys after its own token in the tiles at the diagonal.
 // Roles:
-//  * warps 0-7, softmax and epilogue: warp w serves TMEM lanes 32*(w%4).. (row r = lane r) and
-//    column half w/4 of each tile.  The two warps of a row quarter swap their half-row maxima
-//    through shared memory at a time-bounded mbarrier, so both apply the same running max; once
-//    both have read their half of S(i), each writes its half of P(i) over S(i)'s columns.  Two
-//    softmax warps per SM sub-partition keep the exponential units and issue slots busy.
+//  * warps 0-7, softmax and epilogue: warp w serves TMEM lanes 32*(w%4).. (row r = lane r), all
+//    128 columns of the tiles i with i % 2 == w / 4.  The two warps of a row quarter sit on the
+//    same SM sub-partition and take turns, half a tile apart, so one issues exponentials while
+//    the other waits on its TMEM loads.  The running max is a chain over the tiles: the warp of
+//    tile i reads the max used for tile i-1 from shared memory (published by the other warp at
+//    a time-bounded mbarrier as soon as it was decided), keeps it unless the tile's row max
+//    exceeds it by more than 2^8, publishes its own, and writes P(i) over S(i)'s columns.
 //  * warps 8 and 9, TMA loads (two 64-dim halves per tile, 128-byte swizzle), each in a warp of
 //    its own: warp 8 fills a 3-slot K ring whose slots free up as soon as S(i) completes, warp 9
 //    a 2-slot V ring freed by PV(i); warp 9 also zeroes the rows of a ragged last V tile past
@@ -69,8 +71,9 @@ constexpr int kQBytes = kM * kD * 2;          // 32 KB (two 64-dim K-blocks)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;           // K slot s at kOffK + s*kTile
 constexpr int kOffV = kOffK + kKSlots * kTile;   // V slot s at kOffV + s*kTile
-constexpr int kOffRed = kOffV + kVSlots * kTile; // [2 parities][2 halves][128 rows] partial values
-constexpr int kOffBar = kOffRed + 2 * 2 * kM * 4;
+constexpr int kOffRed = kOffV + kVSlots * kTile; // [2][2 tile parities][128 rows]: row sums, maxima
+constexpr int kOffMPub = kOffRed + 2 * 2 * kM * 4;  // [4 quarters][2 tile parities][32 rows] maxima
+constexpr int kOffBar = kOffMPub + 4 * 2 * 32 * 4;
 constexpr int kBarArea = 512;
 constexpr int kSmemBytes = kOffBar + kBarArea + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -88,13 +91,14 @@ enum : int {
   kBarVFull = kBarKEmpty + kKSlots,         // [kVSlots] TMA -> MMA and last-tile softmax (V)
   kBarVEmpty = kBarVFull + kVSlots,         // [kVSlots] MMA (PV done) -> TMA
   kBarSFull = kBarVEmpty + kVSlots,         // [kSBufs] S(i) in TMEM -> softmax
-  kBarPFull = kBarSFull + kSBufs,           // [kSBufs] P(i) in TMEM -> MMA (256 arrivals)
+  kBarPFull = kBarSFull + kSBufs,           // [kSBufs] P(i) in TMEM -> MMA (128 arrivals)
   kBarPvDone = kBarPFull + kSBufs,          // [kSBufs] PV(i) done -> softmax
   kBarDrain = kBarPvDone + kSBufs,          // all MMAs done -> teardown
-  kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter (64 arrivals)
+  kBarPair = kBarDrain + 1,                 // [4] the two softmax warps of a row quarter, epilogue (64)
   kBarQFull = kBarPair + 4,                 // Q tile loaded by TMA -> MMA
   kBarVZero = kBarQFull + 1,                // ragged last V tile cleared past its end -> MMA
-  kNumBars = kBarVZero + 1
+  kBarMPub = kBarVZero + 1,                 // [4 quarters][2 parities] max of a tile published (32)
+  kNumBars = kBarMPub + 8
 };
 static_assert(8 * kNumBars + 16 <= kBarArea, "barrier area");
 
@@ -108,7 +112,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   const uint32_t base = (raw_u + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw_u);
   const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
-  float* red = reinterpret_cast<float*>(smem + kOffRed);  // red[(parity*2 + half)*kM + row]
+  float* red = reinterpret_cast<float*>(smem + kOffRed);  // red[(kind*2 + parity)*kM + row]
   const uint32_t sBar = base + kOffBar;
   auto bar = [&](int i) { return sBar + 8u * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars);
@@ -157,8 +161,9 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     if (q_tma) tma_prefetch_desc(tmq);
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1u;
-      if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxThreads;
+      if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxThreads / 2;
       if (i >= kBarPair && i < kBarPair + 4) count = 64u;
+      if (i >= kBarMPub && i < kBarMPub + 8) count = 32u;
       mbar_init(bar(i), count);
     }
     *abort_flag = slab_ok ? 0 : 1;
@@ -357,12 +362,14 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       }
     }
   } else {
-    // ---------------- softmax warps 0-7: row r, column half `half` ----------------
+    // ---------------- softmax warps 0-7: rows of quarter `quad`, tiles of parity `par` ----------------
     const int quad = warp & 3;
-    const int half = warp >> 2;
+    const int par = warp >> 2;
+    const int half = par;                           // the epilogue's column half of O
     const int r = quad * 32 + lane;                 // row = TMEM lane
     const uint32_t lane_off = (uint32_t)((quad * 32) << 16);
     const int pair_bar = kBarPair + quad;           // mbarrier of the two warps sharing rows
+    float* mpub = reinterpret_cast<float*>(smem + kOffMPub) + quad * 64;  // [tile parity][lane]
     const float scale = p.scale_log2;
     // this row's request, head and record, looked up now so the loads finish during the tiles
     const int32_t row = rbase + r;
@@ -374,11 +381,11 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     }
     // keys this row may see end at row_end (slab coordinates): its own token + 1 when causal
     const int32_t row_end = (causal && row < rows) ? min(t1, row / g + 1) : t1;
-    float m_used = -INFINITY;  // running max in scaled (base-2) units, identical in both halves
-    float l = 0.f;             // this half's share of the row sum
+    float m_own = -INFINITY;   // max (scaled, base-2 units) used for this warp's latest tile
+    float l = 0.f;             // this warp's share of the row sum, relative to m_own
     int pair_phase = 0;
     bool ok = !*abort_flag;
-    for (int i = 0; ok && i < n_tiles; ++i) {
+    for (int i = par; ok && i < n_tiles; i += 2) {
       const int sb = i % kSBufs;
       ok = mbar_wait_bounded(bar(kBarSFull + sb), (i / kSBufs) & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);  // the TMEM loads below are warp-collective
@@ -386,65 +393,67 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
       tc_fence_after();
       const int valid = min(kN, t1 - t0 - i * kN);               // tokens of the tile in range
       const int valid_row = min(valid, row_end - t0 - i * kN);    // of those, keys this row sees
-      const uint32_t ts = tmem + lane_off + (uint32_t)(sb * kN + half * kHalfCols);
-      float s[kHalfCols];
-      {
-        uint32_t u[2][32];
-        GRANIKV_TMEM_LD32(ts, u[0]);
-        GRANIKV_TMEM_LD32(ts + 32, u[1]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = __uint_as_float(u[0][k]);
-          s[32 + k] = __uint_as_float(u[1][k]);
-        }
-      }
-      if (valid_row < kN) {
-#pragma unroll
-        for (int k = 0; k < kHalfCols; ++k) s[k] = half * kHalfCols + k < valid_row ? s[k] : -INFINITY;
-      }
-      // half-row max (scale > 0 commutes with max), swapped with the other half
+      const uint32_t ts = tmem + lane_off + (uint32_t)(sb * kN);
+      // row max over the 128 columns (scale > 0 commutes with max); S(i) is read again below
+      // for the exponentials, which keeps the thread's registers within the launch's budget
       float mx;
       {
-        static_assert(kHalfCols == 64, "the max tree below covers 64 columns");
-        float t[22], u[8];
+        static_assert(kN == 128, "the max tree below covers 128 columns");
+        uint32_t u[4][32];
+        GRANIKV_TMEM_LD32(ts, u[0]);
+        GRANIKV_TMEM_LD32(ts + 32, u[1]);
+        GRANIKV_TMEM_LD32(ts + 64, u[2]);
+        GRANIKV_TMEM_LD32(ts + 96, u[3]);
+        tmem_wait_ld();
+        if (valid_row < kN) {
 #pragma unroll
-        for (int k = 0; k < 21; ++k) t[k] = max3f(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
-        t[21] = s[63];
+          for (int k = 0; k < kN; ++k) u[k >> 5][k & 31] = k < valid_row ? u[k >> 5][k & 31] : 0xff800000u;
+        }
+        float sv[kN];
 #pragma unroll
-        for (int k = 0; k < 7; ++k) u[k] = max3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
-        u[7] = t[21];
-        mx = max3f(max3f(u[0], u[1], u[2]), max3f(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+        for (int k = 0; k < kN; ++k) sv[k] = __uint_as_float(u[k >> 5][k & 31]);
+        float t[43], w[15];
+#pragma unroll
+        for (int k = 0; k < 42; ++k) t[k] = max3f(sv[3 * k], sv[3 * k + 1], sv[3 * k + 2]);
+        t[42] = fmaxf(sv[126], sv[127]);
+#pragma unroll
+        for (int k = 0; k < 14; ++k) w[k] = max3f(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+        w[14] = t[42];
+        const float v0 = max3f(w[0], w[1], w[2]), v1 = max3f(w[3], w[4], w[5]), v2 = max3f(w[6], w[7], w[8]);
+        const float v3 = max3f(w[9], w[10], w[11]), v4 = max3f(w[12], w[13], w[14]);
+        mx = fmaxf(max3f(v0, v1, v2), fmaxf(v3, v4)) * scale;
       }
-      float* red_i = red + (i & 1) * 2 * kM;
-      red_i[half * kM + r] = mx;
-      mbar_arrive(bar(pair_bar));
-      ok = mbar_wait_bounded(bar(pair_bar), pair_phase & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
-      ++pair_phase;
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      mx = fmaxf(red_i[r], red_i[kM + r]) * scale;
-      // move the running max only when it grows by more than 2^kRescaleThreshold (both halves
-      // see the same row maxima, so both warps of a pair decide alike)
-      const bool first = (i == 0);
-      const bool warp_need = !first && __any_sync(0xffffffffu, mx > m_used + kRescaleThreshold);
-      if (first) {
-        m_used = mx;
-      } else if (warp_need) {
-        // O must hold PV(i-1) before it is rescaled; each half rescales its 64 columns of O
+      // the max used for tile i: that of tile i-1 (decided by the other warp of the quarter),
+      // moved only when this tile's row max exceeds it by more than 2^kRescaleThreshold
+      float m_i = mx;
+      bool warp_need = false;
+      float m_prev = -INFINITY;
+      if (i > 0) {
+        const int pp = (i - 1) & 1;
+        ok = mbar_wait_bounded(bar(kBarMPub + quad * 2 + pp), ((i - 1) >> 1) & 1, abort_flag, p.err, kDevTimeout,
+                               kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        m_prev = mpub[pp * 32 + lane];
+        warp_need = __any_sync(0xffffffffu, mx > m_prev + kRescaleThreshold);
+        m_i = warp_need ? fmaxf(m_prev, mx) : m_prev;
+      }
+      // publish at once, so the warp of tile i+1 is not held up by the rescale below (the slot's
+      // previous value, tile i-2's, was read by that warp before it published tile i-1's)
+      mpub[par * 32 + lane] = m_i;
+      mbar_arrive(bar(kBarMPub + quad * 2 + par));
+      if (warp_need) {
+        // O must hold PV(i-1) before it is rescaled, and PV(i) waits for P(i), written below
         ok = mbar_wait_bounded(bar(kBarPvDone + (i - 1) % kSBufs), ((i - 1) / kSBufs) & 1, abort_flag, p.err,
                                kDevTimeout, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float m_new = fmaxf(m_used, mx);
-        const float alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-        l *= alpha;
+        const float alpha = ex2_approx(m_prev - m_i);
         uint32_t u[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t ta = tmem + lane_off + kColO + half * 64 + c * 32;
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t ta = tmem + lane_off + kColO + c * 32;
           GRANIKV_TMEM_LD32(ta, u);
           tmem_wait_ld();
 #pragma unroll
@@ -453,23 +462,40 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         }
         tmem_wait_st();
       }
-      // P = 2^(s*scale - m) for this half's 64 columns, packed two per 32-bit column and written
-      // over columns [32*half, 32*half + 32) of the S(i) buffer (both halves have read S(i)).
-      // Every exponential goes to MUFU: moving a share of them to a polynomial on the FMA pipe
-      // made the tile slower on this GPU (the extra instructions cost more than MUFU time saved)
-      const uint64_t scale2 = f2_pack(scale, scale), nm2 = f2_pack(-m_used, -m_used);
+      if (m_own != m_i && m_own != -INFINITY) l *= ex2_approx(m_own - m_i);
+      m_own = m_i;
+      // P = 2^(s*scale - m) for the 128 columns, packed two per 32-bit column and written over
+      // columns [0, 64) of the S(i) buffer: S columns [64*hb, 64*hb + 64) are in registers
+      // before their P goes to columns [32*hb, 32*hb + 32).  Every exponential goes to MUFU:
+      // moving a share of them to a polynomial on the FMA pipe made the tile slower on this GPU
+      // (the extra instructions cost more than MUFU time saved)
+      const uint64_t scale2 = f2_pack(scale, scale), nm2 = f2_pack(-m_i, -m_i);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed partial row sums (0.0f bit patterns)
-      uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const uint64_t x = f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), scale2, nm2);
-        float xa, xb;
-        f2_unpack(x, xa, xb);
-        const uint64_t e = f2_pack(ex2_approx(xa), ex2_approx(xb));
-        acc[k & 3] = f2_add(acc[k & 3], e);
-        float a, b;
-        f2_unpack(e, a, b);
-        pk[k] = pack_bf16(a, b);
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t u[2][32];
+        GRANIKV_TMEM_LD32(ts + hb * 64, u[0]);
+        GRANIKV_TMEM_LD32(ts + hb * 64 + 32, u[1]);
+        tmem_wait_ld();
+        if (valid_row < kN) {  // masked keys: -inf, so their weight is 0
+#pragma unroll
+          for (int k = 0; k < 64; ++k) u[k >> 5][k & 31] = 64 * hb + k < valid_row ? u[k >> 5][k & 31] : 0xff800000u;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float sa = __uint_as_float(u[k >> 4][(2 * k) & 31]);
+          const float sb2 = __uint_as_float(u[k >> 4][(2 * k + 1) & 31]);
+          const uint64_t x = f2_fma(f2_pack(sa, sb2), scale2, nm2);
+          float xa, xb;
+          f2_unpack(x, xa, xb);
+          const uint64_t e = f2_pack(ex2_approx(xa), ex2_approx(xb));
+          acc[k & 3] = f2_add(acc[k & 3], e);
+          float a, b2;
+          f2_unpack(e, a, b2);
+          pk[k] = pack_bf16(a, b2);
+        }
+        GRANIKV_TMEM_ST32(tmem + lane_off + (uint32_t)(sb * kN + hb * 32), pk);
       }
       {
         const uint64_t t2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
@@ -477,32 +503,34 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
         f2_unpack(t2, la, lb);
         l += la + lb;
       }
-      GRANIKV_TMEM_ST32(tmem + lane_off + (uint32_t)(sb * kN + half * 32), pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + sb));
     }
-    // epilogue: wait for the last PV, add the two halves' row sums, normalise, write the record
+    // epilogue: wait for the last PV, combine the two warps' row sums (each relative to the max
+    // of its own latest tile; the last tile's max is the final one), normalise, write the record
     if (ok) {
       const int last = n_tiles - 1;
       ok = mbar_wait_bounded(bar(kBarPvDone + last % kSBufs), (last / kSBufs) & 1, abort_flag, p.err, kDevTimeout,
                              kWaitLimitNs);
     }
     ok = __all_sync(0xffffffffu, ok);
-    // swap the partial row sums with the other half at the pair barrier's next phase; a warp
-    // that left the tile loop early has made fewer pair arrivals, so its partner's bounded wait
-    // gives up and both skip the record
-    float* red_e = red + (pair_phase & 1) * 2 * kM;
-    red_e[half * kM + r] = ok ? l : -1.f;
+    // swap the row sums and maxima with the other warp at the pair barrier; a warp that left the
+    // tile loop early may stop waiting for published maxima, so its partner's bounded waits give
+    // up and both skip the record
+    red[par * kM + r] = ok ? l : -1.f;
+    red[2 * kM + par * kM + r] = m_own;
     mbar_arrive(bar(pair_bar));
     bool pair_ok = mbar_wait_bounded(bar(pair_bar), pair_phase & 1, abort_flag, p.err, kDevTimeout, kWaitLimitNs);
     ++pair_phase;
     pair_ok = __all_sync(0xffffffffu, pair_ok);
-    const float l0 = pair_ok ? red_e[r] : -1.f, l1 = pair_ok ? red_e[kM + r] : -1.f;
+    const float l0 = pair_ok ? red[r] : -1.f, l1 = pair_ok ? red[kM + r] : -1.f;
     ok = __all_sync(0xffffffffu, l0 >= 0.f && l1 >= 0.f);
     if (ok) {
       tc_fence_after();
-      const float lt = l0 + l1;
+      const float m_used = n_tiles > 0 ? red[2 * kM + ((n_tiles - 1) & 1) * kM + r] : -INFINITY;
+      const float m0 = red[2 * kM + r], m1 = red[2 * kM + kM + r];
+      const float lt = (l0 > 0.f ? l0 * ex2_approx(m0 - m_used) : 0.f) + (l1 > 0.f ? l1 * ex2_approx(m1 - m_used) : 0.f);
       if (!causal && row < rows && (rec < 0 || rec >= p.n_records)) {
         if (half == 0) atomicCAS(p.err, 0, (int32_t)kDevBadRecord);
         rec = -1;

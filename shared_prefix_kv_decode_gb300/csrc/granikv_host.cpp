@@ -1027,8 +1027,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   {
     // the merge gives a row with many records (a cascade step over all SMs has one per L_p
     // piece) several warps, so that each loads its share in one batch (8, 8, 16 or 24 records
-    // a warp for 1, 2, 4 or 8 warps)
-    p->merge_warps = max_parts <= 8 ? 1 : max_parts <= 16 ? 2 : max_parts <= 64 ? 4 : 8;
+    // a warp for 1, 2, 4 or 8 warps).  That only pays while the rows alone leave the SMs short
+    // of warps: past about 16 warps an SM, the rows' own loads hide each other's latency and the
+    // extra warps' combine step is pure cost, so W halves until the grid is back under that.
+    int32_t wpr = max_parts <= 8 ? 1 : max_parts <= 16 ? 2 : max_parts <= 64 ? 4 : 8;
+    const int64_t rows = (int64_t)B * c->cfg.n_q;
+    while (wpr > 1 && rows * wpr > 16LL * c->num_sms) wpr /= 2;
+    p->merge_warps = wpr;
   }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;
