@@ -54,6 +54,10 @@ enum {
 
 enum { GRANIKV_DTYPE_F32 = 0, GRANIKV_DTYPE_BF16 = 1 };
 
+/* Prefix backends ("3 GraniKV", dual attention backends).  Kernels per shape: bf16 with
+ * head_dim 128 -- dense on tcgen05 (kind::f16, TMA-fed), cascade as a bandwidth kernel over whole
+ * slot rows (g <= 128); fp32 with head_dim 32, 64, 96 or 128 -- dense on tcgen05 (kind::tf32 in
+ * split precision, fp32-accurate), cascade on CUDA cores; any other shape -- both on CUDA cores. */
 enum {
   GRANIKV_BACKEND_AUTO = 0,     /* per-group dispatch on M_eff >= M_sat                    */
   GRANIKV_BACKEND_DENSE = 1,    /* batched-GEMM prefix backend (tensor cores)              */

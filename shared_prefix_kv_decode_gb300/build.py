@@ -44,7 +44,7 @@ def sources():
 
 def _stamp(srcs, extra):
     h = hashlib.sha256()
-    for path in sorted(srcs + [os.path.join(CSRC, n) for n in os.listdir(CSRC) if n.endswith(".h")]
+    for path in sorted(srcs + [os.path.join(CSRC, n) for n in os.listdir(CSRC) if n.endswith((".h", ".cuh"))]
                        + [os.path.join(INCLUDE, n) for n in os.listdir(INCLUDE)]):
         h.update(path.encode())
         with open(path, "rb") as f:

@@ -155,6 +155,9 @@ int32_t prefix_impl_for(const granikv_ctx* c, int32_t backend) {
     if (c->g <= kCascadeStreamCols * kCascadeStreamWarps) return kImplCascadeStream;
     return kImplCascadeMma;
   }
+  if (c->cfg.dtype == GRANIKV_DTYPE_F32 && backend == GRANIKV_BACKEND_DENSE && c->cfg.head_dim % 32 == 0 &&
+      c->cfg.head_dim <= 128)
+    return kImplDenseTf32;
   return kImplGeneric;
 }
 
@@ -219,6 +222,7 @@ int32_t stream_sub_for(int32_t n_req, int32_t g) {
 int32_t rows_per_cta_for(int32_t impl, int32_t g, int32_t sub) {
   switch (impl) {
     case kImplDenseTc: return kDenseRows;
+    case kImplDenseTf32: return kDenseTf32Rows;
     case kImplCascadeMma: return kCascadeRows;
     case kImplCascadeStream: return (kCascadeStreamCols * sub / g) * g;
     default: return kGenericRows;
@@ -228,6 +232,7 @@ int32_t rows_per_cta_for(int32_t impl, int32_t g, int32_t sub) {
 int32_t tile_tokens_for(int32_t impl, int32_t sub) {
   switch (impl) {
     case kImplDenseTc: return kDenseTile;
+    case kImplDenseTf32: return kDenseTf32Tile;
     case kImplCascadeMma: return kCascadeTile;
     case kImplCascadeStream: return kCascadeStreamTile * sub;
     default: return kGenericTile;
@@ -745,10 +750,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const bool fast_suffix_pre = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   bool fused = c->fused_merge && (fast_suffix_pre || T_all == 0);
   for (int32_t i = 0; i < G; ++i)
-    if (groups[i].impl == kImplGeneric) fused = false;
+    if (groups[i].impl == kImplGeneric || groups[i].impl == kImplDenseTf32) fused = false;
   bool fast_all = fast_suffix_pre || T_all == 0;
   for (int32_t i = 0; i < G; ++i)
-    if (groups[i].impl == kImplGeneric) fast_all = false;
+    if (groups[i].impl == kImplGeneric || groups[i].impl == kImplDenseTf32) fast_all = false;
   bool concurrent = fast_all && c->concurrent && G > 0 && T_all > 0;
   const bool split_sms = concurrent && c->prefix_share < 0.999f;
   const bool auto_share = split_sms && c->prefix_share <= 0.f;
@@ -1264,6 +1269,10 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
       r = launch_prefix_generic(c->cfg.dtype, a, p->pitem_first[kImplGeneric], p->pitem_count[kImplGeneric], st);
       c->n_kernels += 1;
     }
+    if (r == cudaSuccess && p->pitem_count[kImplDenseTf32] > 0) {
+      r = launch_dense_tf32(a, p->pitem_first[kImplDenseTf32], p->pitem_count[kImplDenseTf32], st);
+      c->n_kernels += 1;
+    }
     if (r == cudaSuccess && p->pitem_count[kImplCascadeMma] > 0) {
       r = launch_cascade_mma(a, p->pitem_first[kImplCascadeMma], p->pitem_count[kImplCascadeMma], st);
       c->n_kernels += 1;
@@ -1276,7 +1285,7 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
     if (r == cudaSuccess && p->pitem_count[kImplDenseTc] > 0) {
       if (!c->has_tmaps) return cudaErrorNotSupported;
       const bool first = p->pitem_count[kImplGeneric] == 0 && p->pitem_count[kImplCascadeMma] == 0 &&
-                         p->pitem_count[kImplCascadeStream] == 0;
+                         p->pitem_count[kImplCascadeStream] == 0 && p->pitem_count[kImplDenseTf32] == 0;
       r = launch_dense_tc(a, p->pitem_first[kImplDenseTc], p->pitem_count[kImplDenseTc], c->tmap_k[layer],
                           c->tmap_v[layer], tmq, st, first);
       c->n_kernels += 1;

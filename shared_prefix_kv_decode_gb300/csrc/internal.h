@@ -31,7 +31,8 @@ enum Impl : int32_t {
   kImplCascadeMma = 1,// bf16, head_dim 128: warp-level tensor-core cascade kernel
   kImplDenseTc = 2,   // bf16, head_dim 128: tcgen05/TMEM dense kernel
   kImplSuffixMma = 3, // bf16, head_dim 128, g <= 8: warp-level tensor-core suffix kernel
-  kImplCascadeStream = 4,  // bf16, head_dim 128, g <= 16: cascade over whole 2 KB slot rows
+  kImplCascadeStream = 4,  // bf16, head_dim 128, g <= 128: cascade over whole 2 KB slot rows
+  kImplDenseTf32 = 5,      // f32, head_dim % 32 == 0 up to 128: tcgen05 kind::tf32 dense kernel
 };
 
 // Geometry of each prefix kernel: query rows per CTA and tokens per tile.  The planner and the
@@ -39,6 +40,7 @@ enum Impl : int32_t {
 constexpr int kGenericRows = 16, kGenericTile = 32;
 constexpr int kCascadeRows = 128, kCascadeTile = 64;
 constexpr int kDenseRows = 128, kDenseTile = 128;
+constexpr int kDenseTf32Rows = 128, kDenseTf32Tile = 32;
 // The streaming cascade kernel: eight consumer warps, each over 16-token sub-tiles and at most 16
 // query columns (request, head-in-group pairs) of one KV head; with `sub` warps per KV head a
 // CTA covers 8 / sub KV heads and 16 * sub columns of each.
@@ -155,6 +157,8 @@ cudaError_t launch_cascade_mma(const AttnParams& p, int32_t first_item, int32_t 
 cudaError_t launch_dense_tc(const AttnParams& p, int32_t first_item, int32_t n_items, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, const CUtensorMap& tmq, cudaStream_t s, bool pdl);
 cudaError_t launch_cascade_stream(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s, bool pdl);
+// fp32 dense prefix items on the tcgen05 tensor cores (kind::tf32); head_dim 32, 64, 96 or 128.
+cudaError_t launch_dense_tf32(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 // One launch for the prefix and suffix work: CTAs [0, n_dense) run dense prefix items
 // first_dense.., the next n_casc the streaming cascade items first_casc.., the rest the suffix
 // token-CTAs (n_scta per KV-head group of eight).
@@ -166,7 +170,7 @@ cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_dense, in
 // each row's records.
 cudaError_t launch_merge_rows(const AttnParams& p, int32_t warps_per_row, cudaStream_t s, bool pdl);
 
-constexpr int kNumImpl = 5;
+constexpr int kNumImpl = 6;
 
 }  // namespace granikv
 

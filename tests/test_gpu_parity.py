@@ -2,8 +2,9 @@
 
 Tolerances, for bf16 inputs with fp32 accumulation: o max-abs <= 1e-2, mean-abs <= 1e-3,
 lse max-abs <= 1e-3, plus relative L2 error <= 1e-2 (the near-uniform softmax of the Llama
-shape makes |o| ~ 0.01, where an absolute bound alone says little).  fp32 inputs: the
-CUDA-core paths within 1e-5; the tensor-core dense path on fp32 is held to the bf16 bounds.
+shape makes |o| ~ 0.01, where an absolute bound alone says little).  fp32 inputs: every path
+within 1e-5, the tf32 tensor-core dense path included (it runs each product in split precision,
+hi and lo tf32 parts, so its results are fp32-accurate).
 Indices (COLD token tables) must match the oracle's ring restatement bit for bit.
 """
 
@@ -69,7 +70,7 @@ def test_tiny_fp32(cuda_ok, seed, backend):
     lw = _load(wl)
     o, lse = _run(lw, backend)
     o_ref, lse_ref = OA.decode_attention(wl)
-    assert_close(o, lse, o_ref, lse_ref, "f32", f"tiny seed {seed} {backend}", dense=(backend == "dense"))
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"tiny seed {seed} {backend}")
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -91,7 +92,7 @@ def test_small_mixed_fp32(cuda_ok, backend):
     lw = _load(wl)
     o, lse = _run(lw, backend)
     o_ref, lse_ref = OA.decode_attention(wl)
-    assert_close(o, lse, o_ref, lse_ref, "f32", f"small_mixed fp32 {backend}", dense=(backend == "dense"))
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"small_mixed fp32 {backend}")
 
 
 @pytest.mark.parametrize("backend", BACKENDS)
@@ -180,18 +181,52 @@ def test_cold_slot_permutation_invariance(cuda_ok, backend):
 
 @pytest.mark.parametrize("shape", ["bf16_d128", "f32_d64"])
 def test_backends_agree(cuda_ok, shape):
-    """Forced dense and forced cascade give the same attention.  Meaningful where the two
-    backends are different kernels (bf16, head_dim 128: tcgen05 dense vs the bandwidth cascade);
-    fp32 and other head sizes run one CUDA-core prefix kernel for both, so there the comparison
-    would be of a kernel with itself (each backend is still checked against the oracle by the
-    tiny and small-mixed fp32 tests)."""
+    """Forced dense and forced cascade give the same attention, and are different kernels: bf16
+    / head_dim 128 runs the tcgen05 dense kernel against the bandwidth cascade, fp32 the tf32
+    tcgen05 dense kernel against the CUDA-core cascade (their outputs differ in the last bits,
+    so they are not one kernel run twice).  bf16: within the bf16 bounds of each other; fp32:
+    within 2e-5 (each is within 1e-5 of the oracle)."""
     if shape == "f32_d64":
-        pytest.skip("fp32 / head_dim 64: both backends run the same CUDA-core prefix kernel")
-    wl = W.small_mixed(8, dtype="bf16", q_scale=1.0)
+        wl = W.small_mixed(8, dtype="f32", n_q=8, n_kv=2, d=64, q_scale=1.0)
+    else:
+        wl = W.small_mixed(8, dtype="bf16", q_scale=1.0)
     lw = _load(wl)
     od, ld = _run(lw, "dense")
     oc, lc = _run(lw, "cascade")
-    assert np.max(np.abs(od - oc)) <= 1e-2 and np.max(np.abs(ld - lc)) <= 1e-3
+    tol_o, tol_l = (2e-5, 2e-5) if shape == "f32_d64" else (1e-2, 1e-3)
+    assert np.max(np.abs(od - oc)) <= tol_o and np.max(np.abs(ld - lc)) <= tol_l
+    assert not np.array_equal(od, oc)
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
+@pytest.mark.parametrize("q_scale", [1.0 / 8.0, 1.0])
+def test_fp32_dense_tensor_core_head_dims(cuda_ok, d, q_scale):
+    """The tf32 dense kernel at every head size it serves (32, 64, 96, 128: one to four 32-wide
+    column blocks of the swizzled operands), ragged prefixes (1000 and 333 tokens: ragged last
+    32-token tiles) and a peaked query scale, against the oracle within the fp32 bounds."""
+    wl = W.small_mixed(6, dtype="f32", n_q=8, n_kv=2, d=d, q_scale=q_scale)
+    lw = _load(wl)
+    o, lse = _run(lw, "dense")
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"fp32 dense d {d} q {q_scale}")
+
+
+def test_fp32_dense_several_row_blocks(cuda_ok):
+    """fp32, 48 requests of one ragged prefix (g = 4: 192 rows per KV head, two 128-row blocks,
+    the second partial) over several L_p pieces: the tf32 dense kernel against the oracle, and
+    the CUDA-core cascade backend on the same batch within the fp32 bounds."""
+    from workloads.synth import Workload, WorkloadSpec
+    rng = np.random.default_rng(11)
+    spec = WorkloadSpec(name="fp32_rows", dtype="f32", n_q=8, n_kv=2, d=64, prefix_lens=[1500],
+                        req_prefix=[0] * 48, suffix_lens=[int(x) for x in rng.integers(1, 80, size=48)],
+                        q_scale=0.5, n_slots=8192, prefix_in_hot=[True], needles=[], schedule_max_chunk=32)
+    wl = Workload(spec, 11)
+    lw = _load(wl)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    o, lse = _run(lw, "dense")
+    assert_close(o, lse, o_ref, lse_ref, "f32", "fp32 dense 192 rows")
+    o, lse = _run(lw, "cascade")
+    assert_close(o, lse, o_ref, lse_ref, "f32", "fp32 cascade 192 rows")
 
 
 @pytest.mark.parametrize("backend", ["dense", "cascade"])
