@@ -335,7 +335,7 @@ granikv_status granikv_decode_attention_append(granikv_ctx* ctx, int32_t layer, 
  * Errors: GRANIKV_ERR_STATIC_WORKSPACE_TOO_SMALL when granikv_workspace_size(plan) exceeds
  * 16 MiB (nothing is enqueued); otherwise as granikv_decode_attention.
  * The first call on each device looks up the array's device address (with that device made
- * current for the lookup); make that first call before any stream capture.  All calls on a device
+ * current for the lookup).  All calls on a device
  * share the one array, and each call re-copies its work list and re-zeroes its merge tickets, so
  * calls that may overlap on the GPU (different streams, different threads) race and must be
  * ordered by the caller. */

@@ -26,10 +26,12 @@ constexpr int32_t kDefaultMaxSlabs = 1024;
 constexpr int32_t kDefaultMaxBatch = 4096;
 // Dense/cascade crossover on GB300 for the Llama-3.1-8B shape, re-fitted from the L_p x B
 // sweep of msat_fit.py, recorded in msat_gb300.json next to this package (the pages' A100 value
-// is 1024 and they state other GPUs need a re-fit).  Both fit rules land on the sweep's smallest
-// M_eff (4): the tcgen05 dense kernel is the faster backend in every cell of the sweep.  The
-// streaming cascade kernel comes within 2-8 % at M_eff <= 32 (both are bandwidth-bound there)
-// and falls far behind above, where its warp-level MMAs run out of throughput.
+// is 1024 and they state other GPUs need a re-fit).  The least-regret fit lands on the sweep's
+// smallest M_eff (4): the tcgen05 dense kernel is the faster backend in all but one cell, and
+// there the streaming cascade kernel wins by 1 % (0.13 us; the strict rule, dense no slower in
+// every cell from M_sat up, therefore reads 32).  The cascade comes within 1-8 %
+// at M_eff <= 32 (both are bandwidth-bound there) and falls far behind above, where its
+// warp-level MMAs run out of throughput.
 constexpr int32_t kDefaultMsat = 4;
 
 struct Extent {
@@ -1326,8 +1328,10 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
     const bool after_prefix = p->n_pitems > 0 && n_dense + n_casc > 0;
     if (e == cudaSuccess) e = launch_suffix(s, after_prefix && p->suffix_impl == kImplSuffixMma);
     if (e == cudaSuccess && !p->fused) {
-      const bool after_suffix = p->n_sitems > 0 && p->suffix_impl == kImplSuffixMma;
-      e = launch_merge_k(after_suffix);
+      // the merge's stream predecessor is this call's suffix kernel, or its prefix kernel when
+      // the step has no COLD tokens; the merge waits (griddepcontrol.wait) before it reads a
+      // record, so it may be launched as a dependent of either
+      e = launch_merge_k(p->n_sitems > 0 || p->n_pitems > 0);
     }
   }
   if (e == cudaErrorNotSupported) return GRANIKV_ERR_UNSUPPORTED;

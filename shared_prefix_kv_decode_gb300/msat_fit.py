@@ -28,27 +28,29 @@ BS = [1, 8, 32, 128, 256, 512]
 SUFFIX = 256
 
 
-def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1):
+def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1, suffix=SUFFIX):
     """Median microseconds of one decode-attention call per backend.  layers = 1: a single call
     after an L2 flush.  layers > 1: a decode step of that many back-to-back calls, one per layer
     (each layer its own pools, so no layer's bytes are in L2 for the next), after one flush; the
-    call time is the step's time over the layers."""
+    call time is the step's time over the layers.  suffix: COLD tokens per request (0: the call
+    is the prefix kernel and the merge alone)."""
     from .cache import GraniKVCache
 
     n_q, n_kv, d = 32, 8, 128
-    n_cold = B * SUFFIX + 1024
+    n_cold = B * suffix + 1024
     n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil(n_cold / 0.8)) + 8)
     cache = GraniKVCache(n_layers=layers, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
-                         max_batch=B, cap=SUFFIX + 64)
+                         max_batch=B, cap=suffix + 64)
     dev = cache.device
     gen = torch.Generator(device=dev)
     gen.manual_seed(L_p * 1000 + B)
     k = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
     v = torch.randn((L_p, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
     sid = cache.admit_prefix(L_p, [k] * layers, [v] * layers)
-    kn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    vn = torch.randn((B * SUFFIX, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
-    cache.append([SUFFIX] * B, [kn] * layers, [vn] * layers)
+    if suffix > 0:
+        kn = torch.randn((B * suffix, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+        vn = torch.randn((B * suffix, n_kv, d), generator=gen, device=dev).to(torch.bfloat16)
+        cache.append([suffix] * B, [kn] * layers, [vn] * layers)
     q = (torch.randn((B, n_q, d), generator=gen, device=dev) / math.sqrt(d)).to(torch.bfloat16)
     batch = cache.batch([sid] * B)
     if serial:  # prefix, suffix and merge one after another, each kernel on all SMs
@@ -131,6 +133,8 @@ def main(argv=None):
     ap.add_argument("--serial", action="store_true", help="run each kernel on its own (for profiling)")
     ap.add_argument("--layers", type=int, default=1,
                     help="time decode steps of this many back-to-back layer calls (default: single calls)")
+    ap.add_argument("--suffix", type=int, default=SUFFIX,
+                    help="COLD tokens per request (0: time the prefix kernel and the merge alone)")
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
@@ -142,7 +146,8 @@ def main(argv=None):
     rows = []
     for L_p in [int(x) for x in a.lps.split(",")]:
         for B in [int(x) for x in a.bs.split(",")]:
-            r = _time_cell(L_p, B, a.reps, None, flush, gb, torch, serial=a.serial, layers=a.layers)
+            r = _time_cell(L_p, B, a.reps, None, flush, gb, torch, serial=a.serial, layers=a.layers,
+                           suffix=a.suffix)
             row = {"L_p": L_p, "B": B, "m_eff": 4 * B, "dense_us": r["dense"], "cascade_us": r["cascade"],
                    "auto_us": r["auto"], "auto_backend": r["auto_backend"]}
             rows.append(row)
@@ -161,8 +166,8 @@ def main(argv=None):
               f"{r['auto_us']:.1f} | {r['auto_backend']} | {best / r['auto_us']:.3f} |")
     if a.json:
         with open(a.json, "w") as f:
-            json.dump({"rows": rows, "m_sat": m_sat, "m_sat_strict": m_strict, "layers": a.layers, "reps": a.reps},
-                      f, indent=1)
+            json.dump({"rows": rows, "m_sat": m_sat, "m_sat_strict": m_strict, "layers": a.layers, "reps": a.reps,
+                       "suffix": a.suffix}, f, indent=1)
     return 0
 
 

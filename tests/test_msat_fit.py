@@ -40,10 +40,11 @@ def test_always_and_never():
 
 
 def test_committed_gb300_sweep_fits_the_built_in_threshold():
-    """The GB300 sweep committed with the package (the table the built-in M_sat comes from):
-    both fit rules give the library's default M_sat of 4 (the dense backend from the smallest
-    M_eff of the grid), and the dispatched call is within 2 % of the faster single backend in
-    every cell ("3 GraniKV", per-step dispatch: never slower than either backend alone)."""
+    """The GB300 sweep committed with the package (the table the built-in M_sat comes from): the
+    least-regret fit gives the library's default M_sat of 4 (the dense backend from the smallest
+    M_eff of the grid), the recorded strict-rule threshold is what the strict rule gives on the
+    table, and the dispatched call is within 2 % of the faster single backend in every cell
+    ("3 GraniKV", per-step dispatch: never slower than either backend alone)."""
     import json
     import os
     from shared_prefix_kv_decode_gb300 import msat_fit as MF
@@ -53,7 +54,7 @@ def test_committed_gb300_sweep_fits_the_built_in_threshold():
     rows = d["rows"]
     assert len(rows) == 30 and {r["L_p"] for r in rows} == {512, 2048, 8192, 16384, 32768}
     assert MF.fit_msat(rows) == d["m_sat"] == 4
-    assert MF.fit_msat_strict(rows) == d["m_sat_strict"] == 4
+    assert MF.fit_msat_strict(rows) == d["m_sat_strict"]
     worst = max(rows, key=MF.dispatch_ratio)
     assert MF.dispatch_ratio(worst) <= 1.02, worst
 
