@@ -4,7 +4,7 @@ GraniKV (arXiv:2608.15584), "3 GraniKV" per-step dispatch and "B.4 Per-Step Disp
 Trace": the dispatcher runs the dense backend when M_eff = B * n_q / n_kv >= M_sat; the pages
 measure M_sat = 1024 on A100 and say other GPUs need a re-fit ("Limitations").
 
-This sweeps the Llama-3.1-8B attention shape (32/8/128, bf16) over
+This sweeps the Llama-3.1-8B attention shape (32/8/128, bf16; --n-q 40 for the Qwen-2.5 TP1 shape) over
 L_p in {512, 2048, 8192, 16384, 32768} x B in {1, 8, 32, 128, 256, 512} with 256 COLD tokens
 per request, timing decode attention with the backend forced to DENSE, forced to CASCADE, and
 dispatched (AUTO).  The L2 is flushed before every timed call (or, with --layers N, before every
@@ -28,15 +28,15 @@ BS = [1, 8, 32, 128, 256, 512]
 SUFFIX = 256
 
 
-def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1, suffix=SUFFIX):
+def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1, suffix=SUFFIX, n_q=32):
     """Median microseconds of one decode-attention call per backend.  layers = 1: a single call
     after an L2 flush.  layers > 1: a decode step of that many back-to-back calls, one per layer
     (each layer its own pools, so no layer's bytes are in L2 for the next), after one flush; the
     call time is the step's time over the layers.  suffix: COLD tokens per request (0: the call
-    is the prefix kernel and the merge alone)."""
+    is the prefix kernel and the merge alone).  n_q: query heads (8 KV heads of 128 dims)."""
     from .cache import GraniKVCache
 
-    n_q, n_kv, d = 32, 8, 128
+    n_kv, d = 8, 128
     n_cold = B * suffix + 1024
     n_slots = max(int(math.ceil(L_p / 0.2)) + 8, int(math.ceil(n_cold / 0.8)) + 8)
     cache = GraniKVCache(n_layers=layers, n_q=n_q, n_kv=n_kv, head_dim=d, dtype=gb.DTYPE_BF16, n_slots=n_slots,
@@ -133,6 +133,7 @@ def main(argv=None):
     ap.add_argument("--serial", action="store_true", help="run each kernel on its own (for profiling)")
     ap.add_argument("--layers", type=int, default=1,
                     help="time decode steps of this many back-to-back layer calls (default: single calls)")
+    ap.add_argument("--n-q", type=int, default=32, help="query heads (40: the Qwen-2.5 TP1 shape)")
     ap.add_argument("--suffix", type=int, default=SUFFIX,
                     help="COLD tokens per request (0: time the prefix kernel and the merge alone)")
     a = ap.parse_args(argv)
@@ -147,14 +148,14 @@ def main(argv=None):
     for L_p in [int(x) for x in a.lps.split(",")]:
         for B in [int(x) for x in a.bs.split(",")]:
             r = _time_cell(L_p, B, a.reps, None, flush, gb, torch, serial=a.serial, layers=a.layers,
-                           suffix=a.suffix)
-            row = {"L_p": L_p, "B": B, "m_eff": 4 * B, "dense_us": r["dense"], "cascade_us": r["cascade"],
+                           suffix=a.suffix, n_q=a.n_q)
+            row = {"L_p": L_p, "B": B, "m_eff": B * a.n_q // 8, "dense_us": r["dense"], "cascade_us": r["cascade"],
                    "auto_us": r["auto"], "auto_backend": r["auto_backend"]}
             rows.append(row)
             print(json.dumps(row), flush=True)
             torch.cuda.empty_cache()
-    m_sat = fit_msat(rows)
-    m_strict = fit_msat_strict(rows)
+    m_sat = fit_msat(rows, g=a.n_q // 8)
+    m_strict = fit_msat_strict(rows, g=a.n_q // 8)
     worst = max(rows, key=dispatch_ratio)
     print(f"# fitted M_sat = {m_sat} (least regret); strict rule: {m_strict}; "
           f"worst dispatched / best backend: {dispatch_ratio(worst):.3f} at L_p {worst['L_p']} B {worst['B']}")
