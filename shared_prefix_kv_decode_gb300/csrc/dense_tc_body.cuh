@@ -191,20 +191,40 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
   grid_dep_launch_dependents();
   // Q rows of this block -> shared memory, K-major with 128-byte swizzle: row r, 16-byte
   // chunk c lives in 64-dim block c/8 at r*128 + ((c%8) ^ (r%8))*16 (the layout the TMA box
-  // load produces); rows past the group are 0
-  for (int idx = q_tma ? kM * 16 : tid; idx < kM * 16; idx += kThreads) {
-    const int r = idx >> 4;
-    const int c = idx & 15;
-    const int32_t row = rbase + r;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (row < rows) {
-      const int32_t b = p.group_req[gr.req_begin + row / g];
-      const int32_t h = j * g + row % g;
-      v = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.n_q + h) * kD)[c];
+  // load produces); rows past the group are 0.  A thread's chunks are gathered in three passes
+  // (all request lookups, then all q loads, then the stores), so its loads are in flight together
+  if (!q_tma) {
+    constexpr int kQIters = (kM * 16 + kThreads - 1) / kThreads;
+    int32_t qoff[kQIters];
+#pragma unroll
+    for (int k = 0; k < kQIters; ++k) {
+      const int idx = tid + k * kThreads;
+      const int32_t row = rbase + (idx >> 4);
+      qoff[k] = -1;
+      if (idx < kM * 16 && row < rows) qoff[k] = p.group_req[gr.req_begin + row / g];
     }
-    const uint32_t dst = sQ + (c >> 3) * (kM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
+    uint4 qv[kQIters];
+#pragma unroll
+    for (int k = 0; k < kQIters; ++k) {
+      const int idx = tid + k * kThreads;
+      const int32_t row = rbase + (idx >> 4);
+      qv[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (qoff[k] >= 0)
+        qv[k] = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                               ((int64_t)qoff[k] * p.n_q + j * g + row % g) * kD)[idx & 15];
+    }
+#pragma unroll
+    for (int k = 0; k < kQIters; ++k) {
+      const int idx = tid + k * kThreads;
+      if (idx < kM * 16) {
+        const int r = idx >> 4;
+        const int c = idx & 15;
+        const uint32_t dst = sQ + (c >> 3) * (kM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(qv[k].x), "r"(qv[k].y), "r"(qv[k].z),
+                     "r"(qv[k].w)
+                     : "memory");
+      }
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
