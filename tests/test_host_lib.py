@@ -314,3 +314,43 @@ def test_concurrency_share_sizes_prefix_pieces(granikv_lib):
     for bad in (-0.1, 1.5, float("nan")):
         with pytest.raises(gb.GranikvError):
             ctx.set_concurrency(True, bad)
+
+
+def _group_kernel(plan):
+    """(kernel implementation, query rows a CTA, tokens a tile) of the plan's first prefix group,
+    read from its device image (the group records lead the image; 64 bytes each: slab offset,
+    then int32 L_p, n_req, req_begin, n_splits, split_len, backend, impl, rows_per_cta,
+    row_blocks, n_long, tile, ...)."""
+    import struct
+    img = plan.image()
+    f = struct.unpack_from("<q14i", img, 0)
+    impl, rows_per_cta, tile = f[7], f[8], f[11]
+    return impl, rows_per_cta, tile
+
+
+@pytest.mark.parametrize("shape", ["bf16_d128", "f32_d64", "f32_d96", "f32_d256", "bf16_d64"])
+def test_backend_kernels_per_shape(granikv_lib, shape):
+    """Which kernel each forced backend runs ("3 GraniKV": dense = a batched GEMM on the tensor
+    cores, cascade = the prefix read once per step): bf16 / d 128 -> tcgen05 dense (128 rows, 128-
+    token tiles) and the streaming cascade; fp32 / d <= 128 -> tf32 tcgen05 dense (128 rows, 32-
+    token tiles) and the CUDA-core cascade; other shapes -> the CUDA-core kernel for both."""
+    dtype, d = shape.split("_d")
+    d = int(d)
+    ctx = gb.Context(n_layers=1, n_q=8, n_kv=2, head_dim=d,
+                     dtype=gb.DTYPE_BF16 if dtype == "bf16" else gb.DTYPE_F32, n_slots=20000,
+                     hot_fraction=0.2, max_slabs=4, m_sat=1024, host_only=True)
+    sid, _ = ctx.hot_alloc(1000)
+    batch = gb.Batch([sid] * 4, [20] * 4, 0, 64)
+    got = {}
+    for name, backend in (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE)):
+        ctx.force_backend(backend)
+        got[name] = _group_kernel(ctx.dispatch(batch, ctx.plan()))
+    generic = (0, 16, 32)        # CUDA-core kernel: 16 rows, 32-token tiles
+    if shape == "bf16_d128":
+        assert got["dense"] == (2, 128, 128)
+        assert got["cascade"][0] == 4 and got["cascade"][2] == 16   # streaming cascade, 16-token stages
+    elif shape in ("f32_d64", "f32_d96"):
+        assert got["dense"] == (5, 128, 32)
+        assert got["cascade"] == generic
+    else:
+        assert got["dense"] == generic and got["cascade"] == generic
