@@ -481,14 +481,15 @@ def test_full_size_whole_batch_through_the_benchmarked_call(cuda_ok):
     assert_close(o, lse, o_ref, lse_ref, "bf16", "llama8b whole batch, fused append")
 
 
-@pytest.mark.parametrize("shape", [(32, 16), (8, 8), (64, 8), (16, 2), (64, 2)])
+@pytest.mark.parametrize("shape", [(32, 16), (8, 8), (64, 8), (16, 2), (64, 2), (160, 1)])
 @pytest.mark.parametrize("backend", BACKENDS)
 def test_head_shapes(cuda_ok, shape, backend):
     """GQA shapes besides the configurations': more than eight KV heads (two head groups in the
     suffix and streaming cascade kernels), one query head per KV head (g = 1), g = 8, two KV
-    heads, and g = 32 (beyond the streaming cascade kernel's 16 query columns: the warp-MMA
-    cascade kernel and the CUDA-core suffix kernel); bf16, d = 128, the small mixed batch (ragged
-    prefixes, a prefix-only and a prefix-less request)."""
+    heads, g = 32 (the streaming cascade with several warps a KV head; the CUDA-core suffix
+    kernel) and g = 160 (past the streaming cascade's 128 query columns: the warp-MMA cascade
+    kernel; a request's rows span two 128-row dense blocks); bf16, d = 128, the small mixed batch
+    (ragged prefixes, a prefix-only and a prefix-less request)."""
     n_q, n_kv = shape
     wl = W.small_mixed(4, dtype="bf16", n_q=n_q, n_kv=n_kv, q_scale=1.0)
     lw = _load(wl)
@@ -510,6 +511,23 @@ def test_single_request(cuda_ok, backend, lens):
     o, lse = _run(lw, backend)
     o_ref, lse_ref = OA.decode_attention(wl)
     assert_close(o, lse, o_ref, lse_ref, "bf16", f"single {lens} {backend}")
+
+
+@pytest.mark.parametrize("backend", ["dense", "cascade"])
+def test_fp32_tile_boundaries(cuda_ok, backend):
+    """fp32 (d = 64): prefixes of 1, 31, 32, 33 and 65 tokens (around the tf32 dense kernel's
+    32-token tiles and the CUDA-core kernel's), groups of 1 to 3 requests, suffixes of 0 to 2
+    tokens, within the fp32 bounds."""
+    lps = [1, 31, 32, 33, 65]
+    req_prefix = [0, 1, 1, 2, 2, 2, 3, 4, 4]
+    spec = W.WorkloadSpec(name="fp32_edges", dtype="f32", n_q=8, n_kv=2, d=64, prefix_lens=lps,
+                          req_prefix=req_prefix, suffix_lens=[i % 3 for i in range(len(req_prefix))],
+                          q_scale=1.0, n_slots=4096)
+    wl = W.Workload(spec, 17)
+    lw = _load(wl)
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "f32", f"fp32 tile edges {backend}")
 
 
 @pytest.mark.parametrize("shape,prefix_lens,group_sizes", [
