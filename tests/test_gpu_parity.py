@@ -385,6 +385,29 @@ def test_full_size_sampled(cuda_ok, name):
         assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
+def test_largest_batch(cuda_ok):
+    """B = 4096, the default largest batch of a context: two prefixes (384 and 1000 tokens),
+    requests alternating between them, 1-8 COLD tokens each.  The dense kernel runs 64 row
+    blocks per KV head and group (8192 rows), the merge 131,072 rows, each suffix token-CTA
+    dozens of requests.  Every backend, checked on sampled requests the oracle computes
+    one by one; every output finite."""
+    B = 4096
+    rng = np.random.default_rng(4096)
+    spec = W.WorkloadSpec(name="largest_batch", dtype="bf16", n_q=32, n_kv=8, d=128, prefix_lens=[384, 1000],
+                          req_prefix=[b % 2 for b in range(B)],
+                          suffix_lens=[int(x) for x in rng.integers(1, 9, size=B)], q_scale=1.0,
+                          n_slots=65536, schedule_max_chunk=8)
+    wl = W.Workload(spec, 5)
+    lw = _load(wl)
+    sample = [0, 1, 2, 1023, 2048, 2049, 3333, 4094, 4095]
+    refs = {b: OA.request_attention(wl, b) for b in sample}
+    for backend in BACKENDS:
+        o, lse = _run(lw, backend)
+        for b in sample:
+            assert_close(o[b], lse[b], refs[b][0], refs[b][1], "bf16", f"largest batch b={b} {backend}")
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
 @pytest.mark.parametrize("backend", ["dense", "cascade"])
 def test_hot_layout_equals_paged_equivalent_layout(cuda_ok, backend):
     """The comparator's batch (one shared prefix, every request with its own suffix) stored with
