@@ -385,6 +385,22 @@ def test_full_size_sampled(cuda_ok, name):
         assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
+@pytest.mark.parametrize("backend", BACKENDS)
+def test_slab_fills_hot_and_table_fills_cap(cuda_ok, backend):
+    """A prefix as long as the whole HOT range (1638 of 8192 slots: the slab ends exactly at the
+    HOT/COLD boundary) and a token table filled to its capacity (64 COLD tokens, cap 64), next
+    to a short suffix and an empty one."""
+    spec = W.WorkloadSpec(name="hot_full", dtype="bf16", n_q=32, n_kv=8, d=128, prefix_lens=[1638],
+                          req_prefix=[0, 0, 0], suffix_lens=[64, 5, 0], q_scale=1.0, n_slots=8192)
+    wl = W.Workload(spec, 9)
+    lw = _load(wl, cap=64)
+    off, L = lw.cache.ctx.hot_info(lw.slab_ids[0])
+    assert off == 0 and off + L == lw.cache.n_hot
+    o, lse = _run(lw, backend)
+    o_ref, lse_ref = OA.decode_attention(wl)
+    assert_close(o, lse, o_ref, lse_ref, "bf16", f"HOT-filling slab {backend}")
+
+
 def test_largest_batch(cuda_ok):
     """B = 4096, the default largest batch of a context: two prefixes (384 and 1000 tokens),
     requests alternating between them, 1-8 COLD tokens each.  The dense kernel runs 64 row
