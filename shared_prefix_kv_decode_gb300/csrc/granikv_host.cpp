@@ -121,6 +121,11 @@ struct granikv_plan {
     std::vector<char> grp_contig;         // group's requests consecutive in the batch
     bool pitems_cached = false;
     std::vector<int32_t> pitems_key;      // the group fields the prefix items depend on
+    // The serial dense schedule's choice of piece length (see the planner), memoised on the
+    // groups' tile counts: tail_key -> tail_len (0: the balanced one-wave pieces).
+    std::vector<int64_t> tail_key, tail_key_now, sim_heap;
+    int64_t tail_len = 0;
+    std::vector<char> grp_tail;           // group's last piece is a shorter remainder
   } scratch;
 };
 
@@ -857,6 +862,78 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       dg.q_b0 = -1;
       dg.causal = 0;
     }
+    // Serial schedule, dense groups only (the dense kernel on all SMs by itself): when the
+    // units do not divide into the SMs, the balanced one-wave pieces leave SMs idle (40 units of
+    // the Qwen-2.5 shape: 3 pieces each, 120 CTAs on 152 SMs).  Pieces of a fixed length L with
+    // a shorter remainder, launched longest first, put the remainders on the idle SMs and then
+    // run them as a short second wave.  A greedy schedule of the pieces (longest first, each on
+    // the SM that frees first; a CTA costs its tiles plus about 7 tiles of set-up and epilogue)
+    // picks L, or keeps the balanced plan when that finishes first.  Only for groups of one
+    // length (one shared prefix, or several of equal length): with prefixes of different
+    // lengths the remainders come out of very different sizes, and measured on GB300 (eight
+    // prefixes of 2K-16K) the second wave cost more than it saved.  The choice depends only on
+    // the groups' tile counts, so it is memoised on them.
+    w.grp_tail.assign(G, 0);
+    bool all_dense = G > 0;
+    for (int32_t i = 0; i < G; ++i)
+      all_dense = all_dense && groups[i].impl == kImplDenseTc && groups[i].L_p == groups[0].L_p;
+    if (!concurrent && all_dense) {
+      constexpr int64_t kCtaFixedTiles = 7;
+      std::vector<int64_t>& key = w.tail_key_now;
+      key.assign({lo, (int64_t)c->num_sms});
+      for (int32_t i = 0; i < G; ++i)
+        key.insert(key.end(), {(groups[i].L_p + kDenseTile - 1) / kDenseTile, ctas_per_piece(groups[i], n_kv)});
+      if (key != w.tail_key) {
+        w.tail_key = key;
+        std::vector<int64_t> lens;
+        auto makespan = [&]() {
+          std::sort(lens.begin(), lens.end(), std::greater<int64_t>());
+          std::vector<int64_t>& heap = w.sim_heap;
+          heap.assign((size_t)c->num_sms, 0);  // finish time of each SM (all 0: a valid min-heap)
+          int64_t end = 0;
+          for (const int64_t len : lens) {
+            std::pop_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+            heap.back() += kCtaFixedTiles + len;
+            end = std::max(end, heap.back());
+            std::push_heap(heap.begin(), heap.end(), std::greater<int64_t>());
+          }
+          return end;
+        };
+        for (int32_t i = 0; i < G; ++i) {  // the balanced plan made above
+          const DevGroup& dg = groups[i];
+          const int64_t base = dg.split_len / kDenseTile;
+          for (int32_t sp = 0; sp < dg.n_splits; ++sp)
+            lens.insert(lens.end(), (size_t)ctas_per_piece(dg, n_kv), base + (sp < dg.n_long ? 1 : 0));
+        }
+        int64_t best = makespan(), best_len = 0;
+        for (int64_t len = lo - 1; len >= std::max<int64_t>(1, lo - lo / 3); --len) {
+          lens.clear();
+          for (int32_t i = 0; i < G; ++i) {
+            const int64_t t = (groups[i].L_p + kDenseTile - 1) / kDenseTile;
+            const int64_t per = ctas_per_piece(groups[i], n_kv), pieces = (t + len - 1) / len;
+            lens.insert(lens.end(), (size_t)(per * (pieces - 1)), len);
+            lens.insert(lens.end(), (size_t)per, t - (pieces - 1) * len);
+          }
+          if ((int64_t)lens.size() > 2LL * c->num_sms) break;
+          const int64_t m = makespan();
+          if (m < best) {
+            best = m;
+            best_len = len;
+          }
+        }
+        w.tail_len = best_len;
+      }
+      if (w.tail_len > 0) {
+        for (int32_t i = 0; i < G; ++i) {
+          DevGroup& dg = groups[i];
+          const int64_t t = (dg.L_p + kDenseTile - 1) / kDenseTile;
+          dg.n_splits = (int32_t)((t + w.tail_len - 1) / w.tail_len);
+          dg.split_len = (int32_t)(w.tail_len * kDenseTile);
+          dg.n_long = 0;
+          w.grp_tail[i] = t % w.tail_len != 0 ? 1 : 0;
+        }
+      }
+    }
     // the tensor-core prefix kernels hold one SM per CTA; the suffix gets every other SM (an
     // automatic split that found no piece length leaving the suffix an SM shares them all)
     if (split_sms && (!auto_share || auto_found))
@@ -974,7 +1051,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     key_now.push_back(n_kv);
     for (int32_t i = 0; i < G; ++i) {
       const DevGroup& dg = groups[i];
-      key_now.insert(key_now.end(), {dg.impl, dg.sub, dg.n_splits, dg.row_blocks, dg.split_len, dg.n_long});
+      key_now.insert(key_now.end(), {dg.impl, dg.sub, dg.n_splits, dg.row_blocks, dg.split_len, dg.n_long, w.grp_tail[i]});
     }
     if (w.pitems_cached && key_now != w.pitems_key) w.pitems_cached = false;
     if (!w.pitems_cached) w.pitems_key.swap(key_now);
@@ -987,9 +1064,18 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       const DevGroup& dg = groups[i];
       if (dg.impl != impl) continue;
       const int32_t units = impl == kImplCascadeStream ? (int32_t)(ctas_per_piece(dg, n_kv) / dg.row_blocks) : n_kv;
+      // a group whose last piece is a shorter remainder puts those pieces after all others
+      // (longest first: they fill the SMs the long pieces leave, then run as a second wave)
+      const int32_t s_end = w.grp_tail[i] ? dg.n_splits - 1 : dg.n_splits;
       for (int32_t j = 0; j < units; ++j)
-        for (int32_t s = 0; s < dg.n_splits; ++s)
+        for (int32_t s = 0; s < s_end; ++s)
           for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, s});
+    }
+    for (int32_t i = 0; i < G; ++i) {
+      const DevGroup& dg = groups[i];
+      if (dg.impl != impl || !w.grp_tail[i]) continue;
+      for (int32_t j = 0; j < n_kv; ++j)
+        for (int32_t rb = 0; rb < dg.row_blocks; ++rb) pitems.push_back({i, j, rb, dg.n_splits - 1});
     }
     p->pitem_count[impl] = (int32_t)pitems.size() - p->pitem_first[impl];
   }
