@@ -519,7 +519,7 @@ def run_granikv(args):
                    "suffix": WORKLOADS[args.workload][1],
                    "layers_per_step": L, "backend": args.backend,
                    "append": "fused into the attention launch" if fused else "own launch per layer",
-                   "schedule": plan.schedule(),
+                   "schedule": dict(plan.schedule(), dense_l2_ahead=plan.dense_l2_ahead()),
                    "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                "n_splits": g["n_splits"]} for g in groups],

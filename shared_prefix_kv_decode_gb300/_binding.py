@@ -129,6 +129,8 @@ _SIGNATURES = [
     ("granikv_workspace_size", C.c_int32, [C.c_void_p, C.c_void_p, C.POINTER(C.c_size_t)]),
     ("granikv_set_concurrency", C.c_int32, [C.c_void_p, C.c_int32, C.c_float]),
     ("granikv_set_fused_merge", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_set_dense_l2_ahead", C.c_int32, [C.c_void_p, C.c_int32]),
+    ("granikv_plan_dense_l2_ahead", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_set_msat", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_get_msat", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_force_backend", C.c_int32, [C.c_void_p, C.c_int32]),
@@ -255,6 +257,12 @@ class Plan:
         _check(self._ctx._lib.granikv_plan_schedule(self.handle, C.byref(a), C.byref(b), C.byref(c)),
                "granikv_plan_schedule")
         return {"concurrent": bool(a.value), "prefix_ctas": b.value, "suffix_ctas": c.value}
+
+    def dense_l2_ahead(self) -> int:
+        """Tiles the dense kernel reads ahead into L2 in this plan's launches (0: none)."""
+        n = C.c_int32()
+        _check(self._ctx._lib.granikv_plan_dense_l2_ahead(self.handle, C.byref(n)), "granikv_plan_dense_l2_ahead")
+        return n.value
 
     def image(self) -> bytes:
         """The plan's device image (the work list copied into the workspace), for diagnostics."""
@@ -454,6 +462,10 @@ class Context:
 
     def set_fused_merge(self, on: bool):
         _check(self._lib.granikv_set_fused_merge(self.handle, 1 if on else 0), "granikv_set_fused_merge")
+
+    def set_dense_l2_ahead(self, tiles: int):
+        """Dense kernel's L2 read-ahead in tiles: -1 automatic (the default), 0 off, 1-64 forced."""
+        _check(self._lib.granikv_set_dense_l2_ahead(self.handle, int(tiles)), "granikv_set_dense_l2_ahead")
 
     def set_msat(self, m_sat: int):
         _check(self._lib.granikv_set_msat(self.handle, m_sat), "granikv_set_msat")

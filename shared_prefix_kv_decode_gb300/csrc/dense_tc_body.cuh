@@ -155,6 +155,19 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     tma_load_3d(dst, tm, 0, j, z, bar(full));
     tma_load_3d(dst + kHalf, tm, 64, j, z, bar(full));
   };
+  // Read-ahead into L2 (p.l2_ahead > 0): when a ring slot is refilled with tile i, tile
+  // i + l2_ahead of the same tensor is requested into L2, so this CTA keeps more of its bytes
+  // in flight than its shared-memory ring holds.  Next to suffix CTAs that keep HBM busy, this
+  // raises the prefix side's share of the bandwidth; the first tiles are not read ahead, which
+  // would hold back the tiles the pipeline waits for first.
+  const int l2_ahead = p.l2_ahead;
+  auto read_ahead = [&](bool is_k, int i) {
+    if (l2_ahead <= 0 || i >= n_tiles) return;
+    const CUtensorMap* tm = is_k ? tmk : tmv;
+    const int32_t z = (int32_t)(gr.slab_off + t0 + i * kN);
+    tma_prefetch_l2_3d(tm, 0, j, z);
+    tma_prefetch_l2_3d(tm, 64, j, z);
+  };
   if (warp == kWarpTmaK && lane == 0) {
     tma_prefetch_desc(tmk);
     tma_prefetch_desc(tmv);
@@ -247,6 +260,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
                                kWaitLimitNs))
           break;
         issue_tile(is_k, i);
+        read_ahead(is_k, i + l2_ahead);
         issued = i + 1;
       }
     }

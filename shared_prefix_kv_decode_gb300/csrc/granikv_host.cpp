@@ -76,6 +76,7 @@ struct granikv_ctx {
   float prefix_share = 0.0f;  // 0: automatic
   int32_t inject_stall = 0;   // test hook for the next decode call
   int32_t fused_merge = 0;  // merge by the last producer instead of a merge kernel
+  int32_t l2_ahead = -1;    // dense kernel's L2 read-ahead in tiles; -1: chosen per step
   // tickets of the last call (zeroed again after a device check failure)
   void* last_tickets = nullptr;
   size_t last_tickets_bytes = 0;
@@ -95,6 +96,7 @@ struct granikv_plan {
   bool concurrent = false;  // suffix kernel on the auxiliary stream next to the prefix kernel
   int32_t suffix_impl = kImplGeneric;
   int32_t merge_warps = 1;  // warps of the merge kernel per (request, head) row
+  int32_t l2_ahead = 0;     // dense kernel's L2 read-ahead in tiles
   int32_t pitem_first[kNumImpl] = {};  // prefix items are ordered by implementation
   int32_t pitem_count[kNumImpl] = {};
   std::vector<granikv_group_info> info;
@@ -673,6 +675,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   std::vector<int32_t>& req_group = w.req_group;
   int64_t T_all = 0;    // COLD tokens of the batch
   int64_t T_tiles = 0;  // their 16-token tiles, counted per request
+  int64_t n_sreq = 0;   // requests with COLD tokens
   // the groups of the last dispatch stand if the batch has the same slab ids and each group's
   // slab is still the same live extent
   bool same_groups = w.groups_cached && (int32_t)w.cache_slab_id.size() == B &&
@@ -690,6 +693,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       if (L < 0 || L > bt->cap || (L == 0 && bt->slab_id[b] < 0)) return GRANIKV_ERR_INVALID;
       T_all += L;
       T_tiles += (L + 15) / 16;
+      n_sreq += L > 0 ? 1 : 0;
     }
   } else {
     w.pitems_cached = false;
@@ -712,6 +716,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       if (L < 0 || L > bt->cap) return GRANIKV_ERR_INVALID;
       T_all += L;
       T_tiles += (L + 15) / 16;
+      n_sreq += L > 0 ? 1 : 0;
       if (sid < 0) {
         if (L == 0) return GRANIKV_ERR_INVALID;
         continue;
@@ -767,6 +772,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const int32_t prefix_sms =
       split_sms && !auto_share ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
   int32_t suffix_sms = c->num_sms;  // set after the prefix pieces when the SMs are split
+  bool prefix_longer = false;       // the split's prefix side is estimated to end last
 
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
   //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
@@ -839,6 +845,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
           auto_found = true;
         }
       }
+      if (auto_found) prefix_longer = prefix_time(lo) > w_s / (double)(c->num_sms - ctas_for(lo));
       // serial: the suffix kernel starts only after the prefix kernel's last CTA (its tail and
       // the second kernel's ramp measured at about 5 us)
       const double t_serial =
@@ -951,27 +958,34 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     gi.slot_offset = dg.slab_off;
   }
   // 4. suffix: cut the concatenation of all requests' COLD tokens, in 16-token tiles counted
-  //    per request (a request's last tile may be partial), into one equal run of tiles per
-  //    token-CTA (stream-K); each request segment inside a run is one work item and record.
-  //    Cuts fall on tile boundaries of the request, so a CTA's time follows its tile count.
+  //    per request (a request's last tile may be partial), into one run per token-CTA
+  //    (stream-K); each request segment inside a run is one work item and record.  Cuts fall on
+  //    tile boundaries of the request.  A segment costs its CTA about one tile on top of its
+  //    tiles (measured on GB300, Llama-3.1-8B shape, 88 token-CTAs of 22-23 tiles: 0.54-0.76 us
+  //    a segment against 0.6-0.7 us a tile; the segments of short requests also hold their
+  //    recently appended tokens, whose slots are scattered), so the runs are cut where the
+  //    running count of tiles plus segments reaches each CTA's equal share.
   constexpr int64_t kSTile = 16;
   static_assert(kSTile == 16, "the tile count above uses 16-token tiles");
+  constexpr int64_t kSegTiles = 1;
   const int64_t T = T_tiles;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
   int32_t n_scta = 0;
-  int64_t q_base = 1, q_extra = 0;  // token-CTA k streams q_base tiles, plus one if k < q_extra
+  int64_t U = 0;  // tiles plus segment costs, with every cut counted as inside a request
   if (T > 0) {
     // one wave over the suffix's SMs, with at least kMinCtaTiles tiles per token-CTA (a CTA's
     // set-up and first-tile latency cost about as much as three tiles, and every CTA adds a
     // record per request it touches), unless a CTA would then stream more tokens than it can
     // stage slot ids for
     constexpr int64_t kMinCtaTiles = 4;
+    constexpr int64_t kMaxCtaTiles = kSuffixMaxCtaTokens / kSTile;
     n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + kMinCtaTiles - 1) / kMinCtaTiles);
-    n_scta = (int32_t)std::max<int64_t>(n_scta, (T + kSuffixMaxCtaTokens / kSTile - 1) / (kSuffixMaxCtaTokens / kSTile));
-    q_base = T / n_scta;
-    q_extra = T % n_scta;
+    n_scta = (int32_t)std::max<int64_t>(n_scta, (T + n_sreq + kMaxCtaTiles - 3) / (kMaxCtaTiles - 2));
+    U = T + kSegTiles * (n_sreq + n_scta - 1);
   }
+  // cumulative share of tiles plus segment costs at the end of token-CTA k
+  auto share_end = [&](int64_t k) { return U * (k + 1) / n_scta; };
 
   // 5. records and work items
   std::vector<int32_t>& group_req = w.group_req;
@@ -1005,8 +1019,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int32_t n_si = 0;
   int64_t rec = 0;
   int32_t cta = 0;
-  int64_t used = 0;
-  int64_t quota = q_base + (0 < q_extra ? 1 : 0);
+  int64_t done = 0;         // tiles plus segment costs given to the CTAs so far
+  bool cta_open = false;    // the current CTA has a segment
   int32_t max_parts = 0;
   for (int32_t b = 0; b < B; ++b) {
     DevReq& r = reqs[b];
@@ -1018,7 +1032,16 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     int32_t k = 0;
     const int64_t n_t = (L + kSTile - 1) / kSTile;
     for (int64_t t = 0; t < n_t;) {
-      const int64_t take = std::min<int64_t>(n_t - t, quota - used);
+      const bool last_cta = cta >= n_scta - 1;
+      int64_t room = last_cta ? n_t - t : share_end(cta) - done - kSegTiles;
+      if (room <= 0 && cta_open) {
+        // no tile more fits in this CTA: the request goes on in the next one
+        ++cta;
+        scta_begin[cta] = n_si;
+        cta_open = false;
+        continue;
+      }
+      const int64_t take = std::min<int64_t>(n_t - t, std::max<int64_t>(room, 1));
       DevSuffixItem& it = si[n_si++];
       it.b = b;
       it.t0 = (int32_t)(t * kSTile);
@@ -1026,12 +1049,12 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       it.rec = (int32_t)(rec + n_prefix + k);
       ++k;
       t += take;
-      used += take;
-      if (used == quota) {
+      done += kSegTiles + take;
+      cta_open = true;
+      if (!last_cta && done >= share_end(cta)) {
         ++cta;
-        if (cta <= n_scta) scta_begin[std::min(cta, n_scta)] = n_si;
-        used = 0;
-        quota = q_base + (cta < q_extra ? 1 : 0);
+        scta_begin[cta] = n_si;
+        cta_open = false;
       }
     }
     r.n_parts = n_prefix + k;
@@ -1130,6 +1153,16 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;
+  // The dense CTAs of a split whose prefix side is estimated to end last read two tiles ahead
+  // into L2: their per-tile chain keeps few bytes in flight, and next to suffix CTAs that keep
+  // HBM busy they fall behind.  Measured on GB300 (Llama-3.1-8B shape, 16K prefix, B = 64, a
+  // 32-layer step): 42.7 -> 40.9 us a call with two tiles ahead, 41.0 / 41.1 / 41.4 us with
+  // three / four / five; on another box 43.2 -> 43.0 / 46.1 us with six / eight (further ahead
+  // takes the suffix side's bandwidth).  Where the suffix side ends last (Qwen-2.5 shape) it
+  // does not help, and with the kernels one after another (eight prefixes) six tiles ahead
+  // cost 17 %.
+  constexpr int32_t kAutoL2Ahead = 2;
+  p->l2_ahead = c->l2_ahead >= 0 ? c->l2_ahead : (concurrent && prefix_longer ? kAutoL2Ahead : 0);
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
   // this dispatch succeeded: its groups and prefix items may serve the next one
@@ -1152,6 +1185,12 @@ granikv_status granikv_plan_num_groups(const granikv_plan* p, int32_t* n) {
 granikv_status granikv_plan_group(const granikv_plan* p, int32_t i, granikv_group_info* out) {
   if (!p || !out || !p->valid || i < 0 || i >= p->n_groups) return GRANIKV_ERR_INVALID;
   *out = p->info[i];
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_plan_dense_l2_ahead(const granikv_plan* p, int32_t* tiles) {
+  if (!p || !p->valid || !tiles) return GRANIKV_ERR_INVALID;
+  *tiles = p->l2_ahead;
   return GRANIKV_OK;
 }
 
@@ -1229,6 +1268,12 @@ granikv_status granikv_set_concurrency(granikv_ctx* c, int32_t on, float share) 
 granikv_status granikv_set_fused_merge(granikv_ctx* c, int32_t on) {
   if (!c) return GRANIKV_ERR_INVALID;
   c->fused_merge = on ? 1 : 0;
+  return GRANIKV_OK;
+}
+
+granikv_status granikv_set_dense_l2_ahead(granikv_ctx* c, int32_t tiles) {
+  if (!c || tiles < -1 || tiles > 64) return GRANIKV_ERR_INVALID;
+  c->l2_ahead = tiles;
   return GRANIKV_OK;
 }
 
@@ -1330,6 +1375,7 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
   a.checks = c->checks;
   a.tickets = tickets;
   a.fused_merge = p->fused ? 1 : 0;
+  a.l2_ahead = p->l2_ahead;
   a.inject_stall = c->inject_stall;
   c->inject_stall = 0;
   a.live_len = bt->seq_len_dev;

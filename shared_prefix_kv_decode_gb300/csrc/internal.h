@@ -121,6 +121,7 @@ struct AttnParams {
   int32_t* tickets;       // [B, n_q] arrivals per row (fused merge), zero between calls
   int32_t fused_merge;    // 1: the last producer of a row merges it (no merge kernel)
   int32_t q_tma;          // 1: the q tensor map passed to the dense kernel is valid
+  int32_t l2_ahead;       // dense kernel: K/V tiles requested into L2 ahead of its ring (0: none)
   int32_t inject_stall;   // test hook: suffix token-CTA 0 withholds its first tile (see header)
   const void* k_new;        // [B, n_kv, d] or NULL: K of each request's last COLD token, read from
   const void* v_new;        // here (not the pool) and written to its slot by the suffix CTA

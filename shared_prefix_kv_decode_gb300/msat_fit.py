@@ -66,10 +66,11 @@ def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers
         out[name + "_backend"] = gb.BACKEND_NAMES[plans[name].groups()[0]["backend"]]
     torch.cuda.synchronize()
     # the three plans take turns within every repetition, so that slow drift of the GPU's
-    # state is not read as a difference between them
+    # state is not read as a difference between them, and the turn order rotates from one
+    # repetition to the next, so that no plan always runs after the same one
     times = {name: [] for name, _ in names}
-    for _ in range(reps):
-        for name, _ in names:
+    for rep in range(reps):
+        for name, _ in names[rep % len(names):] + names[:rep % len(names)]:
             o, lse = outs[name]
             flush()
             e0 = torch.cuda.Event(enable_timing=True)

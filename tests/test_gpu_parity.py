@@ -250,6 +250,27 @@ def test_concurrency_and_merge_settings(cuda_ok, backend, setting):
     assert_close(o, lse, o_ref, lse_ref, "bf16", f"concurrency {setting} {backend}")
 
 
+@pytest.mark.parametrize("serial", [False, True])
+def test_dense_l2_read_ahead_leaves_results_unchanged(cuda_ok, serial):
+    """The dense kernel's L2 read-ahead only asks for tiles earlier: on the Llama-shape
+    workload (16K prefix, 64 requests) every setting gives bit-identical o and lse within a
+    schedule (one grid, or the kernels one after another), and they match the oracle."""
+    wl = W.llama8b_single_prefix_16k(0)
+    lw = _load(wl)
+    ctx = lw.cache.ctx
+    ctx.set_concurrency(not serial, 0.0)
+    got = {}
+    for tiles in (0, 2, 7, -1):
+        ctx.set_dense_l2_ahead(tiles)
+        got[tiles] = _run(lw, "dense")
+    ctx.set_dense_l2_ahead(-1)
+    for tiles in (2, 7, -1):
+        assert np.array_equal(got[tiles][0], got[0][0]) and np.array_equal(got[tiles][1], got[0][1]), tiles
+    reqs = [0, 21, 42, 63]
+    o_ref, lse_ref = OA.decode_attention(wl, requests=reqs)
+    assert_close(got[2][0][reqs], got[2][1][reqs], o_ref, lse_ref, "bf16", f"read-ahead, serial={serial}")
+
+
 def test_run_to_run_deterministic(cuda_ok):
     wl = W.small_mixed(9, dtype="bf16", q_scale=1.0)
     lw = _load(wl)
@@ -500,6 +521,7 @@ def test_full_size_whole_batch_through_the_benchmarked_call(cuda_ok):
     plan = ctx.dispatch(batch)
     sched = plan.schedule()
     assert sched["concurrent"] and sched["prefix_ctas"] + sched["suffix_ctas"] == 152
+    assert plan.dense_l2_ahead() == 2  # the dense CTAs read ahead into L2 in this split
     ws = cache.workspace(plan)
     o = torch.empty((B, spec.n_q, 128), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, spec.n_q), dtype=torch.float32, device="cuda")

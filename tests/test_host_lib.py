@@ -391,3 +391,95 @@ def test_serial_dense_pieces_fill_the_sms(granikv_lib):
     sid2, _ = ctx.hot_alloc(9000)
     plan = ctx.dispatch(gb.Batch([sid] * 64 + [sid2] * 64, [0] * 128, 0, 64), ctx.plan())
     assert plan.schedule()["prefix_ctas"] <= 152
+
+
+def _suffix_runs(plan, G, B, n_scta):
+    """The plan image's suffix work items (request, t0, t1, record) and each token-CTA's first
+    item: the items follow the prefix items (16 bytes each), and the CTA offsets follow the
+    items directly, ending with the item count."""
+    import struct
+    img = plan.image()
+    a16 = lambda x: (x + 15) // 16 * 16
+    off_s = a16(a16(a16(64 * G + 4 * B) + 16 * B) + 16 * plan.schedule()["prefix_ctas"])
+    for n in range(n_scta, (len(img) - off_s) // 16 + 1):
+        off_c = off_s + 16 * n
+        if off_c + 4 * (n_scta + 1) > len(img):
+            break
+        cb = struct.unpack_from("<%di" % (n_scta + 1), img, off_c)
+        if cb[0] == 0 and cb[-1] == n and all(cb[i] <= cb[i + 1] for i in range(n_scta)):
+            items = [struct.unpack_from("<4i", img, off_s + 16 * i) for i in range(n)]
+            return items, cb
+    raise AssertionError("no suffix item table found")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_suffix_runs_cover_every_tile_once_and_balance_tiles_plus_segments(granikv_lib, seed):
+    """Token-CTA runs (stream-K over the concatenated COLD tiles): every request's tokens are
+    covered once, in order, by its segments, whose records follow its prefix records; and the
+    runs are cut so that each CTA's tiles plus segments (a segment costs about one tile) are its
+    equal share, to within one tile."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(8, 200))
+    lens = [int(x) for x in np.clip(rng.lognormal(np.log(300), 1.0, B), 1, 2048)]
+    ctx = _host_ctx(n_slots=400000, max_slabs=4, m_sat=4)
+    sid, _ = ctx.hot_alloc(8192)
+    plan = ctx.dispatch(gb.Batch([sid] * B, lens, 0, 4096), ctx.plan())
+    n_scta = plan.schedule()["suffix_ctas"]
+    items, cb = _suffix_runs(plan, 1, B, n_scta)
+    n_prefix = plan.groups()[0]["n_splits"]
+    nxt = [0] * B
+    seg_no = [0] * B
+    for b, t0, t1, rec in items:
+        assert t0 == nxt[b] and t1 > t0 and t0 % 16 == 0
+        assert t1 % 16 == 0 or t1 == lens[b]
+        nxt[b] = t1
+        seg_no[b] += 1
+    assert nxt == lens
+    # records: one per segment after the request's prefix pieces, consecutive over the batch
+    rec_base, base = {}, 0
+    for b in range(B):
+        rec_base[b] = base
+        base += n_prefix + seg_no[b]
+    k_of = [0] * B
+    for b, t0, t1, rec in items:
+        assert rec == rec_base[b] + n_prefix + k_of[b]
+        k_of[b] += 1
+    tiles = sum((L + 15) // 16 for L in lens)
+    U = tiles + B + n_scta - 1
+    for k in range(n_scta):
+        run = items[cb[k]:cb[k + 1]]
+        cost = sum((t1 - t0 + 15) // 16 for _, t0, t1, _ in run) + len(run)
+        share = U * (k + 1) // n_scta - U * k // n_scta
+        assert cost <= share + 1, (k, cost, share)
+        if k < n_scta - 1:
+            assert cost >= share - 1, (k, cost, share)
+
+
+def test_dense_l2_read_ahead_follows_the_split(granikv_lib):
+    """The dense kernel reads two tiles ahead into L2 when the step runs as one grid whose
+    prefix side is estimated to end last (Llama-3.1-8B shape, 16K prefix, B = 64, suffixes of a
+    few hundred tokens), not when the suffix side ends last (Qwen-2.5 shape, B = 128, longer
+    suffixes) or the kernels run one after another; a forced setting applies to every plan."""
+    rng = np.random.default_rng(7)
+    llama = _host_ctx(n_slots=400000, m_sat=4)
+    sid, _ = llama.hot_alloc(16384)
+    lens = [int(x) for x in np.clip(rng.lognormal(np.log(300), 1.0, 64), 32, 2048)]
+    batch = gb.Batch([sid] * 64, lens, 0, 4096)
+    plan = llama.dispatch(batch, llama.plan())
+    assert plan.schedule()["concurrent"] and plan.dense_l2_ahead() == 2
+    qwen = gb.Context(n_layers=1, n_q=40, n_kv=8, head_dim=128, dtype=gb.DTYPE_BF16, n_slots=400000,
+                      max_slabs=4, m_sat=4, host_only=True)
+    qsid, _ = qwen.hot_alloc(16384)
+    qlens = [int(x) for x in rng.integers(64, 1025, 128)]
+    qplan = qwen.dispatch(gb.Batch([qsid] * 128, qlens, 0, 4096), qwen.plan())
+    assert qplan.schedule()["concurrent"] and qplan.dense_l2_ahead() == 0
+    llama.set_concurrency(False, 0.0)
+    assert llama.dispatch(batch, llama.plan()).dense_l2_ahead() == 0
+    llama.set_dense_l2_ahead(5)
+    assert llama.dispatch(batch, llama.plan()).dense_l2_ahead() == 5
+    llama.set_dense_l2_ahead(0)
+    llama.set_concurrency(True, 0.0)
+    assert llama.dispatch(batch, llama.plan()).dense_l2_ahead() == 0
+    for bad in (-2, 65):
+        with pytest.raises(Exception):
+            llama.set_dense_l2_ahead(bad)
