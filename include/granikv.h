@@ -262,6 +262,12 @@ granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_g
  * prefix CTAs and of suffix CTAs it launches. */
 granikv_status granikv_plan_schedule(const granikv_plan* plan, int32_t* concurrent, int32_t* prefix_ctas,
                                      int32_t* suffix_ctas);
+/* The plan's suffix runs (token-CTA work lists, one KV-head group's; the generic suffix kernel:
+ * its work items) and, of them, the tail runs: when the step runs as one grid in which every
+ * prefix CTA is dense and the suffix side is estimated to end last, the last tail_runs runs
+ * are taken by dense CTAs 0.. after their prefix piece (granikv_plan_schedule counts the
+ * suffix CTAs launched, without them). */
+granikv_status granikv_plan_suffix_runs(const granikv_plan* plan, int32_t* runs, int32_t* tail_runs);
 /* The dense kernel's L2 read-ahead (in tiles, 0 for none) the plan's launches use; see
  * granikv_set_dense_l2_ahead. */
 granikv_status granikv_plan_dense_l2_ahead(const granikv_plan* plan, int32_t* tiles);

@@ -131,6 +131,7 @@ _SIGNATURES = [
     ("granikv_set_fused_merge", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_set_dense_l2_ahead", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_plan_dense_l2_ahead", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
+    ("granikv_plan_suffix_runs", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     ("granikv_set_msat", C.c_int32, [C.c_void_p, C.c_int32]),
     ("granikv_get_msat", C.c_int32, [C.c_void_p, C.POINTER(C.c_int32)]),
     ("granikv_force_backend", C.c_int32, [C.c_void_p, C.c_int32]),
@@ -257,6 +258,13 @@ class Plan:
         _check(self._ctx._lib.granikv_plan_schedule(self.handle, C.byref(a), C.byref(b), C.byref(c)),
                "granikv_plan_schedule")
         return {"concurrent": bool(a.value), "prefix_ctas": b.value, "suffix_ctas": c.value}
+
+    def suffix_runs(self) -> dict:
+        """{"runs": suffix runs (token-CTA work lists), "tail_runs": of them, those the one
+        grid's dense CTAs take after their prefix piece}."""
+        a, t = C.c_int32(), C.c_int32()
+        _check(self._ctx._lib.granikv_plan_suffix_runs(self.handle, C.byref(a), C.byref(t)), "granikv_plan_suffix_runs")
+        return {"runs": a.value, "tail_runs": t.value}
 
     def dense_l2_ahead(self) -> int:
         """Tiles the dense kernel reads ahead into L2 in this plan's launches (0: none)."""

@@ -97,6 +97,7 @@ struct granikv_plan {
   int32_t suffix_impl = kImplGeneric;
   int32_t merge_warps = 1;  // warps of the merge kernel per (request, head) row
   int32_t l2_ahead = 0;     // dense kernel's L2 read-ahead in tiles
+  int32_t n_tail = 0;       // suffix runs (the last of n_scta) taken by the one grid's dense CTAs
   int32_t pitem_first[kNumImpl] = {};  // prefix items are ordered by implementation
   int32_t pitem_count[kNumImpl] = {};
   std::vector<granikv_group_info> info;
@@ -773,6 +774,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       split_sms && !auto_share ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
   int32_t suffix_sms = c->num_sms;  // set after the prefix pieces when the SMs are split
   bool prefix_longer = false;       // the split's prefix side is estimated to end last
+  double tail_frac = 0.0;           // share of the suffix work the dense CTAs take after their piece
 
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
   //    CTA count fits the target, pieces balanced to within one tile.  The tensor-core
@@ -846,6 +848,19 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
         }
       }
       if (auto_found) prefix_longer = prefix_time(lo) > w_s / (double)(c->num_sms - ctas_for(lo));
+      // When the suffix side is estimated to end last and every prefix CTA is dense (one grid,
+      // one KV-head group), the dense CTAs take suffix runs after their prefix piece: x SM-us of
+      // suffix work such that both sides end together, after the dense CTA's set-up for its run
+      // (the suffix body's set-up and first tiles, about 4 us).  Qwen-2.5 shape, 16K prefix,
+      // B = 128: the 80 dense CTAs ended 20 us before the 72 suffix CTAs without it.
+      bool all_dense = G > 0 && n_kv <= 8;
+      for (int32_t i = 0; i < G; ++i) all_dense = all_dense && groups[i].impl == kImplDenseTc;
+      if (auto_found && all_dense) {
+        constexpr double kTailSetupUs = 4.0;
+        const double n_d = (double)ctas_for(lo), n_s = (double)c->num_sms - n_d;
+        const double x = (w_s / n_s - prefix_time(lo) - kTailSetupUs) / (1.0 / n_s + 1.0 / n_d);
+        if (x > 0.0) tail_frac = x / w_s;
+      }
       // serial: the suffix kernel starts only after the prefix kernel's last CTA (its tail and
       // the second kernel's ramp measured at about 5 us)
       const double t_serial =
@@ -854,6 +869,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
         lo = lo_serial;
         auto_found = false;
         concurrent = false;
+        tail_frac = 0.0;
       }
     }
     for (int32_t i = 0; i < G; ++i) {
@@ -971,8 +987,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const int64_t T = T_tiles;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
-  int32_t n_scta = 0;
-  int64_t U = 0;  // tiles plus segment costs, with every cut counted as inside a request
+  int32_t n_scta = 0;       // token-CTA runs
+  int32_t n_tail = 0;       // of them, the last n_tail are run by the dense CTAs of one grid
+  int64_t U = 0;            // tiles plus segment costs, with every cut counted as inside a request
+  int64_t U_tail = 0;       // of U, the tail runs' share
   if (T > 0) {
     // one wave over the suffix's SMs, with at least kMinCtaTiles tiles per token-CTA (a CTA's
     // set-up and first-tile latency cost about as much as three tiles, and every CTA adds a
@@ -982,10 +1000,27 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     constexpr int64_t kMaxCtaTiles = kSuffixMaxCtaTokens / kSTile;
     n_scta = (int32_t)std::min<int64_t>(suffix_sms, (T + kMinCtaTiles - 1) / kMinCtaTiles);
     n_scta = (int32_t)std::max<int64_t>(n_scta, (T + n_sreq + kMaxCtaTiles - 3) / (kMaxCtaTiles - 2));
+    const int32_t n_dense_ctas = (int32_t)(c->num_sms - suffix_sms);
+    if (tail_frac > 0.0 && n_scta == suffix_sms && n_dense_ctas > 0) {
+      n_tail = n_dense_ctas;
+      n_scta += n_tail;
+    }
     U = T + kSegTiles * (n_sreq + n_scta - 1);
+    U_tail = n_tail > 0 ? (int64_t)(tail_frac * (double)U) : 0;
+    if (U_tail < 3 * (int64_t)n_tail) {  // under about two tiles a run: not worth a run's set-up
+      n_scta -= n_tail;
+      n_tail = 0;
+      U_tail = 0;
+      U = T + kSegTiles * (n_sreq + n_scta - 1);
+    }
   }
-  // cumulative share of tiles plus segment costs at the end of token-CTA k
-  auto share_end = [&](int64_t k) { return U * (k + 1) / n_scta; };
+  // cumulative share of tiles plus segment costs at the end of token-CTA run k: the suffix
+  // CTAs' runs share U - U_tail, the tail runs U_tail
+  const int32_t n_main = n_scta - n_tail;
+  auto share_end = [&](int64_t k) {
+    if (k < n_main) return (U - U_tail) * (k + 1) / n_main;
+    return (U - U_tail) + U_tail * (k - n_main + 1) / n_tail;
+  };
 
   // 5. records and work items
   std::vector<int32_t>& group_req = w.group_req;
@@ -1139,6 +1174,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->n_prefix_records = 0;
   for (int32_t b = 0; b < B; ++b) p->n_prefix_records += reqs[b].n_prefix;
   p->n_scta = n_scta;
+  p->n_tail = n_tail;
   p->suffix_impl = suffix_impl;
   {
     // the merge gives a row with many records (a cascade step over all SMs has one per L_p
@@ -1188,6 +1224,13 @@ granikv_status granikv_plan_group(const granikv_plan* p, int32_t i, granikv_grou
   return GRANIKV_OK;
 }
 
+granikv_status granikv_plan_suffix_runs(const granikv_plan* p, int32_t* runs, int32_t* tail_runs) {
+  if (!p || !p->valid) return GRANIKV_ERR_INVALID;
+  if (runs) *runs = p->suffix_impl == kImplSuffixMma ? p->n_scta : p->n_sitems;
+  if (tail_runs) *tail_runs = p->n_tail;
+  return GRANIKV_OK;
+}
+
 granikv_status granikv_plan_dense_l2_ahead(const granikv_plan* p, int32_t* tiles) {
   if (!p || !p->valid || !tiles) return GRANIKV_ERR_INVALID;
   *tiles = p->l2_ahead;
@@ -1201,7 +1244,7 @@ granikv_status granikv_plan_schedule(const granikv_plan* p, int32_t* concurrent,
   if (prefix_ctas) *prefix_ctas = p->n_pitems;
   if (suffix_ctas) {
     const int32_t head_groups = (p->ctx->cfg.n_kv + 7) / 8;
-    *suffix_ctas = p->suffix_impl == kImplSuffixMma ? p->n_scta * head_groups : p->n_sitems;
+    *suffix_ctas = p->suffix_impl == kImplSuffixMma ? (p->n_scta - p->n_tail) * head_groups : p->n_sitems;
   }
   return GRANIKV_OK;
 }
@@ -1440,8 +1483,12 @@ granikv_status decode_attention_impl(granikv_ctx* c, int32_t layer, const void* 
     // dependent launch
     const CUtensorMap& tk = c->has_tmaps ? c->tmap_k[layer] : tmq;
     const CUtensorMap& tv = c->has_tmaps ? c->tmap_v[layer] : tmq;
+    // the last n_tail suffix runs go to dense CTAs 0.. after their prefix piece (a plan has
+    // them only when every prefix item is dense, one per dense CTA); on any other launch path
+    // every run is a suffix CTA of its own
+    const int32_t n_tail = p->n_tail <= n_dense && n_casc == 0 ? p->n_tail : 0;
     e = launch_prefix_suffix_tc(a, p->pitem_first[kImplDenseTc], n_dense, p->pitem_first[kImplCascadeStream], n_casc,
-                                tk, tv, tmq, a.scta_begin, p->n_scta, s, true);
+                                tk, tv, tmq, a.scta_begin, p->n_scta - n_tail, n_tail, s, true);
     c->n_kernels += 1;
     if (e == cudaSuccess && !p->fused) e = launch_merge_k(true);
   } else if (p->concurrent) {

@@ -162,11 +162,12 @@ cudaError_t launch_cascade_stream(const AttnParams& p, int32_t first_item, int32
 cudaError_t launch_dense_tf32(const AttnParams& p, int32_t first_item, int32_t n_items, cudaStream_t s);
 // One launch for the prefix and suffix work: CTAs [0, n_dense) run dense prefix items
 // first_dense.., the next n_casc the streaming cascade items first_casc.., the rest the suffix
-// token-CTAs (n_scta per KV-head group of eight).
+// token-CTAs (n_scta per KV-head group of eight); dense CTA c < n_tail then runs suffix
+// token-CTA n_scta + c of a plan with one KV-head group.
 cudaError_t launch_prefix_suffix_tc(const AttnParams& p, int32_t first_dense, int32_t n_dense, int32_t first_casc,
                                     int32_t n_casc, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                                    const CUtensorMap& tmq, const int32_t* cta_begin, int32_t n_scta, cudaStream_t s,
-                                    bool pdl);
+                                    const CUtensorMap& tmq, const int32_t* cta_begin, int32_t n_scta, int32_t n_tail,
+                                    cudaStream_t s, bool pdl);
 // The merge kernel, bf16 and head_dim 128, with `warps_per_row` warps (1, 2, 4 or 8) sharing
 // each row's records.
 cudaError_t launch_merge_rows(const AttnParams& p, int32_t warps_per_row, cudaStream_t s, bool pdl);

@@ -271,6 +271,49 @@ def test_dense_l2_read_ahead_leaves_results_unchanged(cuda_ok, serial):
     assert_close(got[2][0][reqs], got[2][1][reqs], o_ref, lse_ref, "bf16", f"read-ahead, serial={serial}")
 
 
+def test_dense_ctas_suffix_runs_match_the_oracle(cuda_ok):
+    """Qwen-2.5 shape at full size (16K prefix, B = 128): in the one grid the dense CTAs also
+    take suffix runs after their prefix pieces.  Every request with a segment in one of those
+    runs is checked against the oracle, and the whole batch repeats bit for bit."""
+    import struct
+    wl = W.qwen_tp1_16k(0)
+    lw = _load(wl)
+    ctx = lw.cache.ctx
+    ctx.force_backend(_gb().BACKEND_AUTO)
+    plan = ctx.dispatch(lw.batch, ctx.plan())
+    runs = plan.suffix_runs()
+    assert plan.schedule()["concurrent"] and runs["tail_runs"] == plan.schedule()["prefix_ctas"]
+    # the suffix items follow the prefix items in the plan image; the run offsets follow them
+    B, n_scta = wl.spec.B, runs["runs"]
+    img = plan.image()
+    a16 = lambda x: (x + 15) // 16 * 16
+    off_s = a16(a16(a16(64 + 4 * B) + 16 * B) + 16 * plan.schedule()["prefix_ctas"])
+    cb = None
+    for n in range(n_scta, (len(img) - off_s) // 16 + 1):
+        c = struct.unpack_from("<%di" % (n_scta + 1), img, off_s + 16 * n)
+        if c[0] == 0 and c[-1] == n and all(c[i] <= c[i + 1] for i in range(n_scta)):
+            cb = c
+            break
+    assert cb is not None
+    first_tail = cb[n_scta - runs["tail_runs"]]
+    tail_reqs = sorted({struct.unpack_from("<4i", img, off_s + 16 * i)[0] for i in range(first_tail, cb[-1])})
+    assert tail_reqs
+    o, lse = lw.cache.decode(0, lw.q, lw.batch, plan)
+    o2, lse2 = lw.cache.decode(0, lw.q, lw.batch, plan)
+    ctx.sync_status(lw.cache.stream())
+    assert torch_equal(o, o2) and torch_equal(lse, lse2)
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    sample = tail_reqs[:: max(1, len(tail_reqs) // 6)][:6]
+    o_ref, lse_ref = OA.decode_attention(wl, requests=sample)
+    assert_close(o[sample], lse[sample], o_ref, lse_ref, "bf16", f"qwen tail runs {sample}")
+
+
+def torch_equal(a, b):
+    import torch
+    return bool(torch.equal(a, b))
+
+
 def test_run_to_run_deterministic(cuda_ok):
     wl = W.small_mixed(9, dtype="bf16", q_scale=1.0)
     lw = _load(wl)

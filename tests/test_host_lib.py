@@ -424,7 +424,13 @@ def test_suffix_runs_cover_every_tile_once_and_balance_tiles_plus_segments(grani
     ctx = _host_ctx(n_slots=400000, max_slabs=4, m_sat=4)
     sid, _ = ctx.hot_alloc(8192)
     plan = ctx.dispatch(gb.Batch([sid] * B, lens, 0, 4096), ctx.plan())
-    n_scta = plan.schedule()["suffix_ctas"]
+    _check_suffix_runs(plan, B, lens)
+
+
+def _check_suffix_runs(plan, B, lens):
+    runs = plan.suffix_runs()
+    n_scta, n_tail = runs["runs"], runs["tail_runs"]
+    assert plan.schedule()["suffix_ctas"] == n_scta - n_tail
     items, cb = _suffix_runs(plan, 1, B, n_scta)
     n_prefix = plan.groups()[0]["n_splits"]
     nxt = [0] * B
@@ -445,14 +451,50 @@ def test_suffix_runs_cover_every_tile_once_and_balance_tiles_plus_segments(grani
         assert rec == rec_base[b] + n_prefix + k_of[b]
         k_of[b] += 1
     tiles = sum((L + 15) // 16 for L in lens)
-    U = tiles + B + n_scta - 1
-    for k in range(n_scta):
-        run = items[cb[k]:cb[k + 1]]
-        cost = sum((t1 - t0 + 15) // 16 for _, t0, t1, _ in run) + len(run)
-        share = U * (k + 1) // n_scta - U * k // n_scta
-        assert cost <= share + 1, (k, cost, share)
-        if k < n_scta - 1:
-            assert cost >= share - 1, (k, cost, share)
+    U = tiles + sum(1 for L in lens if L > 0) + n_scta - 1
+    costs = [sum((t1 - t0 + 15) // 16 for _, t0, t1, _ in items[cb[k]:cb[k + 1]]) + cb[k + 1] - cb[k]
+             for k in range(n_scta)]
+    if n_tail == 0:
+        for k in range(n_scta):
+            share = U * (k + 1) // n_scta - U * k // n_scta
+            assert costs[k] <= share + 1, (k, costs[k], share)
+            if k < n_scta - 1:
+                assert costs[k] >= share - 1, (k, costs[k], share)
+    else:
+        # the suffix CTAs' runs share one amount, the dense CTAs' tail runs a smaller one
+        # (segments are counted as if every cut split a request, so the last tail runs may be
+        # left empty)
+        main, tail = costs[:n_scta - n_tail], costs[n_scta - n_tail:]
+        assert max(main) - min(main) <= 2, main
+        while tail and tail[-1] == 0:
+            tail.pop()
+        assert len(tail) >= n_tail - 4 and max(tail[:-1]) - min(tail[:-1]) <= 2, tail
+        assert tail[-1] <= max(tail[:-1]) + 1 and max(tail) < min(main), tail
+    return n_tail
+
+
+def test_dense_ctas_take_suffix_runs_when_the_suffix_side_ends_last(granikv_lib):
+    """One grid on the Qwen-2.5 shape (40/8/128, 16K prefix, B = 128, suffixes U[64, 1024]):
+    the 80 dense CTAs are estimated to finish well before the 72 suffix CTAs, so each dense CTA
+    also takes a shorter suffix run after its piece; the runs still cover every token once.  The
+    Llama-3.1-8B shape (B = 64, shorter suffixes), whose prefix side ends last, has none."""
+    rng = np.random.default_rng(5)
+    qwen = gb.Context(n_layers=1, n_q=40, n_kv=8, head_dim=128, dtype=gb.DTYPE_BF16, n_slots=400000,
+                      max_slabs=4, m_sat=4, host_only=True)
+    qsid, _ = qwen.hot_alloc(16384)
+    qlens = [int(x) for x in rng.integers(64, 1025, 128)]
+    qplan = qwen.dispatch(gb.Batch([qsid] * 128, qlens, 0, 4096), qwen.plan())
+    sched = qplan.schedule()
+    assert sched["concurrent"] and sched["prefix_ctas"] + sched["suffix_ctas"] == 152
+    assert qplan.suffix_runs()["tail_runs"] == sched["prefix_ctas"]
+    assert _check_suffix_runs(qplan, 128, qlens) > 0
+    llama = _host_ctx(n_slots=400000, m_sat=4)
+    sid, _ = llama.hot_alloc(16384)
+    lens = [int(x) for x in np.clip(rng.lognormal(np.log(300), 1.0, 64), 32, 2048)]
+    plan = llama.dispatch(gb.Batch([sid] * 64, lens, 0, 4096), llama.plan())
+    assert plan.suffix_runs()["tail_runs"] == 0
+    qwen.set_concurrency(False, 0.0)
+    assert qwen.dispatch(gb.Batch([qsid] * 128, qlens, 0, 4096), qwen.plan()).suffix_runs()["tail_runs"] == 0
 
 
 def test_dense_l2_read_ahead_follows_the_split(granikv_lib):
