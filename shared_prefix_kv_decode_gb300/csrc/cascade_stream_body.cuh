@@ -287,11 +287,12 @@ __device__ __forceinline__ bool consume(const AttnParams& p, const DevGroup& gr,
     else latch_err(p.err, kDevBadRecord);
   }
   __syncwarp();
+  const uint64_t keep = l2_policy_keep();
   for (int n = 0; n < ncols; ++n) {
     const int64_t row = __shfl_sync(0xffffffffu, row_l, n);
     if (row < 0) continue;
     const float4 v4 = *reinterpret_cast<const float4*>(so + n * kStageStride + lane * 4);
-    reinterpret_cast<float4*>(p.rec_o + row * kD)[lane] = v4;
+    st_record4(p.rec_o + row * kD + lane * 4, v4, keep);
   }
   // lse of each column, from the lanes that hold its sum (lanes 0-3: columns t*8 + 2*lane + c)
   int32_t bcol[NT][2], hcol[NT][2];
@@ -306,7 +307,7 @@ __device__ __forceinline__ bool consume(const AttnParams& p, const DevGroup& gr,
       bcol[t][c] = have ? b : -1;
       hcol[t][c] = j * g + (c0 + n) % g;
       const float lsum = l[t][c];
-      if (have && lane < 4) p.rec_lse[row] = lsum > 0.f ? (m[t][c] + log2f(lsum)) * kLn2 : -INFINITY;
+      if (have && lane < 4) st_record(p.rec_lse + row, lsum > 0.f ? (m[t][c] + log2f(lsum)) * kLn2 : -INFINITY, keep);
     }
   }
   if (p.fused_merge) {

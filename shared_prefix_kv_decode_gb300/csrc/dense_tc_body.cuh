@@ -597,7 +597,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
           if (row < rows) p.lse[orow] = lse_row;
         } else {
           reinterpret_cast<int64_t*>(smem + kOffV)[r] = rec >= 0 ? ((int64_t)rec * p.n_q + h) * kD : -1;
-          if (rec >= 0) p.rec_lse[(int64_t)rec * p.n_q + h] = lse_row;
+          if (rec >= 0) st_record(p.rec_lse + (int64_t)rec * p.n_q + h, lse_row, l2_policy_keep());
         }
       }
     }
@@ -609,6 +609,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
     if (staged) {
       const unsigned char* stage = smem + kOffK;
       const int64_t* sdst = reinterpret_cast<const int64_t*>(smem + kOffV);
+      const uint64_t keep = l2_policy_keep();
 #pragma unroll 4
       for (int i = 0; i < 16; ++i) {
         const int rr = quad * 32 + half * 16 + i;
@@ -619,7 +620,7 @@ __device__ __forceinline__ void dense_tc_body(const AttnParams& p, int32_t item,
           *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + d + lane * 4) =
               make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
         } else {
-          *reinterpret_cast<float4*>(p.rec_o + d + lane * 4) = x;
+          st_record4(p.rec_o + d + lane * 4, x, keep);
         }
       }
       if (p.fused_merge && !causal) {

@@ -351,21 +351,22 @@ __device__ __forceinline__ void suffix_mma_body(const AttnParams& p, const int32
     float* dst0 = p.rec_o + ((int64_t)rec * p.n_q + hq0) * kD + (lane >> 2);
     float* dst1 = dst0 + kD;
     const bool w0 = h0 < g, w1 = h0 + 1 < g;
+    const uint64_t keep = l2_policy_keep();
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       if (w0) {
-        dst0[mt * 16] = o[mt][0] * inv0;
-        dst0[mt * 16 + 8] = o[mt][2] * inv0;
+        st_record(dst0 + mt * 16, o[mt][0] * inv0, keep);
+        st_record(dst0 + mt * 16 + 8, o[mt][2] * inv0, keep);
       }
       if (w1) {
-        dst1[mt * 16] = o[mt][1] * inv1;
-        dst1[mt * 16 + 8] = o[mt][3] * inv1;
+        st_record(dst1 + mt * 16, o[mt][1] * inv1, keep);
+        st_record(dst1 + mt * 16 + 8, o[mt][3] * inv1, keep);
       }
     }
     if (lane < 4) {
       float* ldst = p.rec_lse + (int64_t)rec * p.n_q + hq0;
-      if (w0) ldst[0] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
-      if (w1) ldst[1] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+      if (w0) st_record(ldst, l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY, keep);
+      if (w1) st_record(ldst + 1, l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY, keep);
     }
     if (p.fused_merge) {
       __threadfence();

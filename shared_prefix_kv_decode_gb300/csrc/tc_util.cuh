@@ -82,6 +82,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// ---- partial-state records kept in L2 ---------------------------------------------------
+// The records a decode call writes are read back by its merge microseconds later, while the
+// call streams hundreds of MB of K/V through L2.  Stored with an evict-last policy they stay in
+// L2 until then (and the next call's records overwrite them there), instead of being evicted
+// to HBM and read back.  Measured on GB300 (32-layer steps): Llama-3.1-8B shape 40.0 -> 38.7 us
+// a call, eight prefixes 110.6 -> 106.4 us, Qwen-2.5 shape 84.0 -> 83.4 us.
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void st_record(float* a, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_record4(float* a, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(a), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 // L2 prefetch of one tensor-map box: no shared memory and no completion; the box's lines are
 // requested from HBM now, so that a later load of the same box finds them in L2
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
