@@ -1056,6 +1056,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   int32_t cta = 0;
   int64_t done = 0;         // tiles plus segment costs given to the CTAs so far
   bool cta_open = false;    // the current CTA has a segment
+  int64_t end_cur = n_scta > 0 ? share_end(0) : 0;  // (one division per CTA, not per segment)
   int32_t max_parts = 0;
   for (int32_t b = 0; b < B; ++b) {
     DevReq& r = reqs[b];
@@ -1068,12 +1069,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     const int64_t n_t = (L + kSTile - 1) / kSTile;
     for (int64_t t = 0; t < n_t;) {
       const bool last_cta = cta >= n_scta - 1;
-      int64_t room = last_cta ? n_t - t : share_end(cta) - done - kSegTiles;
+      int64_t room = last_cta ? n_t - t : end_cur - done - kSegTiles;
       if (room <= 0 && cta_open) {
         // no tile more fits in this CTA: the request goes on in the next one
         ++cta;
         scta_begin[cta] = n_si;
         cta_open = false;
+        end_cur = share_end(cta);
         continue;
       }
       const int64_t take = std::min<int64_t>(n_t - t, std::max<int64_t>(room, 1));
@@ -1086,10 +1088,11 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       t += take;
       done += kSegTiles + take;
       cta_open = true;
-      if (!last_cta && done >= share_end(cta)) {
+      if (!last_cta && done >= end_cur) {
         ++cta;
         scta_begin[cta] = n_si;
         cta_open = false;
+        end_cur = share_end(cta);
       }
     }
     r.n_parts = n_prefix + k;
