@@ -301,7 +301,7 @@ granikv_status granikv_set_fused_merge(granikv_ctx* ctx, int32_t on);
  * shared-memory K (or V) ring with tile i of its prefix piece, it also requests tile i + tiles
  * into L2 (a bulk-tensor L2 prefetch: no data moves to the SM, results are unchanged).  -1 (the
  * default): two tiles when the step runs as one grid whose prefix side is estimated to finish
- * after its suffix side, else none; 0: never; 1-64: that many tiles for every dense decode
+ * after its suffix side and whose suffix side reads at least as many bytes, else none; 0: never; 1-64: that many tiles for every dense decode
  * launch.  GRANIKV_ERR_INVALID outside [-1, 64].  Takes effect at the next granikv_dispatch. */
 granikv_status granikv_set_dense_l2_ahead(granikv_ctx* ctx, int32_t tiles);
 

@@ -773,7 +773,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   const int32_t prefix_sms =
       split_sms && !auto_share ? std::max(1, (int32_t)std::lround(c->prefix_share * c->num_sms)) : c->num_sms;
   int32_t suffix_sms = c->num_sms;  // set after the prefix pieces when the SMs are split
-  bool prefix_longer = false;       // the split's prefix side is estimated to end last
+  bool read_ahead = false;          // the split's dense CTAs read ahead into L2 (see below)
   double tail_frac = 0.0;           // share of the suffix work the dense CTAs take after their piece
 
   // 3. prefix pieces: the smallest piece length (in tiles, one length for all groups) whose
@@ -847,7 +847,10 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
           auto_found = true;
         }
       }
-      if (auto_found) prefix_longer = prefix_time(lo) > w_s / (double)(c->num_sms - ctas_for(lo));
+      // read-ahead pays where the prefix side is estimated to end last and the suffix side
+      // competes with it for HBM (suffix bytes at least the prefix's)
+      if (auto_found)
+        read_ahead = prefix_time(lo) > w_s / (double)(c->num_sms - ctas_for(lo)) && suffix_bytes >= prefix_bytes;
       // When the suffix side is estimated to end last and every prefix CTA is dense (one grid,
       // one KV-head group), the dense CTAs take suffix runs after their prefix piece: x SM-us of
       // suffix work such that both sides end together, after the dense CTA's set-up for its run
@@ -1192,16 +1195,17 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   }
   p->fused = fused && (T == 0 || suffix_impl == kImplSuffixMma);
   p->concurrent = concurrent;
-  // The dense CTAs of a split whose prefix side is estimated to end last read two tiles ahead
-  // into L2: their per-tile chain keeps few bytes in flight, and next to suffix CTAs that keep
-  // HBM busy they fall behind.  Measured on GB300 (Llama-3.1-8B shape, 16K prefix, B = 64, a
+  // The dense CTAs of a split whose prefix side is estimated to end last, next to a suffix side
+  // that reads at least as many bytes, read two tiles ahead into L2: their per-tile chain keeps
+  // few bytes in flight, and next to suffix CTAs that keep HBM busy they fall behind.  Measured on GB300 (Llama-3.1-8B shape, 16K prefix, B = 64, a
   // 32-layer step): 42.7 -> 40.9 us a call with two tiles ahead, 41.0 / 41.1 / 41.4 us with
   // three / four / five; on another box 43.2 -> 43.0 / 46.1 us with six / eight (further ahead
   // takes the suffix side's bandwidth).  Where the suffix side ends last (Qwen-2.5 shape) it
-  // does not help, and with the kernels one after another (eight prefixes) six tiles ahead
-  // cost 17 %.
+  // does not help; next to a light suffix side it costs (16K prefix, 256 COLD tokens a request:
+  // B = 1 17.7 -> 18.4 us, B = 8 18.9 -> 19.8 us); and with the kernels one after another
+  // (eight prefixes) six tiles ahead cost 17 %.
   constexpr int32_t kAutoL2Ahead = 2;
-  p->l2_ahead = c->l2_ahead >= 0 ? c->l2_ahead : (concurrent && prefix_longer ? kAutoL2Ahead : 0);
+  p->l2_ahead = c->l2_ahead >= 0 ? c->l2_ahead : (concurrent && read_ahead ? kAutoL2Ahead : 0);
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
   // this dispatch succeeded: its groups and prefix items may serve the next one

@@ -499,9 +499,11 @@ def test_dense_ctas_take_suffix_runs_when_the_suffix_side_ends_last(granikv_lib)
 
 def test_dense_l2_read_ahead_follows_the_split(granikv_lib):
     """The dense kernel reads two tiles ahead into L2 when the step runs as one grid whose
-    prefix side is estimated to end last (Llama-3.1-8B shape, 16K prefix, B = 64, suffixes of a
-    few hundred tokens), not when the suffix side ends last (Qwen-2.5 shape, B = 128, longer
-    suffixes) or the kernels run one after another; a forced setting applies to every plan."""
+    prefix side is estimated to end last next to a suffix side that reads at least as many
+    bytes (Llama-3.1-8B shape, 16K prefix, B = 64, suffixes of a few hundred tokens); not when
+    the suffix side ends last (Qwen-2.5 shape, B = 128, longer suffixes), is light (B = 1 or 8
+    with 256 COLD tokens each) or the kernels run one after another; a forced setting applies
+    to every plan."""
     rng = np.random.default_rng(7)
     llama = _host_ctx(n_slots=400000, m_sat=4)
     sid, _ = llama.hot_alloc(16384)
@@ -509,6 +511,9 @@ def test_dense_l2_read_ahead_follows_the_split(granikv_lib):
     batch = gb.Batch([sid] * 64, lens, 0, 4096)
     plan = llama.dispatch(batch, llama.plan())
     assert plan.schedule()["concurrent"] and plan.dense_l2_ahead() == 2
+    for B in (1, 8):
+        light = llama.dispatch(gb.Batch([sid] * B, [256] * B, 0, 4096), llama.plan())
+        assert light.dense_l2_ahead() == 0, B
     qwen = gb.Context(n_layers=1, n_q=40, n_kv=8, head_dim=128, dtype=gb.DTYPE_BF16, n_slots=400000,
                       max_slabs=4, m_sat=4, host_only=True)
     qsid, _ = qwen.hot_alloc(16384)
