@@ -303,7 +303,11 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
 // Records are read with streaming loads (they are not read again).  Two CTAs per SM (at most 128
 // registers per thread): with programmatic dependent launch the CTAs become resident as the
 // decode CTAs leave, spread over about 128 SMs rather than packed four to an SM on the first
-// ones freed, which measured 1.5-2 us shorter from the release to the end.
+// ones freed, which measured 1.5-2 us shorter from the release to the end.  A one-warp merge
+// with more rows than two CTAs an SM hold at once (more than one wave) takes a build limited to
+// 80 registers, three CTAs an SM: Qwen-2.5 shape (5,120 rows) 83.0 -> 82.4 us a call, eight
+// prefixes 107.5 -> 106.8 us; with one wave the two-CTA build stays (the headline's 2,048 rows:
+// 38.7 against 39.2 us).
 // Records per warp loaded together: one memory round trip for rows of up to W * kBatch records.
 template <int W>
 struct MergeCfg {
@@ -311,8 +315,8 @@ struct MergeCfg {
   static constexpr int kMinBlocks = W >= 4 ? 1 : 2;  // registers for the larger batches
 };
 
-template <int W>
-__global__ void __launch_bounds__(256, MergeCfg<W>::kMinBlocks) merge_bf16_d128_kernel(AttnParams p) {
+template <int W, int kBlocks = MergeCfg<W>::kMinBlocks>
+__global__ void __launch_bounds__(256, kBlocks) merge_bf16_d128_kernel(AttnParams p) {
   constexpr int kMergeBatch = MergeCfg<W>::kBatch;
   constexpr int kRowsPerCta = 8 / W;
   __shared__ float4 s_acc[W > 1 ? 8 : 1][32];
@@ -414,13 +418,21 @@ cudaError_t launch_merge_w(const AttnParams& p, cudaStream_t s, bool pdl) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = prefer_max_shared(merge_bf16_d128_kernel<W>);
+    if (e == cudaSuccess && W == 1) e = prefer_max_shared(merge_bf16_d128_kernel<1, 3>);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int64_t rows = (int64_t)p.B * p.n_q;
   const int64_t per_cta = 8 / W;
-  return launch_kernel(merge_bf16_d128_kernel<W>, dim3((unsigned)((rows + per_cta - 1) / per_cta)), dim3(256), 0, s,
-                       pdl, p);
+  const dim3 grid((unsigned)((rows + per_cta - 1) / per_cta));
+  if constexpr (W == 1) {
+    int dev = 0, num_sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        (int64_t)grid.x > 2LL * num_sms)
+      return launch_kernel(merge_bf16_d128_kernel<1, 3>, grid, dim3(256), 0, s, pdl, p);
+  }
+  return launch_kernel(merge_bf16_d128_kernel<W>, grid, dim3(256), 0, s, pdl, p);
 }
 
 template <typename T, int VPL>
