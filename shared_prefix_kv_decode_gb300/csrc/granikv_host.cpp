@@ -853,15 +853,16 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
         read_ahead = prefix_time(lo) > w_s / (double)(c->num_sms - ctas_for(lo)) && suffix_bytes >= prefix_bytes;
       // When the suffix side is estimated to end last and every prefix CTA is dense (one grid,
       // one KV-head group), the dense CTAs take suffix runs after their prefix piece: x SM-us of
-      // suffix work such that both sides end together, after the dense CTA's set-up for its run
-      // (the suffix body's set-up and first tiles, about 4 us).  Qwen-2.5 shape, 16K prefix,
-      // B = 128: the 80 dense CTAs ended 20 us before the 72 suffix CTAs without it.
+      // suffix work such that both sides end together.  Qwen-2.5 shape, 16K prefix, B = 128:
+      // the 80 dense CTAs ended 20 us before the 72 suffix CTAs without it.  The dense CTA's
+      // set-up for its run (a few us) is left out: the prefix estimate runs about 6 us long on
+      // that shape, which covers it; with 4 / 2 / 0 us set aside for it the call took 82.9 /
+      // 81.0 / 80.3 us, and at 0 both sides end within 0.4 us of each other.
       bool all_dense = G > 0 && n_kv <= 8;
       for (int32_t i = 0; i < G; ++i) all_dense = all_dense && groups[i].impl == kImplDenseTc;
       if (auto_found && all_dense) {
-        constexpr double kTailSetupUs = 4.0;
         const double n_d = (double)ctas_for(lo), n_s = (double)c->num_sms - n_d;
-        const double x = (w_s / n_s - prefix_time(lo) - kTailSetupUs) / (1.0 / n_s + 1.0 / n_d);
+        const double x = (w_s / n_s - prefix_time(lo)) / (1.0 / n_s + 1.0 / n_d);
         if (x > 0.0) tail_frac = x / w_s;
       }
       // serial: the suffix kernel starts only after the prefix kernel's last CTA (its tail and
