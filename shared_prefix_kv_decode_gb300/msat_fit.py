@@ -29,7 +29,7 @@ SUFFIX = 256
 
 
 def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers=1, suffix=SUFFIX, n_q=32,
-               l2_ahead=-1):
+               l2_ahead=-1, fused=False):
     """Median microseconds of one decode-attention call per backend.  layers = 1: a single call
     after an L2 flush.  layers > 1: a decode step of that many back-to-back calls, one per layer
     (each layer its own pools, so no layer's bytes are in L2 for the next), after one flush; the
@@ -57,6 +57,7 @@ def _time_cell(L_p, B, reps, m_sat_probe, flush, gb, torch, serial=False, layers
     if serial:  # prefix, suffix and merge one after another, each kernel on all SMs
         cache.ctx.set_concurrency(False, 0.0)
     cache.ctx.set_dense_l2_ahead(l2_ahead)
+    cache.ctx.set_fused_merge(fused)
     out = {}
     stream = cache.stream()
     names = (("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE), ("auto", gb.BACKEND_AUTO))
@@ -137,6 +138,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=1,
                     help="time decode steps of this many back-to-back layer calls (default: single calls)")
     ap.add_argument("--n-q", type=int, default=32, help="query heads (40: the Qwen-2.5 TP1 shape)")
+    ap.add_argument("--fused-merge", action="store_true",
+                    help="merge each row in the producer that finishes it last (no merge kernel)")
     ap.add_argument("--dense-l2-ahead", type=int, default=-1,
                     help="dense kernel's L2 read-ahead in tiles (-1: the library's per-step choice)")
     ap.add_argument("--suffix", type=int, default=SUFFIX,
@@ -153,7 +156,7 @@ def main(argv=None):
     for L_p in [int(x) for x in a.lps.split(",")]:
         for B in [int(x) for x in a.bs.split(",")]:
             r = _time_cell(L_p, B, a.reps, None, flush, gb, torch, serial=a.serial, layers=a.layers,
-                           suffix=a.suffix, n_q=a.n_q, l2_ahead=a.dense_l2_ahead)
+                           suffix=a.suffix, n_q=a.n_q, l2_ahead=a.dense_l2_ahead, fused=a.fused_merge)
             row = {"L_p": L_p, "B": B, "m_eff": B * a.n_q // 8, "dense_us": r["dense"], "cascade_us": r["cascade"],
                    "auto_us": r["auto"], "auto_backend": r["auto_backend"]}
             rows.append(row)
