@@ -334,14 +334,15 @@ def hetero_multi_prefix_k8(seed: int = 0, q_scale: Optional[float] = None) -> Wo
 
 def qwen_tp1_16k(seed: int = 0, q_scale: Optional[float] = None) -> Workload:
     """Qwen-2.5-14B/32B attention shape at TP=1 (40/8/128), bf16, one prefix of 16384 tokens,
-    B=128, suffixes U[64,1024]."""
+    B=128, suffixes U[64,1024].  KV budget 131072 slots: the COLD part (104,858 slots) holds the
+    suffixes (about 70K tokens) and a few hundred decode steps of all 128 requests."""
     rng = _struct_rng(seed, "qwen")
     B = 128
     spec = WorkloadSpec(
         name="qwen_tp1_16k", dtype="bf16", n_q=40, n_kv=8, d=128,
         prefix_lens=[16384], req_prefix=[0] * B,
         suffix_lens=[int(x) for x in rng.integers(64, 1025, size=B)],
-        q_scale=(1.0 / math.sqrt(128.0)) if q_scale is None else q_scale, n_slots=98304,
+        q_scale=(1.0 / math.sqrt(128.0)) if q_scale is None else q_scale, n_slots=131072,
         schedule_max_chunk=512)
     return Workload(spec, seed)
 
