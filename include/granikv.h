@@ -262,14 +262,16 @@ granikv_status granikv_plan_group(const granikv_plan* plan, int32_t i, granikv_g
  * prefix CTAs and of suffix CTAs it launches. */
 granikv_status granikv_plan_schedule(const granikv_plan* plan, int32_t* concurrent, int32_t* prefix_ctas,
                                      int32_t* suffix_ctas);
-/* The plan's suffix runs (token-CTA work lists, one KV-head group's; the generic suffix kernel:
- * its work items) and, of them, the tail runs: when the step runs as one grid in which every
- * prefix CTA is dense and the suffix side is estimated to end last, the last tail_runs runs
- * are taken by dense CTAs 0.. after their prefix piece (granikv_plan_schedule counts the
- * suffix CTAs launched, without them). */
+/* Diagnostics of the schedule (no counterpart in the paper).  The plan's suffix runs (token-CTA
+ * work lists, one KV-head group's; the generic suffix kernel: its work items) and, of them, the
+ * tail runs: when the step runs as one grid in which every prefix CTA is dense and the suffix
+ * side is estimated to end last, the last tail_runs runs are taken by dense CTAs 0.. after
+ * their prefix piece (granikv_plan_schedule counts the suffix CTAs launched, without them).
+ * Either output pointer may be NULL.  GRANIKV_ERR_INVALID for a plan not yet dispatched. */
 granikv_status granikv_plan_suffix_runs(const granikv_plan* plan, int32_t* runs, int32_t* tail_runs);
-/* The dense kernel's L2 read-ahead (in tiles, 0 for none) the plan's launches use; see
- * granikv_set_dense_l2_ahead. */
+/* Diagnostics (no counterpart in the paper): the dense kernel's L2 read-ahead (in tiles, 0 for
+ * none) the plan's launches use; see granikv_set_dense_l2_ahead.  GRANIKV_ERR_INVALID for a
+ * NULL output or a plan not yet dispatched. */
 granikv_status granikv_plan_dense_l2_ahead(const granikv_plan* plan, int32_t* tiles);
 /* Diagnostics (no counterpart in the paper): copy the plan's device image -- the work list that
  * granikv_decode_attention copies to the front of the workspace -- into host memory.  *size
@@ -297,12 +299,14 @@ granikv_status granikv_set_concurrency(granikv_ctx* ctx, int32_t on, float prefi
  * producer that finishes last merges the row.  Takes effect at the next granikv_dispatch. */
 granikv_status granikv_set_fused_merge(granikv_ctx* ctx, int32_t on);
 
-/* L2 read-ahead of the dense tensor-core prefix kernel: when a CTA refills a slot of its
- * shared-memory K (or V) ring with tile i of its prefix piece, it also requests tile i + tiles
- * into L2 (a bulk-tensor L2 prefetch: no data moves to the SM, results are unchanged).  -1 (the
- * default): two tiles when the step runs as one grid whose prefix side is estimated to finish
- * after its suffix side and whose suffix side reads at least as many bytes, else none; 0: never; 1-64: that many tiles for every dense decode
- * launch.  GRANIKV_ERR_INVALID outside [-1, 64].  Takes effect at the next granikv_dispatch. */
+/* Scheduling knob (no counterpart in the paper): L2 read-ahead of the dense tensor-core prefix
+ * kernel.  When a CTA refills a slot of its shared-memory K (or V) ring with tile i of its
+ * prefix piece, it also requests tile i + tiles into L2 (a bulk-tensor L2 prefetch: no data
+ * moves to the SM, results are unchanged).  -1 (the default): two tiles when the step runs as
+ * one grid whose prefix side is estimated to finish after its suffix side and whose suffix side
+ * reads at least as many bytes, else none; 0: never; 1-64: that many tiles for every dense
+ * decode launch.  GRANIKV_ERR_INVALID outside [-1, 64].  Takes effect at the next
+ * granikv_dispatch. */
 granikv_status granikv_set_dense_l2_ahead(granikv_ctx* ctx, int32_t tiles);
 
 granikv_status granikv_set_msat(granikv_ctx* ctx, int32_t m_sat);
