@@ -1198,13 +1198,13 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->concurrent = concurrent;
   // The dense CTAs of a split whose prefix side is estimated to end last, next to a suffix side
   // that reads at least as many bytes, read two tiles ahead into L2: their per-tile chain keeps
-  // few bytes in flight, and next to suffix CTAs that keep HBM busy they fall behind.  Measured on GB300 (Llama-3.1-8B shape, 16K prefix, B = 64, a
-  // 32-layer step): 42.7 -> 40.9 us a call with two tiles ahead, 41.0 / 41.1 / 41.4 us with
-  // three / four / five; on another box 43.2 -> 43.0 / 46.1 us with six / eight (further ahead
-  // takes the suffix side's bandwidth).  Where the suffix side ends last (Qwen-2.5 shape) it
-  // does not help; next to a light suffix side it costs (16K prefix, 256 COLD tokens a request:
-  // B = 1 17.7 -> 18.4 us, B = 8 18.9 -> 19.8 us); and with the kernels one after another
-  // (eight prefixes) six tiles ahead cost 17 %.
+  // few bytes in flight, and next to suffix CTAs that keep HBM busy they fall behind.  Measured
+  // on GB300 (Llama-3.1-8B shape, 16K prefix, B = 64, a 32-layer step): 42.7 -> 40.9 us a call
+  // with two tiles ahead, 41.0 / 41.1 / 41.4 us with three / four / five; on another GB300
+  // 43.2 -> 43.0 / 46.1 us with six / eight (further ahead takes the suffix side's bandwidth).
+  // Where the suffix side ends last (Qwen-2.5 shape) it does not help; next to a light suffix
+  // side it costs (16K prefix, 256 COLD tokens a request: B = 1 17.7 -> 18.4 us, B = 8 18.9 ->
+  // 19.8 us); and with the kernels one after another (eight prefixes) six tiles ahead cost 17 %.
   constexpr int32_t kAutoL2Ahead = 2;
   p->l2_ahead = c->l2_ahead >= 0 ? c->l2_ahead : (concurrent && read_ahead ? kAutoL2Ahead : 0);
   p->group_impl.resize(G);
