@@ -15,9 +15,10 @@
 // softmax (running max and sum per head column) reduces across lanes with warp shuffles.
 //
 // Work split: the plan cuts the concatenation of all requests' COLD tokens into one contiguous
-// run per token-CTA (stream-K style, cut on 16-token tile boundaries of each request), so every
-// CTA streams the same number of tiles; each
-// request segment inside a run writes one partial-state record.  A second index picks a group of
+// run per token-CTA (stream-K style, cut on 16-token tile boundaries of each request), so that
+// every CTA's tiles plus one tile per request segment come to the same count; each request
+// segment inside a run writes one partial-state record.  In one grid whose dense CTAs finish
+// early, the dense CTAs run the last runs after their prefix pieces.  A second index picks a group of
 // up to eight KV heads, whose K (and V) rows of one slot are contiguous in the pool (2 KB for
 // eight heads).
 //
