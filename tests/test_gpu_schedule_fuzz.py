@@ -73,3 +73,50 @@ def test_random_batches_match_the_oracle(cuda_ok, seed):
             f"schedule {plan.schedule()}, runs {plan.suffix_runs()}, read-ahead {plan.dense_l2_ahead()}")
     assert_close(o[sample], lse[sample], o_ref, lse_ref, "bf16", what)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def _case_f32(seed: int) -> W.Workload:
+    rng = np.random.default_rng(2000 + seed)
+    d = [32, 64, 96, 128, 160, 256][seed % 6]
+    n_kv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.integers(1, 9))
+    n_prefix = int(rng.integers(1, 3))
+    prefix_lens = [int(x) for x in rng.integers(16, 3000, size=n_prefix)]
+    B = int(rng.integers(1, 90))
+    req_prefix = [int(x) if rng.random() > 0.1 else -1 for x in rng.integers(0, n_prefix, size=B)]
+    suffix_lens = [int(x) for x in rng.integers(0, 300, size=B)]
+    for b in range(B):
+        if req_prefix[b] < 0 and suffix_lens[b] == 0:
+            suffix_lens[b] = 1
+    n_slots = max(int(math.ceil(sum(prefix_lens) / 0.2)), int(math.ceil(sum(suffix_lens) / 0.8))) + 2048
+    spec = W.WorkloadSpec(
+        name=f"fuzz_f32_{seed}", dtype="f32", n_q=n_kv * g, n_kv=n_kv, d=d, prefix_lens=prefix_lens,
+        req_prefix=req_prefix, suffix_lens=suffix_lens, q_scale=1.0, n_slots=n_slots,
+        schedule_max_chunk=int(rng.choice([1, 16, 64])))
+    return W.Workload(spec, seed)
+
+
+@pytest.mark.parametrize("seed", list(range(6)))
+def test_random_fp32_batches_match_the_oracle(cuda_ok, seed):
+    """fp32 pools of head sizes 32-256, 1-8 KV heads, GQA groups 1-8, both backends forced and
+    dispatched: the tf32 split-precision dense kernel (head sizes up to 128) and the CUDA-core
+    kernels hold the fp32 tolerance (1e-5) on sampled requests."""
+    from shared_prefix_kv_decode_gb300 import _binding as gb
+    from shared_prefix_kv_decode_gb300.workload_io import load_workload
+    from test_gpu_parity import assert_close
+
+    wl = _case_f32(seed)
+    lw = load_workload(wl)
+    ctx = lw.cache.ctx
+    B = wl.spec.B
+    rng = np.random.default_rng(seed)
+    sample = sorted({0, B - 1, *[int(x) for x in rng.integers(0, B, size=3)]})
+    o_ref, lse_ref = OA.decode_attention(wl, requests=sample)
+    for name, backend in (("auto", gb.BACKEND_AUTO), ("dense", gb.BACKEND_DENSE), ("cascade", gb.BACKEND_CASCADE)):
+        ctx.force_backend(backend)
+        o, lse = lw.cache.decode(0, lw.q, lw.batch)
+        ctx.sync_status(lw.cache.stream())
+        o = o.float().cpu().numpy().astype(np.float64)
+        lse = lse.cpu().numpy().astype(np.float64)
+        what = f"seed {seed} {name}: d {wl.spec.d}, n_kv {wl.spec.n_kv}, g {wl.spec.g}, B {B}, prefixes {wl.spec.prefix_lens}"
+        assert_close(o[sample], lse[sample], o_ref, lse_ref, "f32", what)
