@@ -305,9 +305,10 @@ cudaError_t launch_suffix_generic(int32_t dtype, const AttnParams& p, cudaStream
 // decode CTAs leave, spread over about 128 SMs rather than packed four to an SM on the first
 // ones freed, which measured 1.5-2 us shorter from the release to the end.  A one-warp merge
 // with more rows than two CTAs an SM hold at once (more than one wave) takes a build limited to
-// 80 registers, three CTAs an SM: Qwen-2.5 shape (5,120 rows) 83.0 -> 82.4 us a call, eight
-// prefixes 107.5 -> 106.8 us; with one wave the two-CTA build stays (the headline's 2,048 rows:
-// 38.7 against 39.2 us).
+// 64 registers, four CTAs an SM, six records a batch: Qwen-2.5 shape (5,120 rows) 83.0 -> 82.4
+// us a call with three CTAs an SM (80 registers), 80.8 -> 80.4 us more with four; eight prefixes
+// 107.5 -> 106.8 -> 106.9 us; with one wave the two-CTA build stays (the headline's 2,048 rows:
+// 38.7 against 39.2 us with three CTAs an SM).
 // Records per warp loaded together: one memory round trip for rows of up to W * kBatch records.
 template <int W>
 struct MergeCfg {
@@ -317,7 +318,7 @@ struct MergeCfg {
 
 template <int W, int kBlocks = MergeCfg<W>::kMinBlocks>
 __global__ void __launch_bounds__(256, kBlocks) merge_bf16_d128_kernel(AttnParams p) {
-  constexpr int kMergeBatch = MergeCfg<W>::kBatch;
+  constexpr int kMergeBatch = kBlocks >= 4 ? 6 : MergeCfg<W>::kBatch;  // 64 registers at four CTAs an SM
   constexpr int kRowsPerCta = 8 / W;
   __shared__ float4 s_acc[W > 1 ? 8 : 1][32];
   __shared__ float s_m[W > 1 ? 8 : 1], s_den[W > 1 ? 8 : 1];
@@ -418,7 +419,7 @@ cudaError_t launch_merge_w(const AttnParams& p, cudaStream_t s, bool pdl) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = prefer_max_shared(merge_bf16_d128_kernel<W>);
-    if (e == cudaSuccess && W == 1) e = prefer_max_shared(merge_bf16_d128_kernel<1, 3>);
+    if (e == cudaSuccess && W == 1) e = prefer_max_shared(merge_bf16_d128_kernel<1, 4>);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -430,7 +431,7 @@ cudaError_t launch_merge_w(const AttnParams& p, cudaStream_t s, bool pdl) {
     if (cudaGetDevice(&dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
         (int64_t)grid.x > 2LL * num_sms)
-      return launch_kernel(merge_bf16_d128_kernel<1, 3>, grid, dim3(256), 0, s, pdl, p);
+      return launch_kernel(merge_bf16_d128_kernel<1, 4>, grid, dim3(256), 0, s, pdl, p);
   }
   return launch_kernel(merge_bf16_d128_kernel<W>, grid, dim3(256), 0, s, pdl, p);
 }
