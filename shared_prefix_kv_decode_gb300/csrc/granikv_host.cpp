@@ -111,9 +111,8 @@ struct granikv_plan {
     std::vector<int32_t> slot_of_slab;  // slab id -> group, -1 between dispatches
     std::vector<int32_t> grp_slab, grp_count, req_group, begin, group_req, fill, scta_begin;
     std::vector<DevGroup> groups;
-    std::vector<DevReq> reqs;
-    std::vector<DevSuffixItem> sitems;
     std::vector<DevPrefixItem> pitems;
+    std::vector<int32_t> grp_np;          // prefix records of a request by its group + 1
     // What the last successful dispatch derived from the batch's slab ids alone (the groups,
     // their members, whether each group's requests are consecutive) and from the groups' shapes
     // alone (the prefix work items): a serving loop re-dispatches the same requests step after
@@ -303,6 +302,109 @@ void ws_forget(const void* ws) {
       g_ws_records.erase(g_ws_records.begin() + i);
       return;
     }
+}
+
+// The suffix's COLD tokens are counted in 16-token tiles per request; a segment (one request's
+// part of one token-CTA run) costs its CTA about one tile on top of its tiles.
+constexpr int64_t kSTile = 16;
+constexpr int64_t kSegTiles = 1;
+
+struct SuffixCut {
+  int32_t n_items = 0;         // suffix work items written
+  int32_t max_parts = 0;       // most records of one request
+  int64_t records = 0;         // records of the batch
+  int64_t prefix_records = 0;  // of them, prefix records
+};
+
+// Cuts the concatenation of the B requests' COLD tiles into n_scta token-CTA runs, run k ending
+// where the running count of tiles plus segment costs reaches share_end(k) (the first
+// n_scta - n_tail runs share U - U_tail equally, the last n_tail runs U_tail), cuts falling on
+// a request's tile boundaries.  Writes every request's record layout (np_of[rg[b]] prefix
+// records, then one per segment), one suffix item per segment and each run's first item
+// (scta_begin[0..n_scta]).  Out of line so that its loop's counters stay in registers.
+__attribute__((noinline)) SuffixCut cut_suffix_runs(int32_t B, const int32_t* __restrict__ np_of,
+                                                    const int32_t* __restrict__ rg,
+                                                    const int32_t* __restrict__ seq_len, int32_t n_scta,
+                                                    int32_t n_tail, int64_t U, int64_t U_tail,
+                                                    DevReq* __restrict__ reqs, DevSuffixItem* __restrict__ si,
+                                                    int32_t* __restrict__ scta_begin) {
+  const int32_t n_main = n_scta - n_tail;
+  auto share_end = [&](int64_t k) {
+    if (k < n_main) return (U - U_tail) * (k + 1) / n_main;
+    return (U - U_tail) + U_tail * (k - n_main + 1) / n_tail;
+  };
+  int32_t n_si = 0;
+  int64_t rec = 0;
+  int32_t cta = 0;
+  int64_t done = 0;         // tiles plus segment costs given to the CTAs so far
+  bool cta_open = false;    // the current CTA has a segment
+  int64_t end_cur = n_scta > 0 ? share_end(0) : 0;  // (one division per CTA, not per segment)
+  int32_t max_parts = 0;
+  int64_t n_prefix_records = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    DevReq& r = reqs[b];
+    const int32_t n_prefix = np_of[rg[b]];
+    const int32_t L = seq_len[b];
+    r.rec_base = (int32_t)rec;
+    r.n_prefix = n_prefix;
+    r.seq_len = L;
+    n_prefix_records += n_prefix;
+    int32_t k = 0;
+    const int64_t n_t = (L + kSTile - 1) / kSTile;
+    // the common case: the whole request fits the current run with room to spare (the loop
+    // below would take it in one segment and leave the run open)
+    if (n_t > 0 && (cta >= n_scta - 1 || end_cur - done - kSegTiles > n_t)) {
+      DevSuffixItem& it = si[n_si++];
+      it.b = b;
+      it.t0 = 0;
+      it.t1 = L;
+      it.rec = (int32_t)(rec + n_prefix);
+      done += kSegTiles + n_t;
+      cta_open = true;
+      r.n_parts = n_prefix + 1;
+      max_parts = std::max(max_parts, r.n_parts);
+      rec += r.n_parts;
+      continue;
+    }
+    for (int64_t t = 0; t < n_t;) {
+      const bool last_cta = cta >= n_scta - 1;
+      int64_t room = last_cta ? n_t - t : end_cur - done - kSegTiles;
+      if (room <= 0 && cta_open) {
+        // no tile more fits in this CTA: the request goes on in the next one
+        ++cta;
+        scta_begin[cta] = n_si;
+        cta_open = false;
+        end_cur = share_end(cta);
+        continue;
+      }
+      const int64_t take = std::min<int64_t>(n_t - t, std::max<int64_t>(room, 1));
+      DevSuffixItem& it = si[n_si++];
+      it.b = b;
+      it.t0 = (int32_t)(t * kSTile);
+      it.t1 = (int32_t)std::min<int64_t>((t + take) * kSTile, L);
+      it.rec = (int32_t)(rec + n_prefix + k);
+      ++k;
+      t += take;
+      done += kSegTiles + take;
+      cta_open = true;
+      if (!last_cta && done >= end_cur) {
+        ++cta;
+        scta_begin[cta] = n_si;
+        cta_open = false;
+        end_cur = share_end(cta);
+      }
+    }
+    r.n_parts = n_prefix + k;
+    max_parts = std::max(max_parts, r.n_parts);
+    rec += r.n_parts;
+  }
+  for (int32_t i = std::min(cta + 1, n_scta); i <= n_scta; ++i) scta_begin[i] = n_si;
+  SuffixCut out;
+  out.n_items = n_si;
+  out.max_parts = max_parts;
+  out.records = rec;
+  out.prefix_records = n_prefix_records;
+  return out;
 }
 
 }  // namespace
@@ -985,9 +1087,7 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   //    a segment against 0.6-0.7 us a tile; the segments of short requests also hold their
   //    recently appended tokens, whose slots are scattered), so the runs are cut where the
   //    running count of tiles plus segments reaches each CTA's equal share.
-  constexpr int64_t kSTile = 16;
   static_assert(kSTile == 16, "the tile count above uses 16-token tiles");
-  constexpr int64_t kSegTiles = 1;
   const int64_t T = T_tiles;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
   const int32_t suffix_impl = fast_suffix ? kImplSuffixMma : kImplGeneric;
@@ -1018,13 +1118,6 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
       U = T + kSegTiles * (n_sreq + n_scta - 1);
     }
   }
-  // cumulative share of tiles plus segment costs at the end of token-CTA run k: the suffix
-  // CTAs' runs share U - U_tail, the tail runs U_tail
-  const int32_t n_main = n_scta - n_tail;
-  auto share_end = [&](int64_t k) {
-    if (k < n_main) return (U - U_tail) * (k + 1) / n_main;
-    return (U - U_tail) + U_tail * (k - n_main + 1) / n_tail;
-  };
 
   // 5. records and work items
   std::vector<int32_t>& group_req = w.group_req;
@@ -1047,65 +1140,6 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
     DevGroup& dg = groups[i];
     if (dg.impl == kImplDenseTc && kDenseRows % g == 0 && w.grp_contig[i]) dg.q_b0 = group_req[dg.req_begin];
   }
-  std::vector<DevReq>& reqs = w.reqs;
-  reqs.resize(B);
-  std::vector<DevSuffixItem>& sitems = w.sitems;
-  std::vector<int32_t>& scta_begin = w.scta_begin;
-  scta_begin.assign(n_scta + 1, 0);
-  // at most one item per request plus one per token-CTA boundary
-  sitems.resize((size_t)B + n_scta + 1);
-  DevSuffixItem* si = sitems.data();
-  int32_t n_si = 0;
-  int64_t rec = 0;
-  int32_t cta = 0;
-  int64_t done = 0;         // tiles plus segment costs given to the CTAs so far
-  bool cta_open = false;    // the current CTA has a segment
-  int64_t end_cur = n_scta > 0 ? share_end(0) : 0;  // (one division per CTA, not per segment)
-  int32_t max_parts = 0;
-  for (int32_t b = 0; b < B; ++b) {
-    DevReq& r = reqs[b];
-    const int32_t n_prefix = req_group[b] >= 0 ? groups[req_group[b]].n_splits : 0;
-    const int32_t L = bt->seq_len[b];
-    r.rec_base = (int32_t)rec;
-    r.n_prefix = n_prefix;
-    r.seq_len = L;
-    int32_t k = 0;
-    const int64_t n_t = (L + kSTile - 1) / kSTile;
-    for (int64_t t = 0; t < n_t;) {
-      const bool last_cta = cta >= n_scta - 1;
-      int64_t room = last_cta ? n_t - t : end_cur - done - kSegTiles;
-      if (room <= 0 && cta_open) {
-        // no tile more fits in this CTA: the request goes on in the next one
-        ++cta;
-        scta_begin[cta] = n_si;
-        cta_open = false;
-        end_cur = share_end(cta);
-        continue;
-      }
-      const int64_t take = std::min<int64_t>(n_t - t, std::max<int64_t>(room, 1));
-      DevSuffixItem& it = si[n_si++];
-      it.b = b;
-      it.t0 = (int32_t)(t * kSTile);
-      it.t1 = (int32_t)std::min<int64_t>((t + take) * kSTile, L);
-      it.rec = (int32_t)(rec + n_prefix + k);
-      ++k;
-      t += take;
-      done += kSegTiles + take;
-      cta_open = true;
-      if (!last_cta && done >= end_cur) {
-        ++cta;
-        scta_begin[cta] = n_si;
-        cta_open = false;
-        end_cur = share_end(cta);
-      }
-    }
-    r.n_parts = n_prefix + k;
-    max_parts = std::max(max_parts, r.n_parts);
-    rec += r.n_parts;
-  }
-  sitems.resize(n_si);
-  for (int32_t i = std::min(cta + 1, n_scta); i <= n_scta; ++i) scta_begin[i] = n_si;
-  if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
   // prefix items grouped by kernel; within a group the row blocks of one (KV head, piece)
   // are adjacent so they share the piece's K/V through L2
   std::vector<DevPrefixItem>& pitems = w.pitems;
@@ -1146,40 +1180,65 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   }
   }
 
-  // 6. pack the device image: each array at a 16-byte boundary, the padding between them 0
-  struct Section {
-    const void* src;
-    size_t bytes;
-    size_t align;
-  };
-  const Section sections[] = {
-      {groups.data(), sizeof(DevGroup) * G, 16},
-      {group_req.data(), sizeof(int32_t) * group_req.size(), 16},
-      {reqs.data(), sizeof(DevReq) * B, 16},
-      {pitems.data(), sizeof(DevPrefixItem) * pitems.size(), 16},
-      {sitems.data(), sizeof(DevSuffixItem) * sitems.size(), 16},
-      {scta_begin.data(), sizeof(int32_t) * scta_begin.size(), 256},
-  };
-  size_t* const offs[] = {&p->off_groups, &p->off_group_req, &p->off_req, &p->off_pitems, &p->off_sitems, &p->off_scta};
-  size_t off = 0;
-  for (int k = 0; k < 6; ++k) {
-    *offs[k] = off;
-    off = align_up(off + sections[k].bytes, sections[k].align);
+
+  // The device image: groups, group members, requests, prefix items, suffix items, each
+  // token-CTA's first suffix item; each array at a 16-byte boundary, the padding between them
+  // 0, the whole a multiple of 256 bytes.  The requests and suffix items are written in place
+  // below (the suffix items' count, and so where the last array starts, is known at the end).
+  p->off_groups = 0;
+  p->off_group_req = align_up(sizeof(DevGroup) * G, 16);
+  p->off_req = align_up(p->off_group_req + sizeof(int32_t) * group_req.size(), 16);
+  p->off_pitems = align_up(p->off_req + sizeof(DevReq) * B, 16);
+  p->off_sitems = align_up(p->off_pitems + sizeof(DevPrefixItem) * pitems.size(), 16);
+  // at most one suffix item per request plus one per token-CTA boundary
+  const size_t max_sitems = (size_t)B + n_scta + 1;
+  p->blob.resize(align_up(p->off_sitems + sizeof(DevSuffixItem) * max_sitems + sizeof(int32_t) * (n_scta + 1), 256));
+  unsigned char* const img = p->blob.data();
+  DevReq* const reqs = reinterpret_cast<DevReq*>(img + p->off_req);
+  DevSuffixItem* const si = reinterpret_cast<DevSuffixItem*>(img + p->off_sitems);
+  std::vector<int32_t>& scta_begin = w.scta_begin;
+  scta_begin.assign(n_scta + 1, 0);
+  // the runs, each request's records and the suffix items
+  std::vector<int32_t>& grp_np = w.grp_np;
+  grp_np.resize((size_t)G + 1);
+  grp_np[0] = 0;
+  for (int32_t i = 0; i < G; ++i) grp_np[i + 1] = groups[i].n_splits;
+  const SuffixCut cut = cut_suffix_runs(B, grp_np.data() + 1, req_group.data(), bt->seq_len, n_scta, n_tail, U,
+                                        U_tail, reqs, si, scta_begin.data());
+  const int32_t n_si = cut.n_items;
+  const int32_t max_parts = cut.max_parts;
+  const int64_t rec = cut.records;
+  if (rec > (int64_t)INT32_MAX / 2) return GRANIKV_ERR_INVALID;
+  // 6. the rest of the device image
+  p->off_scta = align_up(p->off_sitems + sizeof(DevSuffixItem) * (size_t)n_si, 16);
+  const size_t img_end = align_up(p->off_scta + sizeof(int32_t) * scta_begin.size(), 256);
+  {
+    struct Part {
+      size_t off;
+      const void* src;  // NULL: written in place above
+      size_t bytes;
+      size_t next;      // where the next array starts
+    };
+    const Part parts[] = {
+        {p->off_groups, groups.data(), sizeof(DevGroup) * G, p->off_group_req},
+        {p->off_group_req, group_req.data(), sizeof(int32_t) * group_req.size(), p->off_req},
+        {p->off_req, nullptr, sizeof(DevReq) * B, p->off_pitems},
+        {p->off_pitems, pitems.data(), sizeof(DevPrefixItem) * pitems.size(), p->off_sitems},
+        {p->off_sitems, nullptr, sizeof(DevSuffixItem) * (size_t)n_si, p->off_scta},
+        {p->off_scta, scta_begin.data(), sizeof(int32_t) * scta_begin.size(), img_end},
+    };
+    for (const Part& pt : parts) {
+      if (pt.src && pt.bytes) std::memcpy(img + pt.off, pt.src, pt.bytes);
+      std::memset(img + pt.off + pt.bytes, 0, pt.next - pt.off - pt.bytes);
+    }
   }
-  p->blob.resize(off);
-  for (int k = 0; k < 6; ++k) {
-    unsigned char* dst = p->blob.data() + *offs[k];
-    if (sections[k].bytes) std::memcpy(dst, sections[k].src, sections[k].bytes);
-    const size_t end = k + 1 < 6 ? *offs[k + 1] : off;
-    std::memset(dst + sections[k].bytes, 0, end - *offs[k] - sections[k].bytes);
-  }
+  p->blob.resize(img_end);
   p->n_groups = G;
   p->n_pitems = (int32_t)pitems.size();
-  p->n_sitems = (int32_t)sitems.size();
+  p->n_sitems = n_si;
   p->B = B;
   p->n_records = (int32_t)rec;
-  p->n_prefix_records = 0;
-  for (int32_t b = 0; b < B; ++b) p->n_prefix_records += reqs[b].n_prefix;
+  p->n_prefix_records = cut.prefix_records;
   p->n_scta = n_scta;
   p->n_tail = n_tail;
   p->suffix_impl = suffix_impl;
@@ -1210,9 +1269,11 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   p->group_impl.resize(G);
   for (int32_t i = 0; i < G; ++i) p->group_impl[i] = groups[i].impl;
   // this dispatch succeeded: its groups and prefix items may serve the next one
-  w.cache_slab_id.assign(bt->slab_id, bt->slab_id + B);
-  w.cache_slab.resize(G);
-  for (int32_t i = 0; i < G; ++i) w.cache_slab[i] = c->slabs[grp_slab[i]];
+  if (!same_groups) {  // (else they hold these values already)
+    w.cache_slab_id.assign(bt->slab_id, bt->slab_id + B);
+    w.cache_slab.resize(G);
+    for (int32_t i = 0; i < G; ++i) w.cache_slab[i] = c->slabs[grp_slab[i]];
+  }
   w.groups_cached = true;
   w.pitems_cached = true;
   p->version++;
