@@ -316,12 +316,16 @@ struct SuffixCut {
   int64_t prefix_records = 0;  // of them, prefix records
 };
 
-// Cuts the concatenation of the B requests' COLD tiles into n_scta token-CTA runs, run k ending
-// where the running count of tiles plus segment costs reaches share_end(k) (the first
-// n_scta - n_tail runs share U - U_tail equally, the last n_tail runs U_tail), cuts falling on
-// a request's tile boundaries.  Writes every request's record layout (np_of[rg[b]] prefix
-// records, then one per segment), one suffix item per segment and each run's first item
-// (scta_begin[0..n_scta]).  Out of line so that its loop's counters stay in registers.
+// Cuts the concatenation of the B requests' COLD tiles into n_scta token-CTA runs, cuts falling
+// on a request's tile boundaries.  U is the batch's tiles plus segment costs when every cut is
+// counted as splitting a request (one more segment); the first n_scta - n_tail runs share
+// U - U_tail, the last n_tail runs U_tail.  Each run's target is set when it starts, as an equal
+// share of what is left: U less the units given out so far and less one for every cut so far
+// that fell between two requests (it added no segment), so that short requests, which most cuts
+// do not split, leave no run short at the end.  Writes every request's record layout
+// (np_of[rg[b]] prefix records, then one per segment), one suffix item per segment and each
+// run's first item (scta_begin[0..n_scta]).  Out of line so that its loop's counters stay in
+// registers.
 __attribute__((noinline)) SuffixCut cut_suffix_runs(int32_t B, const int32_t* __restrict__ np_of,
                                                     const int32_t* __restrict__ rg,
                                                     const int32_t* __restrict__ seq_len, int32_t n_scta,
@@ -329,16 +333,19 @@ __attribute__((noinline)) SuffixCut cut_suffix_runs(int32_t B, const int32_t* __
                                                     DevReq* __restrict__ reqs, DevSuffixItem* __restrict__ si,
                                                     int32_t* __restrict__ scta_begin) {
   const int32_t n_main = n_scta - n_tail;
-  auto share_end = [&](int64_t k) {
-    if (k < n_main) return (U - U_tail) * (k + 1) / n_main;
-    return (U - U_tail) + U_tail * (k - n_main + 1) / n_tail;
-  };
   int32_t n_si = 0;
   int64_t rec = 0;
   int32_t cta = 0;
   int64_t done = 0;         // tiles plus segment costs given to the CTAs so far
+  int64_t whole_cuts = 0;   // cuts so far that fell between two requests
   bool cta_open = false;    // the current CTA has a segment
-  int64_t end_cur = n_scta > 0 ? share_end(0) : 0;  // (one division per CTA, not per segment)
+  // where run k (starting now, at `done`) ends: one division per run, not per segment
+  auto run_end = [&](int64_t k) {
+    const int64_t left = U - done - whole_cuts;
+    if (k < n_main) return done + (left - U_tail) / (n_main - k);
+    return done + left / (n_scta - k);
+  };
+  int64_t end_cur = n_scta > 0 ? run_end(0) : 0;
   int32_t max_parts = 0;
   int64_t n_prefix_records = 0;
   for (int32_t b = 0; b < B; ++b) {
@@ -374,7 +381,8 @@ __attribute__((noinline)) SuffixCut cut_suffix_runs(int32_t B, const int32_t* __
         ++cta;
         scta_begin[cta] = n_si;
         cta_open = false;
-        end_cur = share_end(cta);
+        whole_cuts += t == 0 ? 1 : 0;
+        end_cur = run_end(cta);
         continue;
       }
       const int64_t take = std::min<int64_t>(n_t - t, std::max<int64_t>(room, 1));
@@ -391,7 +399,8 @@ __attribute__((noinline)) SuffixCut cut_suffix_runs(int32_t B, const int32_t* __
         ++cta;
         scta_begin[cta] = n_si;
         cta_open = false;
-        end_cur = share_end(cta);
+        whole_cuts += t == n_t ? 1 : 0;
+        end_cur = run_end(cta);
       }
     }
     r.n_parts = n_prefix + k;
@@ -1085,8 +1094,8 @@ granikv_status granikv_dispatch(granikv_ctx* c, const granikv_batch* bt, granikv
   //    tile boundaries of the request.  A segment costs its CTA about one tile on top of its
   //    tiles (measured on GB300, Llama-3.1-8B shape, 88 token-CTAs of 22-23 tiles: 0.54-0.76 us
   //    a segment against 0.6-0.7 us a tile; the segments of short requests also hold their
-  //    recently appended tokens, whose slots are scattered), so the runs are cut where the
-  //    running count of tiles plus segments reaches each CTA's equal share.
+  //    recently appended tokens, whose slots are scattered), so each run ends where its tiles
+  //    plus segments reach an equal share of what is left when it starts (cut_suffix_runs).
   static_assert(kSTile == 16, "the tile count above uses 16-token tiles");
   const int64_t T = T_tiles;
   const bool fast_suffix = c->cfg.dtype == GRANIKV_DTYPE_BF16 && c->cfg.head_dim == 128 && g <= 8;
