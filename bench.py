@@ -60,6 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--prefix-share", type=float, default=0.0,
                     help="share of the SMs the prefix work list is sized for when running concurrently "
                          "(0: the library's automatic share)")
+    ap.add_argument("--fused-merge", action="store_true",
+                    help="merge each row in the producer that finishes it last (no merge kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused-append", action="store_true",
                     help="append each layer's new K/V with its own launch before the attention call")
@@ -347,6 +349,7 @@ def run_granikv(args):
                        "cascade": gb.BACKEND_CASCADE}[args.backend])
     ctx.set_checks(True)
     ctx.set_concurrency(not args.serial, args.prefix_share)
+    ctx.set_fused_merge(args.fused_merge)
     stream = torch.cuda.current_stream(dev)
     # A step's inputs (q, new K, new V of every layer) live in one device buffer and its outputs
     # (o, lse of every layer) in another, so the end-to-end run moves each direction with one
@@ -521,6 +524,7 @@ def run_granikv(args):
                    "append": "fused into the attention launch" if fused else "own launch per layer",
                    "schedule": dict(plan.schedule(), dense_l2_ahead=plan.dense_l2_ahead()),
                    "concurrency": "serial" if args.serial else f"prefix share {args.prefix_share}",
+                   "merge": "by the last producer of each row" if args.fused_merge else "merge kernel",
                    "groups": [{"m_eff": g["m_eff"], "backend": gb.BACKEND_NAMES[g["backend"]],
                                "n_splits": g["n_splits"]} for g in groups],
                    "l2": (f"inputs larger than L2: each step reads {L} distinct layers' pools, "
